@@ -1,0 +1,464 @@
+"""Benchmark of the TBE hot path on GB300: forward + backward (transpose, sort,
+run-length encoding, segment reduction, fused optimizer update) per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 2] [--index-dtype int64] [--no-e2e] [--no-cpu-baseline]
+
+Prints one JSON line on rank 0.  The default workload is the 8-table fp32
+config (T=8, 1M rows x 128, B=8192, Poisson(20) bags, Zipf(1.05) indices, SGD).
+Timing: CUDA events on the launching stream around each step, L2 flushed
+(256 MiB write) before every step outside the timed interval, W untimed
+warm-up steps, barrier + synchronize around the K timed steps, max over ranks.
+Under torchrun every rank runs its own replica (the path does not shard:
+weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+ELEM = {"f32": 4, "f16": 2, "bf16": 2}
+METRIC = "TBE fwd / fwd+bwd+update lookups/sec and HBM GB/s (% of GB300 roofline), 1 GPU"
+KERNEL_FILES = {
+    "forward": "recommender_sparse_embeddings_gb300/csrc/forward.cu",
+    "prepare": "recommender_sparse_embeddings_gb300/csrc/prepare.cu",
+    "apply": "recommender_sparse_embeddings_gb300/csrc/apply.cu",
+}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_max(value: float, device) -> float:
+    """Max of a host float over all ranks (identity when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device) -> float:
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(specs, batch_lengths, N, B, T, idx_bytes, weights, optimizer, U, passes):
+    """Algorithmic bytes per step, by segment (the formula stated with the
+    workload: gathered rows, indices/offsets/weights, outputs; backward adds
+    the gradient rows gathered per lookup, the sort traffic and the
+    read-modify-write of unique rows and optimizer state)."""
+    per_table_lookups = batch_lengths.view(T, B).sum(1).tolist()
+    gathered = sum(n * s.dim * ELEM[s.dtype] for n, s in zip(per_table_lookups, specs))
+    total_d = sum(s.dim for s in specs)
+    out_bytes = B * total_d * 4
+    fwd = gathered + N * idx_bytes + (T * B + 1) * idx_bytes + (N * 4 if weights else 0) + out_bytes
+    # transpose + sort + run-length: index/offset reads, key/bag (+scale) writes,
+    # each radix pass reads and writes (key, value), run-length reads keys and
+    # writes (uniq, runstart)
+    scale = 4 if weights else 0
+    prep = (N * idx_bytes + (T * B + 1) * idx_bytes + N * (4 + 4 + scale)
+            + passes * N * 16 - N * 4 + N * 4 + U * 8)
+    grad_rows = sum(n * s.dim * 4 for n, s in zip(per_table_lookups, specs))
+    avg_row = sum(s.dim * ELEM[s.dtype] for s in specs) / len(specs)
+    apply = grad_rows + N * (4 + 4 + scale) + U * 8 + 2 * U * avg_row + (
+        2 * U * 4 if optimizer == "adagrad" else 0)
+    return dict(forward=fwd, prepare=prep, apply=apply, step=fwd + prep + apply)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- profile
+
+def profile_traffic(segment: str):
+    """DRAM bytes per launch of a segment's main kernel, from the committed ncu
+    summary, or None if there is none or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{segment}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    src = os.path.join(ROOT, KERNEL_FILES[segment])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
+        return None
+    return float(m.group(1))
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+# ------------------------------------------------------------ CPU baseline
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle (as it stands): the
+    first `tables_in_sample` tables with the full B and the same laws.  One
+    step = oracle forward + oracle backward (with the workload's optimizer)."""
+
+    def __init__(self, cfg, tables_in_sample: int = 2):
+        import numpy as np
+
+        self.cfg = cfg
+        specs = workloads.realize_tables(cfg)[:tables_in_sample]
+        tabs_t = workloads.make_tables(cfg, "cpu", specs)
+        batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
+        self.names = [s.dtype for s in specs]
+        self.tabs = [t.numpy() if t.dtype == torch.float32
+                     else t.view(torch.int16).numpy().view(np.uint16) for t in tabs_t]
+        self.ind, self.off = batch.indices.numpy(), batch.offsets.numpy()
+        self.w = None if batch.weights is None else batch.weights.numpy()
+        self.g = workloads.make_grad(cfg, "cpu", specs).numpy()
+        self.state = (np.zeros(sum(s.rows for s in specs), np.float32)
+                      if cfg.optimizer == "adagrad" else None)
+        self.N = batch.N
+        self.sample = (f"{tables_in_sample} of {len(workloads.realize_tables(cfg))} tables, "
+                       f"B={cfg.B}, {batch.N} lookups per fwd+bwd step, one core")
+
+    def step(self) -> float:
+        import oracle
+
+        c = self.cfg
+        t0 = time.perf_counter()
+        oracle.forward(self.tabs, self.names, self.ind, self.off, c.B, weights=self.w,
+                       pooling=c.pooling)
+        oracle.backward(self.tabs, self.names, self.ind, self.off, c.B, self.g, c.optimizer, c.lr,
+                        eps=c.eps, weights=self.w, pooling=c.pooling, state=self.state)
+        return time.perf_counter() - t0
+
+
+def cpu_oracle_run(cfg, seconds: float = 10.0):
+    s = OracleSample(cfg)
+    steps, el = 0, 0.0
+    while steps == 0 or el < seconds:
+        el += s.step()
+        steps += 1
+    return {"lookups": s.N * steps, "seconds": el, "steps": steps,
+            "sample": s.sample + f", {steps} steps"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import recommender_sparse_embeddings_gb300 as tbe
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    cfg = workloads.get_config(args.config)
+    specs = workloads.realize_tables(cfg)
+    idx_dtype = torch.int64 if args.index_dtype == "int64" else torch.int32
+    tables = workloads.make_tables(cfg, dev, specs)
+    batch = workloads.make_batch(cfg, dev, idx_dtype, specs)
+    grad = workloads.make_grad(cfg, dev, specs)
+    T, B, N = len(specs), cfg.B, batch.N
+    h = tbe.tbe_create(tables, cfg.pooling)
+    ws = tbe.make_workspace(h, N, B, dev)
+    out = torch.empty((B, h.total_dim), dtype=torch.float32, device=dev)
+    state = (torch.zeros(h.total_rows, dtype=torch.float32, device=dev)
+             if cfg.optimizer == "adagrad" else None)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ind, off, w = batch.indices, batch.offsets, batch.weights
+
+    def fwd():
+        tbe.tbe_forward(h, ind, off, B, w, out)
+
+    def prep():
+        tbe.tbe_backward_prepare(h, ind, off, B, ws, w)
+
+    def apply(g=grad):
+        tbe.tbe_backward_apply(h, N, B, g, ws, cfg.optimizer, cfg.lr, cfg.eps, state)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd(); prep(); apply()
+    torch.cuda.synchronize()
+    rc = tbe.tbe_get_error(h)
+    if rc != tbe.TBE_OK:
+        raise RuntimeError(f"device error during warm-up: {tbe.tbe_strerror(rc)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            e = ev[k]
+            e[0].record(stream); fwd()
+            e[1].record(stream); prep()
+            e[2].record(stream); apply()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    seg = {"forward": 0.0, "prepare": 0.0, "apply": 0.0}
+    for e in ev:
+        seg["forward"] += e[0].elapsed_time(e[1])
+        seg["prepare"] += e[1].elapsed_time(e[2])
+        seg["apply"] += e[2].elapsed_time(e[3])
+    local_ms = sum(seg.values())
+    total_ms = reduce_max(local_ms, dev)
+    units = reduce_sum(float(N) * args.steps, dev)
+    rc = tbe.tbe_get_error(h)
+    if rc != tbe.TBE_OK:
+        raise RuntimeError(f"device error in timed region: {tbe.tbe_strerror(rc)}")
+
+    # U (distinct keys) for the byte count: read once after the run
+    lay = tbe.tbe_backward_workspace_layout(h, N, B)
+    U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
+    passes = (max(1, (h.total_rows).bit_length()) + 7) // 8
+    nbytes = algorithmic_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize, w is not None,
+                               cfg.optimizer, U, passes)
+    ms_step = total_ms / args.steps
+    value = units / (total_ms / 1e3)
+    peak, peak_src = measured_hbm_peak()
+    seg_ms = {k: v / args.steps for k, v in seg.items()}
+    dominant = max(seg_ms, key=seg_ms.get)
+    achieved = nbytes[dominant] / (seg_ms[dominant] / 1e3) / 1e9
+    launches_per_step = 2 + (2 + passes) + 2  # fwd pool+long, keys+passes+rle, short+chunks
+
+    # end-to-end through the public API: inputs from pinned host memory every
+    # step, pooled output read back every step
+    e2e = None
+    if not args.no_e2e:
+        h_ind = ind.cpu().pin_memory()
+        h_off = off.cpu().pin_memory()
+        h_w = None if w is None else w.cpu().pin_memory()
+        h_grad = grad.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d_ind, d_off = torch.empty_like(ind), torch.empty_like(off)
+        d_w = None if w is None else torch.empty_like(w)
+        d_grad = torch.empty_like(grad)
+
+        def e2e_step():
+            d_ind.copy_(h_ind, non_blocking=True)
+            d_off.copy_(h_off, non_blocking=True)
+            if d_w is not None:
+                d_w.copy_(h_w, non_blocking=True)
+            d_grad.copy_(h_grad, non_blocking=True)
+            tbe.tbe_forward(h, d_ind, d_off, B, d_w, out)
+            h_out.copy_(out, non_blocking=True)
+            tbe.tbe_backward_prepare(h, d_ind, d_off, B, ws, d_w)
+            tbe.tbe_backward_apply(h, N, B, d_grad, ws, cfg.optimizer, cfg.lr, cfg.eps, state)
+
+        for _ in range(max(1, args.warmup)):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()
+            ev2[k][0].record(stream)
+            e2e_step()
+            ev2[k][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev2), dev)
+        h2d = ind.numel() * ind.element_size() + off.numel() * off.element_size() + \
+            (0 if w is None else w.numel() * 4) + grad.numel() * 4
+        e2e = {"value": units / (e2e_ms / 1e3), "unit": "lookups/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": out.numel() * 4, "ms_per_step": e2e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = cpu_oracle_run(cfg, seconds=args.cpu_seconds)
+        cpu = {"value": r["lookups"] / r["seconds"], "unit": "lookups/s", "cores": 1,
+               "kind": "oracle", "sample": r["sample"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "lookups/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32" if all(s.dtype == "f32" for s in specs) else "mixed(f32 accumulate)",
+            "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
+                    "pages' production shard configurations)",
+            "config": {"workload": cfg.description, "config_id": cfg.cfg_id, "T": T, "B": B,
+                       "N_lookups": N, "unique_rows": U, "index_dtype": args.index_dtype,
+                       "optimizer": cfg.optimizer, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
+            "fwd": {"lookups_per_s": units / (reduce_max(seg["forward"], dev) / 1e3),
+                    "gbs": nbytes["forward"] / (seg_ms["forward"] / 1e3) / 1e9,
+                    "frac": nbytes["forward"] / (seg_ms["forward"] / 1e3) / 1e9 / peak},
+            "step_gbs": nbytes["step"] / (ms_step / 1e3) / 1e9,
+            "segments_ms": seg_ms,
+            "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profile_traffic(dominant),
+                         "kernel": dominant, "peak_source": peak_src},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = workloads.get_config(args.config)
+    sample = OracleSample(cfg)
+    for _ in range(args.warmup):
+        sample.step()
+    total_s = sum(sample.step() for _ in range(args.steps))
+    value = sample.N * args.steps / total_s
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "lookups/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 accumulate",
+        "data": "synthetic: seeded generators with the workload's laws",
+        "config": {"workload": cfg.description, "config_id": cfg.cfg_id,
+                   "reference": "CPU oracle (plain C, one core); the pages ship no "
+                                "implementation to run"},
+        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+                         "sample": sample.sample},
+        "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--index-dtype", choices=["int64", "int32"], default="int64")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = p.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least three warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * tbe.h: C ABI of the GB300 (sm_103a) table-batched embedding library.
+ *
+ * A table-batched embedding (TBE) holds T embedding tables and, in one call,
+ * looks up and pools a batch of sparse indices across all of them (forward),
+ * then scatters the upstream gradient back to the looked-up rows with exactly
+ * one optimizer update per touched (table, row) (backward).
+ *
+ * Sources (web pages on FBTriton table-batched embeddings):
+ *  - "Optimizing Recommendation Systems with FBTriton Table Batched
+ *    Embeddings", "Implementation Guide: Integrating TBE": the forward call
+ *    takes the tables, a flat index list and an offsets list (CSR layout).
+ *  - "FBTriton Rewrites Table Batched Embedding", "Responsibilities of the
+ *    forward and backward passes": gather + aggregate per sample; scatter the
+ *    upstream gradient back and accumulate repeated rows.
+ *  - kimbodo "What Happened": pooling across tables in one launch, per-sample
+ *    weights, higher-precision accumulation, a histogram + tensor-core path
+ *    for eligible small tables; backward grouped by (table, row) with one
+ *    optimizer update per row, a streaming path for short runs and gradient
+ *    accumulation for runs of at least 256 lookups.
+ *  - kimbodo "Kimbodo Engineering Perspective": transpose, sort and
+ *    run-length encoding are the backward's preparation steps, and can be run
+ *    ahead of time (during forward).
+ *
+ * Conventions for every call below
+ *  - Pointers marked "device" are CUDA device pointers of the current device;
+ *    pointers marked "host" are ordinary host memory.  The library never
+ *    takes ownership of caller memory and never allocates per call; the only
+ *    allocation is the small descriptor block that tbe_create makes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on that stream and performs no host
+ *    synchronisation, except tbe_get_error.
+ *  - A handle must not be used from two host threads, or on two streams whose
+ *    work overlaps, at the same time.
+ *  - Return value: TBE_OK (0) or a negative TBE_ERR_* code.  Argument errors
+ *    are reported synchronously and nothing is launched.  Problems only the
+ *    GPU can see (an index out of range, malformed offsets, a bounded wait
+ *    that ran out) raise a sticky flag in the handle that tbe_get_error reads.
+ *
+ * Batch layout (CSR, table-major): B bags per table; bag b of table t is flat
+ * bag t*B+b, and its lookups are indices[offsets[t*B+b] .. offsets[t*B+b+1]).
+ * `offsets` has T*B+1 entries, starts at 0, never decreases and ends at N.
+ * indices and offsets share one integer type (int32 or int64).  An index
+ * outside [0, rows_t) is skipped (contributes nothing, updates nothing) and
+ * raises TBE_ERR_INDEX_OOB.
+ *
+ * Pooled output and upstream gradient: fp32 row-major [B, sum_t dim_t];
+ * table t owns columns [Doff_t, Doff_t + dim_t), Doff_t = sum of the dims of
+ * the tables before t.  Scale of lookup i: s_i = w_i (per-sample weight, or
+ * 1 without weights), times 1/L for mean pooling (L = the bag's CSR length);
+ * an empty bag pools to 0.
+ *
+ * Limits: sum of all tables' rows < 2^32 - 1; every table's rows < 2^31;
+ * N < 2^30 lookups per call; T*B < 2^31; dim in [1, 4096].
+ */
+#ifndef TBE_GB300_H
+#define TBE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define TBE_OK 0
+#define TBE_ERR_INVALID_ARG -1         /* null pointer, bad size, bad enum */
+#define TBE_ERR_UNSUPPORTED -2         /* outside the limits listed above */
+#define TBE_ERR_WORKSPACE_TOO_SMALL -3 /* workspace_bytes below the query */
+#define TBE_ERR_CUDA -4                /* a CUDA runtime call failed */
+#define TBE_ERR_INDEX_OOB -5           /* device: an index outside [0, rows) */
+#define TBE_ERR_BAD_OFFSETS -6         /* device: offsets not 0..N monotone */
+#define TBE_ERR_TIMEOUT -7             /* device: a bounded inter-CTA wait ran out */
+#define TBE_ERR_NO_MEMORY -8           /* tbe_create could not allocate */
+
+/* ------------------------------------------------------------------- enums */
+typedef enum { TBE_F32 = 0, TBE_F16 = 1, TBE_BF16 = 2 } tbe_dtype;
+typedef enum { TBE_I32 = 0, TBE_I64 = 1 } tbe_index_dtype;
+typedef enum { TBE_POOL_SUM = 0, TBE_POOL_MEAN = 1 } tbe_pooling;
+typedef enum { TBE_OPT_SGD = 1, TBE_OPT_ROWWISE_ADAGRAD = 2 } tbe_optimizer_kind;
+
+/* tbe_create flags */
+#define TBE_FLAG_NO_HISTOGRAM 0x1u    /* never use the small-table tensor-core path */
+#define TBE_FLAG_FORCE_HISTOGRAM 0x2u /* use it for every eligible table */
+
+/* One embedding table.  data: device, row-major rows x dim of dtype,
+ * caller-owned, read by forward and updated in place by backward.  The
+ * fastest path wants data 16-byte aligned and dim*sizeof(dtype) a multiple of
+ * 16; other shapes run on a slower element-wise path. */
+typedef struct {
+    int64_t rows;
+    int32_t dim;
+    int32_t dtype; /* tbe_dtype */
+    void* data;
+} tbe_table;
+
+/* Optimizer applied once per touched row by the backward calls.
+ *  SGD:               w <- w - lr * g
+ *  row-wise Adagrad:  m <- m + mean_j g_j^2 ;  w_j <- w_j - lr * g_j / (sqrt(m) + eps)
+ * with g the row's summed gradient in fp32 and one round-to-nearest-even to
+ * the table's dtype.  state: device fp32 [sum of rows], row r of table t at
+ * rowbase_t + r (rowbase_t = rows of the tables before t), caller-owned,
+ * zero-initialised by the caller; unused by SGD. */
+typedef struct {
+    int32_t kind; /* tbe_optimizer_kind */
+    float lr;
+    float eps;
+    float* state;
+} tbe_optimizer;
+
+typedef struct tbe_handle tbe_handle;
+
+/* Byte offsets, inside a backward workspace, of the arrays the preparation
+ * step (transpose, sort, run-length encoding) leaves there.  All arrays are
+ * uint32.  sorted_keys/sorted_pos: N entries (key = rowbase_t + row, or
+ * sum-of-rows for a skipped lookup; pos = the lookup's position in indices),
+ * stably sorted by key.  uniq: the distinct keys ascending; runstart: the
+ * first sorted slot of each (runstart[U] = N); num_unique: one entry, U. */
+typedef struct {
+    uint64_t sorted_keys;
+    uint64_t sorted_pos;
+    uint64_t uniq;
+    uint64_t runstart;
+    uint64_t num_unique;
+    uint64_t total_bytes;
+} tbe_ws_layout;
+
+/* ------------------------------------------------------------------ handle */
+
+/* Validates the table list and builds the device descriptor block (row
+ * bases, column offsets, per-table lookup schedule).  `tables`: host array
+ * of num_tables entries (copied; the data pointers are kept).  pooling:
+ * tbe_pooling.  flags: TBE_FLAG_*.  On success *out receives the handle.
+ * Errors: INVALID_ARG (null/zero/negative sizes, bad enums), UNSUPPORTED
+ * (limits), CUDA, NO_MEMORY. */
+int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uint32_t flags,
+               tbe_handle** out);
+
+/* Frees the descriptor block.  The caller's memory is untouched.  Must not be
+ * called while work that uses the handle may still run. */
+void tbe_destroy(tbe_handle* h);
+
+/* ----------------------------------------------------------------- forward */
+
+/* Pooled lookup of all T*B bags in one pass (forward of the kimbodo "What
+ * Happened" section; CSR call of the integration guide).
+ *  indices: device [num_indices] of index_dtype; offsets: device [T*B+1];
+ *  per_sample_weights: device fp32 [num_indices] or NULL;
+ *  out: device fp32 [batch_size, sum of dims], fully overwritten.
+ * Accumulation is fp32 for every table dtype. */
+int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                float* out, void* stream);
+
+/* ---------------------------------------------------------------- backward */
+
+/* Bytes of device workspace the backward calls need for this batch shape. */
+size_t tbe_backward_workspace_bytes(const tbe_handle* h, int64_t num_indices, int32_t batch_size);
+
+/* Where the preparation step leaves its arrays inside the workspace. */
+int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int32_t batch_size,
+                                  tbe_ws_layout* out);
+
+/* Backward preparation only (kimbodo "Kimbodo Engineering Perspective"):
+ * transpose the batch into one (table,row) key per lookup, radix-sort the
+ * keys stably, run-length encode them.  Results stay in `workspace` (device,
+ * caller-owned, at least tbe_backward_workspace_bytes) for
+ * tbe_backward_apply.  Depends only on indices, offsets and weights, so it
+ * may run as soon as the batch is known, e.g. beside the forward pass. */
+int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets,
+                         int32_t index_dtype, int64_t num_indices, int32_t batch_size,
+                         const float* per_sample_weights, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Backward from a prepared workspace: per unique (table,row) sums
+ * s_i * grad_out[bag_i, Doff_t : Doff_t+dim_t] in fp32 (runs of fewer than 256
+ * lookups stream through one warp; longer runs are split into 256-lookup
+ * chunks whose partial sums are added in a fixed order), then applies the
+ * optimizer once to that row.  grad_out: device fp32 [batch_size, sum of
+ * dims].  num_indices and batch_size must equal the prepare call's. */
+int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size,
+                       const float* grad_out, const tbe_optimizer* opt, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* prepare + apply with SGD. */
+int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                     int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                     const float* grad_out, float lr, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* prepare + apply with row-wise Adagrad (state as in tbe_optimizer). */
+int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void* offsets,
+                                 int32_t index_dtype, int64_t num_indices, int32_t batch_size,
+                                 const float* per_sample_weights, const float* grad_out,
+                                 float* state, float lr, float eps, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- diagnostics */
+
+/* Synchronises `stream`, returns the first device-detected error since the
+ * last call (TBE_ERR_TIMEOUT before TBE_ERR_BAD_OFFSETS before
+ * TBE_ERR_INDEX_OOB) or TBE_OK, and clears it. */
+int tbe_get_error(tbe_handle* h, void* stream);
+
+/* Static description of a status code. */
+const char* tbe_strerror(int code);
+
+/* Per-table schedule chosen at create time, for tests and tuning:
+ * out_path[t] = 0 gather path (vector), 1 gather path (element-wise),
+ * 2 histogram tensor-core path. */
+int tbe_table_paths(const tbe_handle* h, int32_t* out_path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TBE_GB300_H */

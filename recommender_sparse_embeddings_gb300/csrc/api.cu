@@ -1,0 +1,437 @@
+// C ABI of the TBE library: argument checks, the handle's descriptor block,
+// the backward workspace layout, and the order of kernel launches.  The
+// declarations and their contracts are in include/tbe.h.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/tbe.h"
+#include "tbe_internal.cuh"
+
+namespace tbe {
+cudaError_t launch_forward_schedule(TableDesc* tabs, int T, int B, cudaStream_t s);
+}
+
+using namespace tbe;
+
+struct tbe_handle {
+    int device = 0;
+    int T = 0;
+    int pooling = 0;
+    uint32_t flags = 0;
+    int num_sms = 0;
+    std::vector<TableDesc> tabs;
+    void* dev = nullptr;          // DevBlock followed by TableDesc[T]
+    DevBlock* blk = nullptr;
+    TableDesc* dtabs = nullptr;
+    int total_d = 0;
+    int max_dim = 0;
+    uint64_t total_rows = 0;
+    int key_bits = 1;
+    int passes = 1;
+    int last_B = -1;
+    int parity = 0;
+    int vec_out = 0;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+size_t tabs_offset() { return align_up(sizeof(DevBlock)); }
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+struct Layout {
+    size_t counters, hist, status, rle_status, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
+        long_runs, chunk_run, partial, total;
+    size_t zero_bytes;  // counters..rle_status are zeroed per call
+    int64_t max_long, max_chunks;
+    int tiles;
+};
+
+Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
+    Layout L{};
+    const int64_t n = std::max<int64_t>(N, 1);
+    L.tiles = (int)((N + kSortTile - 1) / kSortTile);
+    L.max_long = N / kLongRun + 1;
+    L.max_chunks = 2 * (N / kLongRun) + 2;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.counters = take(sizeof(uint32_t) * CTR_COUNT);
+    L.hist = take(sizeof(uint32_t) * kMaxPasses * kRadix);
+    L.status = take(sizeof(uint32_t) * (size_t)h->passes * std::max(L.tiles, 1) * kRadix);
+    L.rle_status = take(sizeof(uint32_t) * std::max(L.tiles, 1));
+    L.zero_bytes = o;
+    L.keys0 = take(sizeof(uint32_t) * n);
+    L.keys1 = take(sizeof(uint32_t) * n);
+    L.vals0 = take(sizeof(uint32_t) * n);
+    L.vals1 = take(sizeof(uint32_t) * n);
+    L.bag = take(sizeof(uint32_t) * n);
+    L.scale = scale ? take(sizeof(float) * n) : 0;
+    L.uniq = take(sizeof(uint32_t) * n);
+    L.runstart = take(sizeof(uint32_t) * (n + 1));
+    L.long_runs = take(sizeof(uint32_t) * 4 * L.max_long);
+    L.chunk_run = take(sizeof(uint32_t) * L.max_chunks);
+    L.partial = take(sizeof(float) * (size_t)L.max_chunks * h->max_dim);
+    L.total = o;
+    return L;
+}
+
+bool needs_scale(const tbe_handle* h, const float* weights) {
+    return weights != nullptr || h->pooling == TBE_POOL_MEAN;
+}
+
+Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
+    char* p = static_cast<char*>(base);
+    Workspace w{};
+    w.counters = reinterpret_cast<uint32_t*>(p + L.counters);
+    w.hist = reinterpret_cast<uint32_t*>(p + L.hist);
+    w.status = reinterpret_cast<uint32_t*>(p + L.status);
+    w.rle_status = reinterpret_cast<uint32_t*>(p + L.rle_status);
+    w.keys[0] = reinterpret_cast<uint32_t*>(p + L.keys0);
+    w.keys[1] = reinterpret_cast<uint32_t*>(p + L.keys1);
+    w.vals[0] = reinterpret_cast<uint32_t*>(p + L.vals0);
+    w.vals[1] = reinterpret_cast<uint32_t*>(p + L.vals1);
+    w.bag = reinterpret_cast<uint32_t*>(p + L.bag);
+    w.scale = scale ? reinterpret_cast<float*>(p + L.scale) : nullptr;
+    w.uniq = reinterpret_cast<uint32_t*>(p + L.uniq);
+    w.runstart = reinterpret_cast<uint32_t*>(p + L.runstart);
+    w.long_runs = reinterpret_cast<uint32_t*>(p + L.long_runs);
+    w.chunk_run = reinterpret_cast<uint32_t*>(p + L.chunk_run);
+    w.partial = reinterpret_cast<float*>(p + L.partial);
+    w.max_long = L.max_long;
+    w.max_chunks = L.max_chunks;
+    w.tiles = L.tiles;
+    w.passes = h->passes;
+    // the sort ping-pongs once per pass, starting from buffer 0
+    w.sorted_buf = h->passes % 2;
+    return w;
+}
+
+// The scale array exists whenever weights or mean pooling are in play; the
+// workspace is always laid out with room for it so its size only depends on
+// the batch shape.
+constexpr bool kLayoutWithScale = true;
+
+int check_batch(const tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                int64_t N, int32_t B) {
+    if (!h) return TBE_ERR_INVALID_ARG;
+    if (index_dtype != TBE_I32 && index_dtype != TBE_I64) return TBE_ERR_INVALID_ARG;
+    if (N < 0 || B < 0) return TBE_ERR_INVALID_ARG;
+    if (N >= (int64_t(1) << 30)) return TBE_ERR_UNSUPPORTED;
+    if ((int64_t)h->T * B >= (int64_t(1) << 31)) return TBE_ERR_UNSUPPORTED;
+    if (!offsets) return TBE_ERR_INVALID_ARG;
+    if (N > 0 && !indices) return TBE_ERR_INVALID_ARG;
+    if (B == 0 && N > 0) return TBE_ERR_INVALID_ARG;
+    return TBE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? TBE_OK : TBE_ERR_CUDA; }
+
+int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
+    if (B == h->last_B) return TBE_OK;
+    cudaError_t e = launch_forward_schedule(h->dtabs, h->T, B, s);
+    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    h->last_B = B;
+    return TBE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uint32_t flags,
+               tbe_handle** out) {
+    if (!out) return TBE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
+    if (pooling != TBE_POOL_SUM && pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
+    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM)) return TBE_ERR_INVALID_ARG;
+    tbe_handle* h = new (std::nothrow) tbe_handle();
+    if (!h) return TBE_ERR_NO_MEMORY;
+    h->T = num_tables;
+    h->pooling = pooling;
+    h->flags = flags;
+    h->tabs.resize(num_tables);
+    int64_t rowbase = 0;
+    int doff = 0;
+    bool vec_cols = true;
+    for (int t = 0; t < num_tables; ++t) {
+        const tbe_table& in = tables[t];
+        if (in.rows <= 0 || in.dim <= 0 || !in.data) {
+            delete h;
+            return TBE_ERR_INVALID_ARG;
+        }
+        if (in.dtype != TBE_F32 && in.dtype != TBE_F16 && in.dtype != TBE_BF16) {
+            delete h;
+            return TBE_ERR_INVALID_ARG;
+        }
+        if (in.rows >= (int64_t(1) << 31) || in.dim > 4096) {
+            delete h;
+            return TBE_ERR_UNSUPPORTED;
+        }
+        TableDesc& d = h->tabs[t];
+        std::memset(&d, 0, sizeof d);
+        d.data = in.data;
+        d.rows = in.rows;
+        d.rowbase = rowbase;
+        d.dim = in.dim;
+        d.doff = doff;
+        d.dtype = in.dtype;
+        d.row_bytes = in.dim * elem_bytes(in.dtype);
+        const int nvec = d.row_bytes / 16;
+        const bool vec = d.row_bytes % 16 == 0 && ((uintptr_t)in.data % 16) == 0 && nvec <= 128;
+        if (vec) {
+            d.path = PATH_VEC;
+            d.lanes = next_pow2(std::min(nvec, 32));
+            d.vecs = nvec <= 32 ? 1 : (nvec <= 64 ? 2 : 4);
+        } else {
+            d.path = PATH_SCALAR;
+            d.lanes = 32;
+            d.vecs = 1;
+        }
+        if (doff % 4 != 0) vec_cols = false;
+        rowbase += in.rows;
+        doff += in.dim;
+        h->max_dim = std::max(h->max_dim, (int)in.dim);
+    }
+    if ((uint64_t)rowbase >= 0xffffffffull) {
+        delete h;
+        return TBE_ERR_UNSUPPORTED;
+    }
+    h->total_rows = (uint64_t)rowbase;
+    h->total_d = doff;
+    h->vec_out = vec_cols && (doff % 4 == 0);
+    int bits = 1;
+    while (bits < 32 && (uint64_t(1) << bits) <= h->total_rows) ++bits;  // values 0..total_rows
+    h->key_bits = bits;
+    h->passes = (bits + kRadixBits - 1) / kRadixBits;
+
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return TBE_ERR_CUDA;
+    }
+    const size_t bytes = tabs_offset() + sizeof(TableDesc) * num_tables;
+    e = cudaMalloc(&h->dev, bytes);
+    if (e != cudaSuccess) {
+        delete h;
+        return e == cudaErrorMemoryAllocation ? TBE_ERR_NO_MEMORY : TBE_ERR_CUDA;
+    }
+    h->blk = static_cast<DevBlock*>(h->dev);
+    h->dtabs = reinterpret_cast<TableDesc*>(static_cast<char*>(h->dev) + tabs_offset());
+    e = cudaMemset(h->dev, 0, tabs_offset());
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->dtabs, h->tabs.data(), sizeof(TableDesc) * num_tables, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(h->dev);
+        delete h;
+        return TBE_ERR_CUDA;
+    }
+    *out = h;
+    return TBE_OK;
+}
+
+void tbe_destroy(tbe_handle* h) {
+    if (!h) return;
+    if (h->dev) cudaFree(h->dev);
+    delete h;
+}
+
+int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                int64_t num_indices, int32_t batch_size, const float* per_sample_weights, float* out,
+                void* stream) {
+    int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
+    if (rc) return rc;
+    if (batch_size == 0) return TBE_OK;
+    if (!out) return TBE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = ensure_schedule(h, batch_size, s);
+    if (rc) return rc;
+    int64_t warps = 0;
+    for (const TableDesc& d : h->tabs) {
+        if (d.path == PATH_HIST) continue;
+        const int per = d.path == PATH_VEC ? 32 / d.lanes : 1;
+        warps += (batch_size + per - 1) / per;
+    }
+    if (warps >= (int64_t(1) << 31) / 32) return TBE_ERR_UNSUPPORTED;
+    FwdArgs a{};
+    a.tabs = h->dtabs;
+    a.blk = h->blk;
+    a.T = h->T;
+    a.B = batch_size;
+    a.N = num_indices;
+    a.indices = indices;
+    a.offsets = offsets;
+    a.idx64 = index_dtype == TBE_I64;
+    a.weights = per_sample_weights;
+    a.mean = h->pooling == TBE_POOL_MEAN;
+    a.out = out;
+    a.total_d = h->total_d;
+    a.vec_out = h->vec_out && ((uintptr_t)out % 16 == 0);
+    a.total_warps = (int)warps;
+    a.parity = h->parity;
+    a.num_sms = h->num_sms;
+    rc = cuda_status(launch_forward(a, s));
+    if (rc == TBE_OK) h->parity ^= 1;
+    return rc;
+}
+
+size_t tbe_backward_workspace_bytes(const tbe_handle* h, int64_t num_indices, int32_t batch_size) {
+    (void)batch_size;
+    if (!h || num_indices < 0) return 0;
+    return make_layout(h, num_indices, kLayoutWithScale).total;
+}
+
+int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int32_t batch_size,
+                                  tbe_ws_layout* out) {
+    (void)batch_size;
+    if (!h || !out || num_indices < 0) return TBE_ERR_INVALID_ARG;
+    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    const bool odd = h->passes % 2 == 1;
+    out->sorted_keys = odd ? L.keys1 : L.keys0;
+    out->sorted_pos = odd ? L.vals1 : L.vals0;
+    out->uniq = L.uniq;
+    out->runstart = L.runstart;
+    out->num_unique = L.counters + sizeof(uint32_t) * CTR_U;
+    out->total_bytes = L.total;
+    return TBE_OK;
+}
+
+int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                         int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
+    if (rc) return rc;
+    if (!workspace) return TBE_ERR_INVALID_ARG;
+    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    if (workspace_bytes < L.total) return TBE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool scale = needs_scale(h, per_sample_weights);
+    Workspace w = bind(h, L, workspace, scale);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, L.zero_bytes, s);
+    if (e == cudaSuccess && num_indices == 0) e = cudaMemsetAsync(w.runstart, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    // remember, in the workspace's counter block, whether a scale array was written
+    if (scale) e = cudaMemsetAsync(w.counters + CTR_HAS_SCALE, 0xff, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    PrepArgs a{};
+    a.tabs = h->dtabs;
+    a.blk = h->blk;
+    a.T = h->T;
+    a.B = batch_size;
+    a.N = num_indices;
+    a.indices = indices;
+    a.offsets = offsets;
+    a.idx64 = index_dtype == TBE_I64;
+    a.weights = per_sample_weights;
+    a.mean = h->pooling == TBE_POOL_MEAN;
+    a.total_rows = (uint32_t)h->total_rows;
+    a.key_bits = h->key_bits;
+    return cuda_status(launch_prepare(a, w, s));
+}
+
+int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, const float* grad_out,
+                       const tbe_optimizer* opt, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!h || !opt || !workspace) return TBE_ERR_INVALID_ARG;
+    if (num_indices < 0 || batch_size < 0) return TBE_ERR_INVALID_ARG;
+    if (num_indices >= (int64_t(1) << 30)) return TBE_ERR_UNSUPPORTED;
+    if (opt->kind != TBE_OPT_SGD && opt->kind != TBE_OPT_ROWWISE_ADAGRAD) return TBE_ERR_INVALID_ARG;
+    if (opt->kind == TBE_OPT_ROWWISE_ADAGRAD && !opt->state) return TBE_ERR_INVALID_ARG;
+    if (num_indices > 0 && !grad_out) return TBE_ERR_INVALID_ARG;
+    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    if (workspace_bytes < L.total) return TBE_ERR_WORKSPACE_TOO_SMALL;
+    if (num_indices == 0 || batch_size == 0) return TBE_OK;
+    Workspace w = bind(h, L, workspace, true);
+    ApplyArgs a{};
+    a.tabs = h->dtabs;
+    a.blk = h->blk;
+    a.T = h->T;
+    a.B = batch_size;
+    a.N = num_indices;
+    a.grad = grad_out;
+    a.grad_vec = ((uintptr_t)grad_out % 16) == 0;
+    a.total_d = h->total_d;
+    a.max_dim = h->max_dim;
+    a.total_rows = (uint32_t)h->total_rows;
+    a.has_scale = 0;
+    a.opt = opt->kind;
+    a.lr = opt->lr;
+    a.eps = opt->eps;
+    a.state = opt->state;
+    a.num_sms = h->num_sms;
+    return cuda_status(launch_apply(a, w, static_cast<cudaStream_t>(stream)));
+}
+
+int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                     int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                     const float* grad_out, float lr, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    int rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size,
+                                  per_sample_weights, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    tbe_optimizer o{TBE_OPT_SGD, lr, 0.f, nullptr};
+    return tbe_backward_apply(h, num_indices, batch_size, grad_out, &o, workspace, workspace_bytes, stream);
+}
+
+int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void* offsets,
+                                 int32_t index_dtype, int64_t num_indices, int32_t batch_size,
+                                 const float* per_sample_weights, const float* grad_out, float* state,
+                                 float lr, float eps, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    if (!state) return TBE_ERR_INVALID_ARG;
+    int rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size,
+                                  per_sample_weights, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    tbe_optimizer o{TBE_OPT_ROWWISE_ADAGRAD, lr, eps, state};
+    return tbe_backward_apply(h, num_indices, batch_size, grad_out, &o, workspace, workspace_bytes, stream);
+}
+
+int tbe_get_error(tbe_handle* h, void* stream) {
+    if (!h) return TBE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    cudaError_t e = cudaMemcpyAsync(&bits, &h->blk->error, sizeof bits, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&h->blk->error, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    if (bits & ERR_TIMEOUT) return TBE_ERR_TIMEOUT;
+    if (bits & ERR_OFFSETS) return TBE_ERR_BAD_OFFSETS;
+    if (bits & ERR_OOB) return TBE_ERR_INDEX_OOB;
+    return TBE_OK;
+}
+
+const char* tbe_strerror(int code) {
+    switch (code) {
+        case TBE_OK: return "ok";
+        case TBE_ERR_INVALID_ARG: return "invalid argument";
+        case TBE_ERR_UNSUPPORTED: return "unsupported size or layout";
+        case TBE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case TBE_ERR_CUDA: return "CUDA runtime error";
+        case TBE_ERR_INDEX_OOB: return "index out of range (lookup skipped)";
+        case TBE_ERR_BAD_OFFSETS: return "offsets not monotone from 0 to N";
+        case TBE_ERR_TIMEOUT: return "bounded device wait ran out";
+        case TBE_ERR_NO_MEMORY: return "out of memory";
+        default: return "unknown error";
+    }
+}
+
+int tbe_table_paths(const tbe_handle* h, int32_t* out_path) {
+    if (!h || !out_path) return TBE_ERR_INVALID_ARG;
+    for (int t = 0; t < h->T; ++t) out_path[t] = h->tabs[t].path;
+    return TBE_OK;
+}
+
+}  // extern "C"

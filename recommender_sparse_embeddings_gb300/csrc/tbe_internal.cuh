@@ -1,0 +1,267 @@
+// Internal definitions shared by the TBE kernels and the C ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tbe {
+
+enum : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+
+// Sticky device error bits (one word in the descriptor block).
+enum : uint32_t { ERR_OOB = 1u, ERR_OFFSETS = 2u, ERR_TIMEOUT = 4u };
+
+// Forward gather schedule of one table.
+enum : int32_t { PATH_VEC = 0, PATH_SCALAR = 1, PATH_HIST = 2 };
+
+// Bags longer than this are pooled by a whole CTA instead of one slot.
+constexpr int kLongBag = 2048;
+// Capacity of the long-bag list held in the descriptor block.
+constexpr int kLongBagCap = 1 << 16;
+// Runs of at least this many lookups take the chunked accumulate path.
+constexpr int kLongRun = 256;
+// Keys per tile of the sort and run-length kernels (256 threads x 16).
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;
+constexpr int kSortTile = kSortThreads * kSortItems;
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+constexpr int kMaxPasses = 4;
+// Decoupled look-back status words: 2 flag bits + 30 count bits.
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagPrefix = 2u << 30;
+constexpr uint32_t kCountMask = (1u << 30) - 1u;
+// Iteration limit of every spin wait (each iteration sleeps ~100 ns).
+constexpr int kSpinLimit = 1 << 20;
+
+struct TableDesc {
+    void* data;       // device, row-major rows x dim
+    int64_t rows;
+    int64_t rowbase;  // sum of rows of the tables before this one
+    int32_t dim;
+    int32_t doff;       // first output column
+    int32_t dtype;      // DT_*
+    int32_t row_bytes;  // dim * element size
+    int32_t path;       // PATH_*
+    int32_t lanes;      // lanes per row in the vector path (power of 2, <= 32)
+    int32_t vecs;       // 16-byte vectors per lane per row (vector path, 1..4)
+    int32_t warp_begin; // first warp of this table in the forward warp map
+};
+
+// Device-resident descriptor block owned by a handle.
+struct DevBlock {
+    uint32_t error;        // sticky ERR_* bits
+    uint32_t long_count[2];// long-bag list fill counters (alternate per call)
+    uint32_t pad;
+    uint64_t long_bags[2][kLongBagCap];  // flat bag ids of bags longer than kLongBag
+    // TableDesc tables[T] follows (aligned to 64 bytes)
+};
+
+__host__ __device__ inline int elem_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+template <typename T>
+__host__ __device__ __forceinline__ T tmin(T a, T b) { return b < a ? b : a; }
+template <typename T>
+__host__ __device__ __forceinline__ T tmax(T a, T b) { return a < b ? b : a; }
+
+// ------------------------------------------------------------ conversions
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ float h_bits_to_float(uint32_t h) {
+    return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+// Element k of a row as float.
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* base, int64_t k) {
+    if constexpr (DT == DT_F32) {
+        return __ldg(reinterpret_cast<const float*>(base) + k);
+    } else if constexpr (DT == DT_F16) {
+        return __half2float(__ldg(reinterpret_cast<const __half*>(base) + k));
+    } else {
+        return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + k));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void store_elem(void* base, int64_t k, float v) {
+    if constexpr (DT == DT_F32) {
+        reinterpret_cast<float*>(base)[k] = v;
+    } else if constexpr (DT == DT_F16) {
+        reinterpret_cast<__half*>(base)[k] = __float2half_rn(v);
+    } else {
+        reinterpret_cast<__nv_bfloat16*>(base)[k] = __float2bfloat16_rn(v);
+    }
+}
+
+// Unpack one 16-byte vector of DT into E = 16/sizeof(DT) floats.
+template <int DT>
+__device__ __forceinline__ void unpack16(const uint4& v, float* f) {
+    if constexpr (DT == DT_F32) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (DT == DT_F16) {
+                f[2 * i] = h_bits_to_float(w[i] & 0xffffu);
+                f[2 * i + 1] = h_bits_to_float(w[i] >> 16);
+            } else {
+                f[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
+                f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+            }
+        }
+    }
+}
+
+template <typename IDX>
+__device__ __forceinline__ int64_t ld_index(const IDX* p, int64_t k) {
+    return (int64_t)__ldg(p + k);
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_volatile_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Decoupled look-back for one running count: publishes this tile's aggregate,
+// walks back over earlier tiles until one with an inclusive prefix, then
+// publishes this tile's inclusive prefix.  Returns the exclusive prefix.
+// Every earlier tile was claimed (atomic tile counter) by a CTA that is
+// already resident and publishes its aggregate without waiting, so each wait
+// ends; the spin is still bounded and raises ERR_TIMEOUT if it runs out.
+__device__ __forceinline__ uint32_t lookback(uint32_t* status, int tile, uint32_t stride,
+                                             uint32_t aggregate, uint32_t* err) {
+    if (tile == 0) {
+        st_volatile_u32(status, kFlagPrefix | aggregate);
+        return 0;
+    }
+    st_volatile_u32(status + (size_t)tile * stride, kFlagAgg | aggregate);
+    uint32_t excl = 0;
+    int j = tile - 1;
+    int spins = 0;
+    while (j >= 0) {
+        const uint32_t s = ld_volatile_u32(status + (size_t)j * stride);
+        const uint32_t f = s & ~kCountMask;
+        if (f == 0) {
+            if (++spins > kSpinLimit) {
+                atomicOr(err, ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(100);
+            continue;
+        }
+        excl += s & kCountMask;
+        if (f == kFlagPrefix) break;
+        --j;
+    }
+    st_volatile_u32(status + (size_t)tile * stride, kFlagPrefix | ((excl + aggregate) & kCountMask));
+    return excl;
+}
+
+// ------------------------------------------------------------ launch API
+// (host functions defined in the kernel files, called by the ABI layer)
+
+struct FwdArgs {
+    const TableDesc* tabs;
+    DevBlock* blk;
+    int T;
+    int B;
+    int64_t N;
+    const void* indices;
+    const void* offsets;
+    int idx64;
+    const float* weights;
+    int mean;
+    float* out;
+    int total_d;
+    int vec_out;   // output rows and column offsets allow 16-byte stores
+    int total_warps;
+    int parity;    // which long-bag counter this call uses
+    int num_sms;
+};
+
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+
+struct Workspace {
+    uint32_t* counters;   // [64]
+    uint32_t* hist;       // [kMaxPasses][kRadix]
+    uint32_t* status;     // [kMaxPasses][tiles][kRadix]
+    uint32_t* rle_status; // [tiles]
+    uint32_t* keys[2];    // [N] ping-pong
+    uint32_t* vals[2];    // [N] ping-pong
+    uint32_t* bag;        // [N] flat bag of each position
+    float* scale;         // [N] s_i of each position (weights and/or mean)
+    uint32_t* uniq;       // [N]
+    uint32_t* runstart;   // [N+1]
+    uint32_t* long_runs;  // [max_long][4]: unique index, first chunk, chunk count, chunks done
+    uint32_t* chunk_run;  // [max_chunks]: long-run index of each chunk
+    float* partial;       // [max_chunks][max_dim]
+    int64_t max_long;
+    int64_t max_chunks;
+    int tiles;
+    int passes;
+    int sorted_buf;       // which ping-pong buffer holds the sorted result
+};
+
+// Counter slots inside Workspace::counters.
+enum : int {
+    CTR_U = 0,          // number of distinct keys
+    CTR_NLONG = 1,      // number of long runs
+    CTR_NCHUNK = 2,     // number of chunks of long runs
+    CTR_RLE_TILE = 3,   // tile claim counter of the run-length kernel
+    CTR_PASS_TILE = 4,  // tile claim counters of the sort passes [4]
+    CTR_HAS_SCALE = 63, // nonzero when prepare wrote the per-lookup scale array
+    CTR_COUNT = 64,
+};
+
+struct PrepArgs {
+    const TableDesc* tabs;
+    DevBlock* blk;
+    int T;
+    int B;
+    int64_t N;
+    const void* indices;
+    const void* offsets;
+    int idx64;
+    const float* weights;
+    int mean;
+    uint32_t total_rows;  // sentinel key for skipped lookups
+    int key_bits;
+};
+
+cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s);
+
+struct ApplyArgs {
+    const TableDesc* tabs;
+    DevBlock* blk;
+    int T;
+    int B;
+    int64_t N;
+    const float* grad;
+    int grad_vec;  // grad is 16-byte aligned (vector loads allowed)
+    int total_d;
+    int max_dim;
+    uint32_t total_rows;
+    int has_scale;  // filled in on the device from CTR_HAS_SCALE
+    int opt;
+    float lr;
+    float eps;
+    float* state;
+    int num_sms;
+};
+
+cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, cudaStream_t s);
+
+}  // namespace tbe

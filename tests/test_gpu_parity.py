@@ -1,0 +1,113 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Workload shapes follow the five synthetic configs,
+shrunk (fewer bags, fewer rows) so the oracle finishes in seconds while the
+batches still span many warps, several sort tiles and a ragged tail."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import recommender_sparse_embeddings_gb300 as tbe
+import workloads
+from helpers import (FP32_TOL, assert_close, assert_tables_match, oracle_backward, oracle_forward,
+                     table_bits, touched_rows, DT_NAME)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+# (config id, B, rows divisor, minimum rows)
+SCALED = {
+    1: (64, 1, 1),
+    2: (300, 1000, 64),
+    3: (160, 1000, 64),
+    4: (256, 1000, 64),
+    5: (160, 1000, 512),
+}
+
+
+def scaled_cfg(cid):
+    B, div, rmin = SCALED[cid]
+    cfg = workloads.get_config(cid)
+    return cfg if div == 1 and B == cfg.B else cfg.scaled(B=B, rows_div=div, rows_min=rmin)
+
+
+def make_problem(cid, index_dtype=torch.int64):
+    cfg = scaled_cfg(cid)
+    specs = workloads.realize_tables(cfg)
+    tables = [t.to(DEV) for t in workloads.make_tables(cfg, "cpu", specs)]
+    batch = workloads.make_batch(cfg, "cpu", index_dtype, specs)
+    grad = workloads.make_grad(cfg, "cpu", specs)
+    return cfg, tables, batch, grad
+
+
+@pytest.mark.parametrize("index_dtype", [torch.int64, torch.int32])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_forward_matches_oracle(cid, index_dtype):
+    cfg, tables, batch, _ = make_problem(cid, index_dtype)
+    h = tbe.tbe_create(tables, cfg.pooling, tbe.TBE_FLAG_NO_HISTOGRAM)
+    w = None if batch.weights is None else batch.weights.to(DEV)
+    out = tbe.tbe_forward(h, batch.indices.to(DEV), batch.offsets.to(DEV), cfg.B, w)
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    ref, skipped = oracle_forward(tables, batch.indices, batch.offsets, cfg.B, batch.weights, cfg.pooling)
+    assert skipped == 0
+    assert_close(out.cpu().numpy(), ref, what=f"cfg{cid} forward", **FP32_TOL)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_prepare_sort_and_rle_bit_exact(cid):
+    cfg, tables, batch, _ = make_problem(cid)
+    h = tbe.tbe_create(tables, cfg.pooling)
+    ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
+    w = None if batch.weights is None else batch.weights.to(DEV)
+    ws = tbe.make_workspace(h, batch.N, cfg.B)
+    tbe.tbe_backward_prepare(h, ind, off, cfg.B, ws, w)
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    lay = tbe.tbe_backward_workspace_layout(h, batch.N, cfg.B)
+    N = batch.N
+
+    def view(offset, n):
+        return ws[offset:offset + 4 * n].view(torch.int32).cpu().numpy().view(np.uint32).astype(np.int64)
+
+    U = int(view(lay.num_unique, 1)[0])
+    keys, _ = oracle.make_keys([t.shape[0] for t in tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
+    ref = oracle.sort_rle(keys)
+    np.testing.assert_array_equal(view(lay.sorted_keys, N), ref["sorted_keys"])
+    np.testing.assert_array_equal(view(lay.sorted_pos, N), ref["sorted_pos"])
+    assert U == len(ref["uniq"])
+    np.testing.assert_array_equal(view(lay.uniq, U), ref["uniq"])
+    rs = view(lay.runstart, U + 1)
+    np.testing.assert_array_equal(rs[:U], ref["runstart"])
+    assert rs[U] == N
+    np.testing.assert_array_equal(np.diff(rs), ref["runlen"])
+
+
+@pytest.mark.parametrize("index_dtype", [torch.int64, torch.int32])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_backward_matches_oracle(cid, index_dtype):
+    cfg, tables, batch, grad = make_problem(cid, index_dtype)
+    before = [table_bits(t) for t in tables]
+    h = tbe.tbe_create(tables, cfg.pooling)
+    ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
+    w = None if batch.weights is None else batch.weights.to(DEV)
+    ws = tbe.make_workspace(h, batch.N, cfg.B)
+    total_rows = sum(t.shape[0] for t in tables)
+    state = None
+    cpu_tables = [t.cpu() for t in tables]
+    if cfg.optimizer == "sgd":
+        tbe.tbe_backward_sgd(h, ind, off, cfg.B, grad.to(DEV), cfg.lr, ws, w)
+    else:
+        state = torch.zeros(total_rows, dtype=torch.float32, device=DEV)
+        tbe.tbe_backward_rowwise_adagrad(h, ind, off, cfg.B, grad.to(DEV), state, cfg.lr, cfg.eps, ws, w)
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    ref_tabs, ref_state = oracle_backward(
+        cpu_tables, batch.indices, batch.offsets, cfg.B, grad, cfg.optimizer, cfg.lr, cfg.eps,
+        batch.weights, cfg.pooling, None if state is None else torch.zeros(total_rows))
+    touched = touched_rows(cpu_tables, batch.indices, batch.offsets, cfg.B)
+    assert_tables_match(tables, ref_tabs, before, touched, what=f"cfg{cid}")
+    if state is not None:
+        assert_close(state.cpu().numpy(), ref_state, what=f"cfg{cid} state", **FP32_TOL)
+        # one update per row: the state changes exactly at the touched rows
+        st = state.cpu().numpy()
+        assert (st[np.concatenate(touched)] > 0).all() and not st[~np.concatenate(touched)].any()
