@@ -107,6 +107,9 @@ def algorithmic_bytes(specs, batch_lengths, N, B, T, idx_bytes, weights, optimiz
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi samples (every 100 ms) read by a thread; summary() keeps the
+    samples taken between mark_start() and mark_end()."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -114,33 +117,58 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.samples = []  # (host time, line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                if line.strip():
+                    self.samples.append((time.perf_counter(), line))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        deadline = time.perf_counter() + 5.0  # wait for the first sample
+        while not self.samples and time.perf_counter() < deadline:
+            time.sleep(0.02)
         return self
 
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
+            time.sleep(0.15)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.thread.join(timeout=5)
         return False
 
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        t0 = self.t0 if self.t0 is not None else -1e30
+        t1 = (self.t1 + 0.1) if self.t1 is not None else 1e30
+        for ts, l in self.samples:
+            if not (t0 <= ts <= t1):
+                continue
             parts = [p.strip() for p in l.split(",")]
             if len(parts) < 8:
                 continue
@@ -194,9 +222,12 @@ class OracleSample:
     first `tables_in_sample` tables with the full B and the same laws.  One
     step = oracle forward + oracle backward (with the workload's optimizer)."""
 
-    def __init__(self, cfg, tables_in_sample: int = 2):
+    def __init__(self, cfg, tables_in_sample: int = 2, bags: int = 0):
         import numpy as np
 
+        total_tables = len(workloads.realize_tables(cfg))
+        if bags and bags < cfg.B:
+            cfg = cfg.scaled(B=bags)  # same rows and laws, fewer bags per table
         self.cfg = cfg
         specs = workloads.realize_tables(cfg)[:tables_in_sample]
         tabs_t = workloads.make_tables(cfg, "cpu", specs)
@@ -210,7 +241,7 @@ class OracleSample:
         self.state = (np.zeros(sum(s.rows for s in specs), np.float32)
                       if cfg.optimizer == "adagrad" else None)
         self.N = batch.N
-        self.sample = (f"{tables_in_sample} of {len(workloads.realize_tables(cfg))} tables, "
+        self.sample = (f"{tables_in_sample} of {total_tables} tables, "
                        f"B={cfg.B}, {batch.N} lookups per fwd+bwd step, one core")
 
     def step(self) -> float:
@@ -223,6 +254,15 @@ class OracleSample:
         oracle.backward(self.tabs, self.names, self.ind, self.off, c.B, self.g, c.optimizer, c.lr,
                         eps=c.eps, weights=self.w, pooling=c.pooling, state=self.state)
         return time.perf_counter() - t0
+
+
+def _mean_bag_length(spec) -> float:
+    kind = spec.length[0]
+    if kind == "fixed":
+        return float(spec.length[1])
+    if kind == "poisson":
+        return float(spec.length[1])
+    return (spec.length[1] + spec.length[2]) / 2.0
 
 
 def cpu_oracle_run(cfg, seconds: float = 10.0):
@@ -246,6 +286,8 @@ def run_ours(args):
     init_dist(world, "nccl")
     cfg = workloads.get_config(args.config)
     specs = workloads.realize_tables(cfg)
+    if args.tables:
+        specs = specs[:args.tables]
     idx_dtype = torch.int64 if args.index_dtype == "int64" else torch.int32
     tables = workloads.make_tables(cfg, dev, specs)
     batch = workloads.make_batch(cfg, dev, idx_dtype, specs)
@@ -278,9 +320,10 @@ def run_ours(args):
         raise RuntimeError(f"device error during warm-up: {tbe.tbe_strerror(rc)}")
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        clk.mark_start()
         for k in range(args.steps):
             flush.zero_()
             e = ev[k]
@@ -289,6 +332,7 @@ def run_ours(args):
             e[2].record(stream); apply()
             e[3].record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         barrier()
     seg = {"forward": 0.0, "prepare": 0.0, "apply": 0.0}
     for e in ev:
@@ -382,7 +426,9 @@ def run_ours(args):
             "dtype": "f32" if all(s.dtype == "f32" for s in specs) else "mixed(f32 accumulate)",
             "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
                     "pages' production shard configurations)",
-            "config": {"workload": cfg.description, "config_id": cfg.cfg_id, "T": T, "B": B,
+            "config": {"workload": cfg.description + (
+                           f" (first {T} of the tables)" if args.tables else ""),
+                       "config_id": cfg.cfg_id, "T": T, "B": B,
                        "N_lookups": N, "unique_rows": U, "index_dtype": args.index_dtype,
                        "optimizer": cfg.optimizer, "parallelism": f"replicas x{world}",
                        "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
@@ -411,7 +457,13 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = workloads.get_config(args.config)
-    sample = OracleSample(cfg)
+    # bound the per-step sample so warm-up + timed steps take about two minutes
+    # (the oracle does on the order of 1e6 lookups per second on one core)
+    specs = workloads.realize_tables(cfg)
+    per_bag = max(1.0, _mean_bag_length(specs[0]))
+    budget_lookups = 120.0 * 1.0e6 / (args.steps + args.warmup)
+    bags = int(min(cfg.B, max(64, budget_lookups / per_bag)))
+    sample = OracleSample(cfg, tables_in_sample=1, bags=bags)
     for _ in range(args.warmup):
         sample.step()
     total_s = sum(sample.step() for _ in range(args.steps))
@@ -444,14 +496,16 @@ def run_reference(args):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", type=int, default=2)
     p.add_argument("--index-dtype", choices=["int64", "int32"], default="int64")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--tables", type=int, default=0,
+                   help="use only the first K tables of the workload (profiling cases)")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least three warm-up steps
     if args.impl == "reference":
