@@ -196,6 +196,27 @@ int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void*
                                  float* state, float lr, float eps, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* Backward + SGD that allocates nothing.  The paper has no counterpart to
+ * this call; it exists for callers that cannot call cudaMalloc when they run
+ * the backward pass (their device memory is owned by another allocator, or
+ * their rules forbid device allocation after set-up), so they cannot pass a
+ * workspace.  Same arguments and result as tbe_backward_sgd, but the
+ * workspace is a 32 MiB static device array inside the library:
+ *  - a batch whose tbe_backward_workspace_bytes exceeds 32 MiB (33554432) is
+ *    rejected with TBE_ERR_WORKSPACE_TOO_SMALL and nothing is launched;
+ *  - the first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture;
+ *  - every device that loads the library holds the array until exit;
+ *  - all calls on a device share the array and it keeps the last call's
+ *    contents (the call clears what must start at zero), so calls whose GPU
+ *    work overlaps (other streams or host threads) race: order them.
+ * The handle comes from tbe_create (called at set-up). */
+int tbe_backward_sgd_noalloc(tbe_handle* h, const void* indices, const void* offsets,
+                             int32_t index_dtype, int64_t num_indices, int32_t batch_size,
+                             const float* per_sample_weights, const float* grad_out, float lr,
+                             void* stream);
+
 /* ------------------------------------------------------------- diagnostics */
 
 /* Synchronises `stream`, returns the first device-detected error since the

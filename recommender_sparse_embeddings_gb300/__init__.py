@@ -95,6 +95,7 @@ def load_library():
         "tbe_backward_sgd": ([P, P, P, i32, i64, i32, P, P, f32, P, ctypes.c_size_t, P], ctypes.c_int),
         "tbe_backward_rowwise_adagrad": ([P, P, P, i32, i64, i32, P, P, P, f32, f32, P,
                                           ctypes.c_size_t, P], ctypes.c_int),
+        "tbe_backward_sgd_noalloc": ([P, P, P, i32, i64, i32, P, P, f32, P], ctypes.c_int),
         "tbe_get_error": ([P, P], ctypes.c_int),
         "tbe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tbe_table_paths": ([P, ctypes.POINTER(i32)], ctypes.c_int),
@@ -269,6 +270,16 @@ def tbe_backward_rowwise_adagrad(h: Handle, indices, offsets, batch_size: int, g
         batch_size, _ptr(per_sample_weights), _ptr(grad_out), _ptr(state), lr, eps,
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "tbe_backward_rowwise_adagrad")
+
+
+def tbe_backward_sgd_noalloc(h: Handle, indices, offsets, batch_size: int, grad_out, lr: float,
+                             per_sample_weights=None, stream=None):
+    """tbe_backward_sgd with the library's static 32 MiB workspace: for callers
+    that cannot allocate device memory for a workspace (see include/tbe.h)."""
+    rc = load_library().tbe_backward_sgd_noalloc(
+        h.ptr, _ptr(indices), _ptr(offsets), _index_dtype(indices, offsets), indices.numel(),
+        batch_size, _ptr(per_sample_weights), _ptr(grad_out), lr, _stream(stream))
+    _check(rc, "tbe_backward_sgd_noalloc")
 
 
 def tbe_get_error(h: Handle, stream=None) -> int:
