@@ -22,9 +22,12 @@ struct tbe_handle {
     uint32_t flags = 0;
     int num_sms = 0;
     std::vector<TableDesc> tabs;
-    void* dev = nullptr;          // DevBlock followed by TableDesc[T]
+    void* dev = nullptr;          // DevBlock, TableDesc[T], class table list[T]
     DevBlock* blk = nullptr;
     TableDesc* dtabs = nullptr;
+    int32_t* dclass_tables = nullptr;
+    int class_begin[kNumClasses] = {};
+    int class_count[kNumClasses] = {};
     int total_d = 0;
     int max_dim = 0;
     uint64_t total_rows = 0;
@@ -40,6 +43,25 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t tabs_offset() { return align_up(sizeof(DevBlock)); }
+size_t class_list_offset(int T) { return align_up(tabs_offset() + sizeof(TableDesc) * T); }
+
+// Backward class of a table: dtype and row shape (vector lanes for dim 32,
+// 64, 128, 256 when rows and gradient columns are aligned for them).
+int backward_class(const TableDesc& d, int total_d) {
+    const bool rows16 = ((uintptr_t)d.data % 16) == 0;
+    const bool a4 = rows16 && d.doff % 4 == 0 && total_d % 4 == 0;
+    const bool a2 = rows16 && d.doff % 2 == 0 && total_d % 2 == 0;
+    int shape = SHAPE_GENERIC;
+    if (d.dim == 32)
+        shape = SHAPE_D32;
+    else if (d.dim == 64 && a2)
+        shape = SHAPE_D64;
+    else if (d.dim == 128 && a4)
+        shape = SHAPE_D128;
+    else if (d.dim == 256 && a4)
+        shape = SHAPE_D256;
+    return d.dtype * NUM_SHAPES + shape;
+}
 
 int next_pow2(int x) {
     int p = 1;
@@ -49,7 +71,7 @@ int next_pow2(int x) {
 
 struct Layout {
     size_t counters, hist, status, rle_status, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
-        long_runs, chunk_run, partial, total;
+        long_runs, chunk_run, ustart, partial, total;
     size_t zero_bytes;  // counters..rle_status are zeroed per call
     int64_t max_long, max_chunks;
     int tiles;
@@ -82,6 +104,7 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     L.runstart = take(sizeof(uint32_t) * (n + 1));
     L.long_runs = take(sizeof(uint32_t) * 4 * L.max_long);
     L.chunk_run = take(sizeof(uint32_t) * L.max_chunks);
+    L.ustart = take(sizeof(uint32_t) * (h->T + 1));
     L.partial = take(sizeof(float) * (size_t)L.max_chunks * h->max_dim);
     L.total = o;
     return L;
@@ -108,6 +131,7 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.runstart = reinterpret_cast<uint32_t*>(p + L.runstart);
     w.long_runs = reinterpret_cast<uint32_t*>(p + L.long_runs);
     w.chunk_run = reinterpret_cast<uint32_t*>(p + L.chunk_run);
+    w.ustart = reinterpret_cast<uint32_t*>(p + L.ustart);
     w.partial = reinterpret_cast<float*>(p + L.partial);
     w.max_long = L.max_long;
     w.max_chunks = L.max_chunks;
@@ -194,7 +218,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         if (vec) {
             d.path = PATH_VEC;
             d.lanes = next_pow2(std::min(nvec, 32));
-            d.vecs = nvec <= 32 ? 1 : (nvec <= 64 ? 2 : 4);
+            d.vecs = (nvec + 31) / 32;  // column blocks of 32 vectors, one warp each
         } else {
             d.path = PATH_SCALAR;
             d.lanes = 32;
@@ -223,7 +247,20 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         delete h;
         return TBE_ERR_CUDA;
     }
-    const size_t bytes = tabs_offset() + sizeof(TableDesc) * num_tables;
+    std::vector<int32_t> order;
+    {
+        std::vector<std::vector<int32_t>> by_class(kNumClasses);
+        for (int t = 0; t < num_tables; ++t) {
+            h->tabs[t].cls = backward_class(h->tabs[t], h->total_d);
+            by_class[h->tabs[t].cls].push_back(t);
+        }
+        for (int c = 0; c < kNumClasses; ++c) {
+            h->class_begin[c] = (int)order.size();
+            h->class_count[c] = (int)by_class[c].size();
+            order.insert(order.end(), by_class[c].begin(), by_class[c].end());
+        }
+    }
+    const size_t bytes = class_list_offset(num_tables) + sizeof(int32_t) * num_tables;
     e = cudaMalloc(&h->dev, bytes);
     if (e != cudaSuccess) {
         delete h;
@@ -231,9 +268,12 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     }
     h->blk = static_cast<DevBlock*>(h->dev);
     h->dtabs = reinterpret_cast<TableDesc*>(static_cast<char*>(h->dev) + tabs_offset());
+    h->dclass_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + class_list_offset(num_tables));
     e = cudaMemset(h->dev, 0, tabs_offset());
     if (e == cudaSuccess)
         e = cudaMemcpy(h->dtabs, h->tabs.data(), sizeof(TableDesc) * num_tables, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->dclass_tables, order.data(), sizeof(int32_t) * num_tables, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(h->dev);
         delete h;
@@ -263,7 +303,8 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
     for (const TableDesc& d : h->tabs) {
         if (d.path == PATH_HIST) continue;
         const int per = d.path == PATH_VEC ? 32 / d.lanes : 1;
-        warps += (batch_size + per - 1) / per;
+        const int blocks = d.path == PATH_VEC ? d.vecs : 1;
+        warps += (int64_t)(batch_size + per - 1) / per * blocks;
     }
     if (warps >= (int64_t(1) << 31) / 32) return TBE_ERR_UNSUPPORTED;
     FwdArgs a{};
@@ -371,7 +412,8 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.eps = opt->eps;
     a.state = opt->state;
     a.num_sms = h->num_sms;
-    return cuda_status(launch_apply(a, w, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,

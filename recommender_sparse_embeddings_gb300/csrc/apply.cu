@@ -4,22 +4,34 @@
 // streaming path for short runs, gradient accumulation for runs of at least
 // 256 lookups).
 //
-//  short_runs_kernel: one warp per distinct key (persistent grid-stride).  A
-//    run of fewer than kLongRun lookups is summed in order by that warp and
-//    the row is updated in place.  A longer run is only registered: it gets
-//    ceil(len/256) consecutive chunk slots.
-//  long_chunks_kernel: one warp per 256-lookup chunk writes its partial sum;
-//    the warp that completes the last chunk of a run (counted with an atomic
-//    after a fence) adds the run's partials in chunk order and updates the
-//    row.  Results do not depend on scheduling.
+// One kernel per backward class (table dtype x row shape) present in the
+// handle, so each kernel's registers are sized for one shape only.  A class
+// kernel walks a work list: first the 256-lookup chunks of long runs whose
+// table is in the class (registered by the preparation step), then batches
+// of kBatchRows consecutive distinct keys of the class's tables.  Work items
+// go to warps round-robin.
 //
-// Sums use compensated (Kahan) fp32 addition, so a run of 10^5 lookups keeps
-// close to fp32 rounding of the exact sum.  Each lane owns VW consecutive
-// columns of every 32*VW-column block, so the gradient rows are read with
-// 4- to 16-byte loads across the warp.
+//  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
+//    batch into pieces of at most R keys and walks each piece's sorted lookups
+//    as one stream: positions, bags and scales are fetched 32 lookups at a
+//    time one chunk ahead, gradient rows GROUP at a time, and each lookup is
+//    added to its key's sum.  The piece's table rows are read before the
+//    stream starts so the read overlaps the gradient gather; after the stream
+//    each key gets its optimizer step and its row is stored.  Sums are plain
+//    fp32 in lookup order (at most 255 terms).
+//  Long runs, "accumulate": a warp sums one 256-lookup chunk with compensated
+//    (Kahan) fp32 addition and writes the partial; the warp that completes the
+//    last chunk of a run (atomic count after a fence) adds the partials in
+//    chunk order with Kahan addition, updates the row, and resets the count
+//    so the prepared workspace can be applied again.
+//
+// Lanes own columns: lane l holds columns blk*32*VW + l*VW + [0, VW) of each
+// of NB blocks, so gradient rows are read with 4- to 16-byte loads.
 #include "tbe_internal.cuh"
 
 namespace tbe {
+
+constexpr int kBatchRows = 16;  // distinct keys per short-run work item
 
 struct Kahan {
     float s, c;
@@ -50,9 +62,103 @@ __device__ __forceinline__ int table_of(const TableDesc* tabs, int T, uint32_t k
     return lo;
 }
 
-// Loads VW consecutive floats (VW*4 bytes, aligned) into f.
+template <int CODE>
+struct ShapeOf {
+    static constexpr int VW = CODE == SHAPE_D64 ? 2 : (CODE == SHAPE_D128 || CODE == SHAPE_D256 ? 4 : 1);
+    static constexpr int NB = CODE == SHAPE_D256 ? 2 : 1;
+};
+
+// ------------------------------------------------------- row slice helpers
+
+// A lane's slice of one table row: NB blocks of VW consecutive elements,
+// kept as raw 32-bit words (w[WORDS]) until needed.  Static helpers over a
+// plain word array keep the slices in registers.
+template <int DT, int VW, int NB>
+struct Slice {
+    static constexpr int WPB = DT == DT_F32 ? VW : (VW + 1) / 2;  // words per block
+    static constexpr int WORDS = WPB * NB;
+
+    __device__ __forceinline__ static int col(int lane, int q) { return q * 32 * VW + lane * VW; }
+
+    __device__ __forceinline__ static void load(uint32_t (&w)[WORDS], const void* base, int64_t row, int dim,
+                                                int lane) {
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            const int64_t k = row * dim + col(lane, q);
+            if constexpr (DT == DT_F32) {
+                const float* p = reinterpret_cast<const float*>(base) + k;
+                if constexpr (VW == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(p);
+                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y; w[q * WPB + 2] = v.z; w[q * WPB + 3] = v.w;
+                } else if constexpr (VW == 2) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(p);
+                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y;
+                } else {
+                    w[q * WPB] = *reinterpret_cast<const uint32_t*>(p);
+                }
+            } else {
+                const unsigned short* p = reinterpret_cast<const unsigned short*>(base) + k;
+                if constexpr (VW == 4) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(p);
+                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y;
+                } else if constexpr (VW == 2) {
+                    w[q * WPB] = *reinterpret_cast<const uint32_t*>(p);
+                } else {
+                    w[q * WPB] = *p;
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ static void store(const uint32_t (&w)[WORDS], void* base, int64_t row, int dim,
+                                                 int lane) {
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            const int64_t k = row * dim + col(lane, q);
+            if constexpr (DT == DT_F32) {
+                float* p = reinterpret_cast<float*>(base) + k;
+                if constexpr (VW == 4)
+                    *reinterpret_cast<uint4*>(p) = make_uint4(w[q * WPB], w[q * WPB + 1], w[q * WPB + 2], w[q * WPB + 3]);
+                else if constexpr (VW == 2)
+                    *reinterpret_cast<uint2*>(p) = make_uint2(w[q * WPB], w[q * WPB + 1]);
+                else
+                    *reinterpret_cast<uint32_t*>(p) = w[q * WPB];
+            } else {
+                unsigned short* p = reinterpret_cast<unsigned short*>(base) + k;
+                if constexpr (VW == 4)
+                    *reinterpret_cast<uint2*>(p) = make_uint2(w[q * WPB], w[q * WPB + 1]);
+                else if constexpr (VW == 2)
+                    *reinterpret_cast<uint32_t*>(p) = w[q * WPB];
+                else
+                    *p = (unsigned short)w[q * WPB];
+            }
+        }
+    }
+
+    __device__ __forceinline__ static float get(const uint32_t (&w)[WORDS], int q, int v) {
+        if constexpr (DT == DT_F32) {
+            return __uint_as_float(w[q * WPB + v]);
+        } else {
+            const uint32_t h = (w[q * WPB + v / 2] >> (16 * (v & 1))) & 0xffffu;
+            return DT == DT_F16 ? h_bits_to_float(h) : bf16_bits_to_float(h);
+        }
+    }
+
+    __device__ __forceinline__ static void set(uint32_t (&w)[WORDS], int q, int v, float x) {
+        if constexpr (DT == DT_F32) {
+            w[q * WPB + v] = __float_as_uint(x);
+        } else {
+            const uint32_t h = DT == DT_F16 ? (uint32_t)__half_as_ushort(__float2half_rn(x))
+                                            : (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+            uint32_t& word = w[q * WPB + v / 2];
+            word = (v & 1) ? ((word & 0x0000ffffu) | (h << 16)) : ((word & 0xffff0000u) | h);
+        }
+    }
+};
+
+// Loads the lane's VW gradient floats starting at p.
 template <int VW>
-__device__ __forceinline__ void ld_f32v(const float* p, float (&f)[VW]) {
+__device__ __forceinline__ void ld_grad(const float* p, float* f) {
     if constexpr (VW == 4) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(p));
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
@@ -64,134 +170,13 @@ __device__ __forceinline__ void ld_f32v(const float* p, float (&f)[VW]) {
     }
 }
 
-// Row slice of VW elements of dtype DT <-> floats (aligned vector access).
-template <int DT, int VW>
-__device__ __forceinline__ void ld_row(const void* base, int64_t k, float (&f)[VW]) {
-    if constexpr (DT == DT_F32) {
-        const float* p = reinterpret_cast<const float*>(base) + k;
-        if constexpr (VW == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(p);
-            f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-        } else if constexpr (VW == 2) {
-            const float2 v = *reinterpret_cast<const float2*>(p);
-            f[0] = v.x; f[1] = v.y;
-        } else {
-            f[0] = *p;
-        }
-    } else {
-        const unsigned short* p = reinterpret_cast<const unsigned short*>(base) + k;
-        uint32_t w[(VW + 1) / 2];
-        if constexpr (VW == 4) {
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            w[0] = v.x; w[1] = v.y;
-        } else if constexpr (VW == 2) {
-            w[0] = *reinterpret_cast<const uint32_t*>(p);
-        } else {
-            w[0] = *p;
-        }
-#pragma unroll
-        for (int i = 0; i < VW; ++i) {
-            const uint32_t h = (w[i / 2] >> (16 * (i & 1))) & 0xffffu;
-            f[i] = DT == DT_F16 ? h_bits_to_float(h) : bf16_bits_to_float(h);
-        }
-    }
-}
-
-template <int DT, int VW>
-__device__ __forceinline__ void st_row(void* base, int64_t k, const float (&f)[VW]) {
-    if constexpr (DT == DT_F32) {
-        float* p = reinterpret_cast<float*>(base) + k;
-        if constexpr (VW == 4)
-            *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-        else if constexpr (VW == 2)
-            *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
-        else
-            *p = f[0];
-    } else {
-        uint32_t h[VW];
-#pragma unroll
-        for (int i = 0; i < VW; ++i) {
-            if constexpr (DT == DT_F16)
-                h[i] = __half_as_ushort(__float2half_rn(f[i]));
-            else
-                h[i] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i]));
-        }
-        unsigned short* p = reinterpret_cast<unsigned short*>(base) + k;
-        if constexpr (VW == 4)
-            *reinterpret_cast<uint2*>(p) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-        else if constexpr (VW == 2)
-            *reinterpret_cast<uint32_t*>(p) = h[0] | (h[1] << 16);
-        else
-            *p = (unsigned short)h[0];
-    }
-}
-
-// Column layout of a row of D floats for one warp: NB blocks of 32*VW
-// columns; lane owns columns blk*32*VW + lane*VW + [0, VW).
-template <int VW, int NB>
-struct Cols {
-    static constexpr int N = VW * NB;
-    __device__ __forceinline__ static int col(int lane, int blk) { return blk * 32 * VW + lane * VW; }
-};
-
-// Sum of s_i * grad rows over sorted slots [s0, s1) into acc (per lane).
-template <int VW, int NB>
-__device__ __forceinline__ void reduce_run(const ApplyArgs& a, const Workspace& ws, const uint32_t* __restrict__ pos_sorted,
-                                           int t, int doff, uint32_t s0, uint32_t s1, int lane,
-                                           Kahan (&acc)[NB][VW]) {
-    constexpr int U = 4;
-    const int64_t tB = (int64_t)t * a.B;
-    const int64_t nbags = (int64_t)a.T * a.B;
-    for (uint32_t c0 = s0; c0 < s1; c0 += 32) {
-        const uint32_t i = c0 + lane;
-        int64_t b = -1;
-        float s = 1.f;
-        if (i < s1) {
-            const uint32_t pos = __ldg(pos_sorted + i);
-            if (pos < (uint32_t)a.N) {
-                const uint32_t bag = __ldg(ws.bag + pos);
-                if ((int64_t)bag < nbags && (int64_t)bag >= tB && (int64_t)bag < tB + a.B) b = bag - tB;
-                if (a.has_scale) s = __ldg(ws.scale + pos);
-            }
-        }
-        const int n = (int)tmin<uint32_t>(32u, s1 - c0);
-        for (int k0 = 0; k0 < n; k0 += U) {
-            int64_t bb[U];
-            float ss[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                bb[u] = __shfl_sync(0xffffffffu, b, (k0 + u) & 31);
-                ss[u] = __shfl_sync(0xffffffffu, s, (k0 + u) & 31);
-                if (k0 + u >= n) bb[u] = -1;
-            }
-            float g[U][NB][VW];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int q = 0; q < NB; ++q) {
-                    if (bb[u] >= 0) {
-                        ld_f32v<VW>(a.grad + bb[u] * a.total_d + doff + Cols<VW, NB>::col(lane, q), g[u][q]);
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
-                    }
-                }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (bb[u] >= 0)
-#pragma unroll
-                    for (int q = 0; q < NB; ++q)
-#pragma unroll
-                        for (int v = 0; v < VW; ++v) acc[q][v].add_scaled(ss[u], g[u][q][v]);
-        }
-    }
-}
-
-// One optimizer step on row r of table t with gradient g (this lane's columns).
+// Optimizer step for one row given its gradient g (this lane's columns);
+// `row` holds the old values and receives the new ones.  `m_old` is the row's
+// Adagrad state (ignored by SGD); the new state is returned.
 template <int DT, int VW, int NB>
-__device__ __forceinline__ void update_row(const ApplyArgs& a, const TableDesc& td, uint32_t key,
-                                           int64_t r, const float (&g)[NB][VW], int lane) {
-    float step[NB][VW];
+__device__ __forceinline__ float optimizer_step(const ApplyArgs& a, int dim, const float (&g)[NB][VW],
+                                                uint32_t (&row)[Slice<DT, VW, NB>::WORDS], float m_old) {
+    using S = Slice<DT, VW, NB>;
     if (a.opt == 2) {
         float sq = 0.f;
 #pragma unroll
@@ -200,45 +185,195 @@ __device__ __forceinline__ void update_row(const ApplyArgs& a, const TableDesc& 
             for (int v = 0; v < VW; ++v) sq = fmaf(g[q][v], g[q][v], sq);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        const float m = a.state[key] + __fdiv_rn(sq, (float)td.dim);
-        __syncwarp();
-        if (lane == 0) a.state[key] = m;
+        const float m = m_old + __fdiv_rn(sq, (float)dim);
         const float denom = sqrtf(m) + a.eps;
 #pragma unroll
         for (int q = 0; q < NB; ++q)
 #pragma unroll
-            for (int v = 0; v < VW; ++v) step[q][v] = a.lr * __fdiv_rn(g[q][v], denom);
-    } else {
-#pragma unroll
-        for (int q = 0; q < NB; ++q)
-#pragma unroll
-            for (int v = 0; v < VW; ++v) step[q][v] = a.lr * g[q][v];
+            for (int v = 0; v < VW; ++v) S::set(row, q, v, S::get(row, q, v) - a.lr * __fdiv_rn(g[q][v], denom));
+        return m;
     }
-    const int64_t rowoff = r * td.dim;
 #pragma unroll
-    for (int q = 0; q < NB; ++q) {
-        const int c = Cols<VW, NB>::col(lane, q);
-        float w[VW];
-        ld_row<DT, VW>(td.data, rowoff + c, w);
+    for (int q = 0; q < NB; ++q)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) w[v] = w[v] - step[q][v];
-        st_row<DT, VW>(td.data, rowoff + c, w);
+        for (int v = 0; v < VW; ++v) S::set(row, q, v, fmaf(-a.lr, g[q][v], S::get(row, q, v)));
+    return m_old;
+}
+
+// ------------------------------------------------------------- short runs
+
+// Per-lookup metadata of one 32-lookup chunk, lane k holding lookup c0+k:
+// slot = position of its key among the keys of the current piece, or -1 when
+// the lookup is past the end or belongs to a key outside the piece;
+// b = bag row within the table; s = scale.
+struct Meta {
+    int slot;
+    int b;
+    float s;
+};
+
+// Largest batch row l (0..15) whose first sorted slot rs_l <= i; rs of row l
+// is held by lane l (lane n holds the end of the last row, later lanes N).
+__device__ __forceinline__ int row_in_batch(uint32_t rs, uint32_t i) {
+    int lo = 0, hi = kBatchRows - 1;
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int mid = (lo + hi + 1) >> 1;
+        const uint32_t v = __shfl_sync(0xffffffffu, rs, mid);
+        if (v <= i)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                          uint32_t rs, uint32_t piece, uint32_t c0, uint32_t E1, int64_t tB,
+                                          int lane, Meta& m) {
+    const uint32_t i = c0 + lane;
+    const int r = row_in_batch(rs, i < E1 ? i : (E1 > 0 ? E1 - 1 : 0));
+    m.slot = -1;
+    m.b = 0;
+    m.s = 1.f;
+    if (i < E1 && ((piece >> r) & 1u)) {
+        const uint32_t pos = __ldg(pos_sorted + i);
+        if (pos < (uint32_t)a.N) {
+            const int64_t bag = (int64_t)__ldg(ws.bag + pos);
+            if (bag >= tB && bag < tB + a.B) {
+                m.slot = __popc(piece & ((1u << r) - 1u));
+                m.b = (int)(bag - tB);
+                if (a.has_scale) m.s = __ldg(ws.scale + pos);
+            }
+        }
     }
 }
 
-// Element-wise variant for dims that are not 32*VW*NB: lane owns columns
-// lane + 32*j of each 256-column block.
+// Gradient rows in flight per lane (GROUP) and keys per piece (R), whose
+// table-row slices and gradient sums stay in registers.  Sized so the live
+// words R * (row words + columns) + GROUP * columns stay within 32 per lane,
+// which keeps the kernels near 64 registers (4 CTAs of 256 threads per SM).
+template <int DT, int VW, int NB>
+struct ShortTune {
+    static constexpr int WORDS = Slice<DT, VW, NB>::WORDS;
+    static constexpr int COLS = VW * NB;
+    static constexpr int G0 = 16 / COLS;
+    static constexpr int GROUP = G0 > 8 ? 8 : (G0 < 2 ? 2 : G0);
+    static constexpr int R0 = (32 - GROUP * COLS) / (WORDS + COLS);
+    static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
+};
+
+template <int DT, int VW, int NB>
+__device__ __forceinline__ void short_piece(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                            const TableDesc& td, int t, uint32_t rs, uint32_t key, float mstate,
+                                            uint32_t piece, int lane) {
+    using Tn = ShortTune<DT, VW, NB>;
+    using S = Slice<DT, VW, NB>;
+    constexpr int R = Tn::R;
+    constexpr int GROUP = Tn::GROUP;
+    constexpr int WORDS = S::WORDS;
+    const int64_t tB = (int64_t)t * a.B;
+    const int first = __ffs(piece) - 1;
+    const int last = 31 - __clz(piece);
+    const uint32_t E0 = __shfl_sync(0xffffffffu, rs, first);
+    const uint32_t E1 = __shfl_sync(0xffffffffu, rs, last + 1);
+
+    // old values of the piece's rows (slot s = s-th set bit of piece), read
+    // now so the loads overlap the gradient gather below
+    uint32_t wrow[R][WORDS];
+#pragma unroll
+    for (int s = 0; s < R; ++s) {
+        uint32_t m = piece;  // drop the s lowest set bits: the next one is slot s
+#pragma unroll
+        for (int k = 0; k < s; ++k) m &= m - 1u;
+        const int r = m ? __ffs(m) - 1 : 0;
+        const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
+        if (m) S::load(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
+    }
+
+    float acc[R][NB][VW];
+#pragma unroll
+    for (int s = 0; s < R; ++s)
+#pragma unroll
+        for (int q = 0; q < NB; ++q)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) acc[s][q][v] = 0.f;
+
+    // stream the piece's lookups in sorted order
+    Meta cm;
+    load_meta(a, ws, pos_sorted, rs, piece, E0, E1, tB, lane, cm);
+    for (uint32_t c0 = E0; c0 < E1; c0 += 32) {
+        Meta nm;
+        load_meta(a, ws, pos_sorted, rs, piece, c0 + 32, E1, tB, lane, nm);
+        const int n = (int)tmin<uint32_t>(32u, E1 - c0);
+        for (int k0 = 0; k0 < n; k0 += GROUP) {
+            int sl[GROUP];
+            float ss[GROUP];
+            float g[GROUP][NB][VW];
+#pragma unroll
+            for (int u = 0; u < GROUP; ++u) {
+                const int src = (k0 + u) & 31;
+                sl[u] = __shfl_sync(0xffffffffu, cm.slot, src);
+                const int b = __shfl_sync(0xffffffffu, cm.b, src);
+                ss[u] = __shfl_sync(0xffffffffu, cm.s, src);
+                if (k0 + u >= n) sl[u] = -1;
+                const float* grow = a.grad + (int64_t)b * a.total_d + td.doff;
+#pragma unroll
+                for (int q = 0; q < NB; ++q) {
+                    if (sl[u] >= 0) {
+                        ld_grad<VW>(grow + S::col(lane, q), g[u][q]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
+                    }
+                }
+            }
+            // add each lookup to its key's sum (a select, not a branch, keeps
+            // acc in registers)
+#pragma unroll
+            for (int u = 0; u < GROUP; ++u)
+#pragma unroll
+                for (int s = 0; s < R; ++s) {
+                    const float w = sl[u] == s ? ss[u] : 0.f;
+#pragma unroll
+                    for (int q = 0; q < NB; ++q)
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) acc[s][q][v] = fmaf(w, g[u][q][v], acc[s][q][v]);
+                }
+        }
+        cm = nm;
+    }
+
+    // one optimizer step per key of the piece
+    uint32_t m = piece;
+#pragma unroll
+    for (int s = 0; s < R; ++s) {
+        if (m) {
+            const int r = __ffs(m) - 1;
+            m &= m - 1u;
+            const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
+            const float m_old = __shfl_sync(0xffffffffu, mstate, r);
+            const float mnew = optimizer_step<DT, VW, NB>(a, td.dim, acc[s], wrow[s], m_old);
+            S::store(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
+            if (a.opt == 2 && lane == r) a.state[kr] = mnew;
+        }
+    }
+}
+
+// Element-wise rows: one key at a time, whole warp, columns lane + 32*j of
+// each 256-column block.  Adagrad needs the row's sum of squares before any
+// column moves, so it makes two passes.  With partial_src, the gradient is
+// the ordered sum of nchunks partial rows instead of the lookups [s0, s1).
 template <int DT>
-__device__ void reduce_update_generic(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                      const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                                      int lane, const float* partial_src, int nchunks) {
+__device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                            const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
+                                            const float* partial_src, uint32_t nchunks, int lane) {
     const int D = td.dim;
     const int64_t r = (int64_t)key - td.rowbase;
     const int64_t tB = (int64_t)t * a.B;
-    // Adagrad needs the whole row's sum of squares before any column moves:
-    // first pass accumulates it, second pass recomputes g and updates.
     float sq = 0.f;
-    for (int pass = 0; pass < (a.opt == 2 ? 2 : 1); ++pass) {
+    const int passes = a.opt == 2 ? 2 : 1;
+    for (int pass = 0; pass < passes; ++pass) {
         float m = 0.f, denom = 1.f;
         if (a.opt == 2 && pass == 1) {
 #pragma unroll
@@ -251,7 +386,7 @@ __device__ void reduce_update_generic(const ApplyArgs& a, const Workspace& ws, c
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = Kahan{0.f, 0.f};
             if (partial_src) {
-                for (int ch = 0; ch < nchunks; ++ch)
+                for (uint32_t ch = 0; ch < nchunks; ++ch)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int c = cb + lane + 32 * j;
@@ -281,9 +416,9 @@ __device__ void reduce_update_generic(const ApplyArgs& a, const Workspace& ws, c
                     sq = fmaf(g, g, sq);
                     continue;
                 }
-                const float step = a.opt == 2 ? a.lr * __fdiv_rn(g, denom) : a.lr * g;
                 const float w = load_elem<DT>(td.data, r * D + c);
-                store_elem<DT>(td.data, r * D + c, w - step);
+                const float nw = a.opt == 2 ? w - a.lr * __fdiv_rn(g, denom) : fmaf(-a.lr, g, w);
+                store_elem<DT>(td.data, r * D + c, nw);
             }
         }
         if (a.opt == 2 && pass == 1) {
@@ -293,114 +428,132 @@ __device__ void reduce_update_generic(const ApplyArgs& a, const Workspace& ws, c
     }
 }
 
+// One batch: distinct keys [u0, u0 + n) of table t (n <= kBatchRows).
+template <int DT, int CODE>
+__device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                            const TableDesc& td, int t, uint32_t u0, uint32_t n, int lane) {
+    const uint32_t N = (uint32_t)a.N;
+    // lane l <= n: first sorted slot of batch row l (lane n: end of the last
+    // row); lanes past n hold N so no lookup maps to them
+    uint32_t rs = N;
+    if ((uint32_t)lane <= n) rs = tmin<uint32_t>(__ldg(ws.runstart + u0 + lane), N);
+    uint32_t key = 0xffffffffu;
+    if ((uint32_t)lane < n) key = __ldg(ws.uniq + u0 + lane);
+    const uint32_t re = __shfl_down_sync(0xffffffffu, rs, 1);
+    bool is_short = false;
+    float mstate = 0.f;
+    if ((uint32_t)lane < n && key < a.total_rows && re > rs && re - rs < (uint32_t)kLongRun) {
+        is_short = true;
+        if (a.opt == 2) mstate = a.state[key];
+    }
+    uint32_t rows = __ballot_sync(0xffffffffu, is_short);
+    if constexpr (CODE == SHAPE_GENERIC) {
+        while (rows) {
+            const int r = __ffs(rows) - 1;
+            rows &= rows - 1;
+            const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
+            const uint32_t s0 = __shfl_sync(0xffffffffu, rs, r);
+            const uint32_t s1 = __shfl_sync(0xffffffffu, rs, r + 1);
+            generic_row<DT>(a, ws, pos_sorted, td, t, kr, s0, s1, nullptr, 0, lane);
+        }
+    } else {
+        constexpr int VW = ShapeOf<CODE>::VW, NB = ShapeOf<CODE>::NB;
+        constexpr int R = ShortTune<DT, VW, NB>::R;
+        // pieces of at most R consecutive short keys: a long or skipped key
+        // between two short ones ends the piece, so a piece's lookups are
+        // exactly the sorted slots of its own keys
+        while (rows) {
+            const uint32_t low = rows & (0u - rows);
+            uint32_t piece = low;
+#pragma unroll
+            for (int k = 1; k < R; ++k) {
+                const uint32_t bit = low << k;  // next key up (0 past bit 31)
+                if (!(rows & bit)) break;
+                piece |= bit;
+            }
+            rows &= ~piece;
+            short_piece<DT, VW, NB>(a, ws, pos_sorted, td, t, rs, key, mstate, piece, lane);
+        }
+    }
+}
+
+// -------------------------------------------------------------- long runs
+
 template <int DT, int VW, int NB>
-__device__ __forceinline__ void short_run(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                          const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                                          int lane) {
+__device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                               const TableDesc& td, int t, uint32_t s0, uint32_t s1,
+                                               float* part_row, int lane) {
+    using S = Slice<DT, VW, NB>;
+    constexpr int GROUP = NB == 2 ? 2 : 4;
+    const int64_t tB = (int64_t)t * a.B;
     Kahan acc[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    reduce_run<VW, NB>(a, ws, pos_sorted, t, td.doff, s0, s1, lane, acc);
-    float g[NB][VW];
+    auto meta = [&](uint32_t c0, int& b, float& s) {
+        const uint32_t i = c0 + lane;
+        b = -1;
+        s = 1.f;
+        if (i < s1) {
+            const uint32_t pos = __ldg(pos_sorted + i);
+            if (pos < (uint32_t)a.N) {
+                const int64_t bag = (int64_t)__ldg(ws.bag + pos);
+                if (bag >= tB && bag < tB + a.B) b = (int)(bag - tB);
+                if (a.has_scale) s = __ldg(ws.scale + pos);
+            }
+        }
+    };
+    int cb;
+    float cs;
+    meta(s0, cb, cs);
+    for (uint32_t c0 = s0; c0 < s1; c0 += 32) {
+        int nb;
+        float ns;
+        meta(c0 + 32, nb, ns);
+        const int n = (int)tmin<uint32_t>(32u, s1 - c0);
+        for (int k0 = 0; k0 < n; k0 += GROUP) {
+            int bb[GROUP];
+            float ss[GROUP];
+            float g[GROUP][NB][VW];
 #pragma unroll
-    for (int q = 0; q < NB; ++q)
+            for (int u = 0; u < GROUP; ++u) {
+                const int src = (k0 + u) & 31;
+                bb[u] = __shfl_sync(0xffffffffu, cb, src);
+                ss[u] = __shfl_sync(0xffffffffu, cs, src);
+                if (k0 + u >= n) bb[u] = -1;
+                const float* grow = a.grad + (int64_t)(bb[u] < 0 ? 0 : bb[u]) * a.total_d + td.doff;
 #pragma unroll
-        for (int v = 0; v < VW; ++v) g[q][v] = acc[q][v].value();
-    update_row<DT, VW, NB>(a, td, key, (int64_t)key - td.rowbase, g, lane);
-}
-
-// Dispatch on the row shape: dim = 32, 64, 128, 256 use vector lanes when the
-// table rows and the gradient columns are aligned for them; anything else
-// runs element-wise.  Codes: 1 -> (VW 1, NB 1), 2 -> (2, 1), 3 -> (4, 1),
-// 4 -> (4, 2), 0 -> element-wise.
-__device__ __forceinline__ int shape_code(const TableDesc& td, int total_d, bool grad_vec) {
-    const bool rows16 = grad_vec && ((uintptr_t)td.data & 15u) == 0;
-    const bool a4 = rows16 && (td.doff % 4 == 0) && (total_d % 4 == 0);
-    const bool a2 = rows16 && (td.doff % 2 == 0) && (total_d % 2 == 0);
-    if (td.dim == 32) return 1;
-    if (td.dim == 64 && a2) return 2;
-    if (td.dim == 128 && a4) return 3;
-    if (td.dim == 256 && a4) return 4;
-    return 0;
-}
-
-template <int DT>
-__device__ void short_run_dispatch(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                   const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                                   int lane) {
-    switch (shape_code(td, a.total_d, a.grad_vec != 0)) {
-        case 1: short_run<DT, 1, 1>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-        case 2: short_run<DT, 2, 1>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-        case 3: short_run<DT, 4, 1>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-        case 4: short_run<DT, 4, 2>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-        default: reduce_update_generic<DT>(a, ws, pos_sorted, td, t, key, s0, s1, lane, nullptr, 0); break;
-    }
-}
-
-__global__ void __launch_bounds__(256) short_runs_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
-    a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], (uint32_t)a.N);
-    for (int64_t u = gw; u < U; u += nw) {
-        const uint32_t key = __ldg(ws.uniq + u);
-        if (key >= a.total_rows) continue;  // lookups with an index out of range
-        const uint32_t s0 = __ldg(ws.runstart + u), s1 = __ldg(ws.runstart + u + 1);
-        if (s1 > (uint32_t)a.N || s0 >= s1) continue;
-        const uint32_t len = s1 - s0;
-        if (len >= (uint32_t)kLongRun) {
-            uint32_t base = 0, li = 0;
-            const uint32_t nc = (len + kLongRun - 1) / kLongRun;
-            if (lane == 0) {
-                base = atomicAdd(&ws.counters[CTR_NCHUNK], nc);
-                li = atomicAdd(&ws.counters[CTR_NLONG], 1u);
-                if (li < ws.max_long && base + nc <= ws.max_chunks) {
-                    ws.long_runs[4 * li + 0] = (uint32_t)u;
-                    ws.long_runs[4 * li + 1] = base;
-                    ws.long_runs[4 * li + 2] = nc;
-                    ws.long_runs[4 * li + 3] = 0;  // chunks finished
+                for (int q = 0; q < NB; ++q) {
+                    if (bb[u] >= 0) {
+                        ld_grad<VW>(grow + S::col(lane, q), g[u][q]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
+                    }
                 }
             }
-            base = __shfl_sync(0xffffffffu, base, 0);
-            li = __shfl_sync(0xffffffffu, li, 0);
-            if (li < ws.max_long && base + nc <= ws.max_chunks)
-                for (uint32_t j = lane; j < nc; j += 32) ws.chunk_run[base + j] = li;
-            continue;
+#pragma unroll
+            for (int u = 0; u < GROUP; ++u)
+                if (bb[u] >= 0)
+#pragma unroll
+                    for (int q = 0; q < NB; ++q)
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) acc[q][v].add_scaled(ss[u], g[u][q][v]);
         }
-        const int t = table_of(a.tabs, a.T, key);
-        const TableDesc td = a.tabs[t];
-        switch (td.dtype) {
-            case DT_F32: short_run_dispatch<DT_F32>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-            case DT_F16: short_run_dispatch<DT_F16>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-            default: short_run_dispatch<DT_BF16>(a, ws, pos_sorted, td, t, key, s0, s1, lane); break;
-        }
+        cb = nb;
+        cs = ns;
     }
-}
-
-// ------------------------------------------------------------- long runs
-
-template <int DT, int VW, int NB>
-__device__ void long_chunk(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                           const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                           float* part_row, uint32_t li, int lane) {
-    Kahan acc[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    reduce_run<VW, NB>(a, ws, pos_sorted, t, td.doff, s0, s1, lane, acc);
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) part_row[Cols<VW, NB>::col(lane, q) + v] = acc[q][v].value();
+        for (int v = 0; v < VW; ++v) part_row[S::col(lane, q) + v] = acc[q][v].value();
 }
 
 template <int DT, int VW, int NB>
-__device__ void long_combine(const ApplyArgs& a, const TableDesc& td, uint32_t key, const float* part0,
-                             uint32_t nc, int lane) {
+__device__ __forceinline__ void long_combine(const ApplyArgs& a, const TableDesc& td, uint32_t key,
+                                             const float* part0, uint32_t nc, int lane) {
+    using S = Slice<DT, VW, NB>;
     Kahan acc[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
@@ -411,25 +564,29 @@ __device__ void long_combine(const ApplyArgs& a, const TableDesc& td, uint32_t k
 #pragma unroll
         for (int q = 0; q < NB; ++q)
 #pragma unroll
-            for (int v = 0; v < VW; ++v) acc[q][v].add(__ldcg(p + Cols<VW, NB>::col(lane, q) + v));
+            for (int v = 0; v < VW; ++v) acc[q][v].add(__ldcg(p + S::col(lane, q) + v));
     }
     float g[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
         for (int v = 0; v < VW; ++v) g[q][v] = acc[q][v].value();
-    update_row<DT, VW, NB>(a, td, key, (int64_t)key - td.rowbase, g, lane);
+    uint32_t row[S::WORDS];
+    const int64_t r = (int64_t)key - td.rowbase;
+    S::load(row, td.data, r, td.dim, lane);
+    const float m_old = a.opt == 2 ? a.state[key] : 0.f;
+    const float m = optimizer_step<DT, VW, NB>(a, td.dim, g, row, m_old);
+    S::store(row, td.data, r, td.dim, lane);
+    if (a.opt == 2 && lane == 0) a.state[key] = m;
 }
 
-template <int DT>
-__device__ void long_dispatch(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                              const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                              uint32_t chunk, uint32_t li, uint32_t base, uint32_t nc, int lane) {
+template <int DT, int CODE>
+__device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                          const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
+                                          uint32_t chunk, uint32_t li, uint32_t base, uint32_t nc, int lane) {
     float* part_row = ws.partial + (int64_t)chunk * a.max_dim;
-    const int code = shape_code(td, a.total_d, a.grad_vec != 0);
     // 1) this chunk's partial sum
-    if (code == 0) {
-        // element-wise: columns lane + 32*j, blocks of 256
+    if constexpr (CODE == SHAPE_GENERIC) {
         const int D = td.dim;
         const int64_t tB = (int64_t)t * a.B;
         for (int cb = 0; cb < D; cb += 256) {
@@ -455,14 +612,8 @@ __device__ void long_dispatch(const ApplyArgs& a, const Workspace& ws, const uin
                 if (c < D) part_row[c] = acc[j].value();
             }
         }
-    } else if (code == 1) {
-        long_chunk<DT, 1, 1>(a, ws, pos_sorted, td, t, key, s0, s1, part_row, li, lane);
-    } else if (code == 2) {
-        long_chunk<DT, 2, 1>(a, ws, pos_sorted, td, t, key, s0, s1, part_row, li, lane);
-    } else if (code == 3) {
-        long_chunk<DT, 4, 1>(a, ws, pos_sorted, td, t, key, s0, s1, part_row, li, lane);
     } else {
-        long_chunk<DT, 4, 2>(a, ws, pos_sorted, td, t, key, s0, s1, part_row, li, lane);
+        long_chunk_vec<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
     }
     // 2) the warp that finishes a run's last chunk combines all of them
     __threadfence();
@@ -473,50 +624,102 @@ __device__ void long_dispatch(const ApplyArgs& a, const Workspace& ws, const uin
     if (done != nc - 1) return;
     __threadfence();
     const float* part0 = ws.partial + (int64_t)base * a.max_dim;
-    switch (code) {
-        case 0: reduce_update_generic<DT>(a, ws, pos_sorted, td, t, key, 0, 0, lane, part0, (int)nc); break;
-        case 1: long_combine<DT, 1, 1>(a, td, key, part0, nc, lane); break;
-        case 2: long_combine<DT, 2, 1>(a, td, key, part0, nc, lane); break;
-        case 3: long_combine<DT, 4, 1>(a, td, key, part0, nc, lane); break;
-        default: long_combine<DT, 4, 2>(a, td, key, part0, nc, lane); break;
-    }
+    if constexpr (CODE == SHAPE_GENERIC)
+        generic_row<DT>(a, ws, pos_sorted, td, t, key, 0, 0, part0, nc, lane);
+    else
+        long_combine<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, td, key, part0, nc, lane);
+    // every chunk of this run has been counted: reset for the next apply call
+    if (lane == 0) ws.long_runs[4 * li + 3] = 0;
 }
 
-__global__ void __launch_bounds__(256) long_chunks_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
+// ------------------------------------------------------------------ kernel
+
+// All work of one backward class (table dtype DT, row shape CODE): first the
+// long-run chunks whose table is in the class, then the short-run batches of
+// the class's tables.  Work items go to warps round-robin.
+template <int DT, int CODE>
+__global__ void __launch_bounds__(256) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
     a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const uint32_t nchunks = min(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
-    const uint32_t nlong = min(*(volatile uint32_t*)&ws.counters[CTR_NLONG], (uint32_t)ws.max_long);
+    const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], (uint32_t)a.N);
+    const uint32_t nchunks = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
+    const uint32_t nlong = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NLONG], (uint32_t)ws.max_long);
+
     for (int64_t c = gw; c < nchunks; c += nw) {
         const uint32_t li = __ldg(ws.chunk_run + c);
         if (li >= nlong) continue;
         const uint32_t u = __ldg(ws.long_runs + 4 * li), base = __ldg(ws.long_runs + 4 * li + 1),
                        nc = __ldg(ws.long_runs + 4 * li + 2);
-        const uint32_t j = (uint32_t)c - base;
+        if (u >= U || c < base || c - base >= nc) continue;
         const uint32_t key = __ldg(ws.uniq + u);
-        const uint32_t r0 = __ldg(ws.runstart + u), r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
-        const uint32_t s0 = r0 + j * kLongRun, s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
         const int t = table_of(a.tabs, a.T, key);
+        if (a.tabs[t].cls != a.cls) continue;
         const TableDesc td = a.tabs[t];
-        switch (td.dtype) {
-            case DT_F32: long_dispatch<DT_F32>(a, ws, pos_sorted, td, t, key, s0, s1, (uint32_t)c, li, base, nc, lane); break;
-            case DT_F16: long_dispatch<DT_F16>(a, ws, pos_sorted, td, t, key, s0, s1, (uint32_t)c, li, base, nc, lane); break;
-            default: long_dispatch<DT_BF16>(a, ws, pos_sorted, td, t, key, s0, s1, (uint32_t)c, li, base, nc, lane); break;
+        const uint32_t r0 = __ldg(ws.runstart + u);
+        const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
+        const uint32_t s0 = r0 + ((uint32_t)c - base) * kLongRun;
+        const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
+        long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, (uint32_t)c, li, base, nc, lane);
+    }
+
+    // batch items: tables of the class in order, kBatchRows keys per item;
+    // item i of the whole class goes to warp i mod nw
+    int64_t off = 0;
+    for (int k = 0; k < a.class_count; ++k) {
+        const int t = a.class_tables[k];
+        const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
+        const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
+        const int64_t nb = (ue - us + kBatchRows - 1) / kBatchRows;
+        if (nb == 0) continue;
+        const TableDesc td = a.tabs[t];
+        const int64_t first = off + (((gw - off) % nw) + nw) % nw;
+        for (int64_t i = first; i < off + nb; i += nw) {
+            const uint32_t u0 = us + (uint32_t)(i - off) * kBatchRows;
+            short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kBatchRows, ue - u0), lane);
         }
+        off += nb;
     }
 }
 
-cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, cudaStream_t s) {
-    if (a.N == 0) return cudaSuccess;
-    const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
-    const unsigned grid = (unsigned)(a.num_sms * 8);
-    short_runs_kernel<<<grid, 256, 0, s>>>(a, ws, pos_sorted);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    long_chunks_kernel<<<grid, 256, 0, s>>>(a, ws, pos_sorted);
+template <int DT>
+static cudaError_t launch_dtype(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos, int code,
+                                unsigned grid, cudaStream_t s) {
+    switch (code) {
+        case SHAPE_D32: apply_class_kernel<DT, SHAPE_D32><<<grid, 256, 0, s>>>(a, ws, pos); break;
+        case SHAPE_D64: apply_class_kernel<DT, SHAPE_D64><<<grid, 256, 0, s>>>(a, ws, pos); break;
+        case SHAPE_D128: apply_class_kernel<DT, SHAPE_D128><<<grid, 256, 0, s>>>(a, ws, pos); break;
+        case SHAPE_D256: apply_class_kernel<DT, SHAPE_D256><<<grid, 256, 0, s>>>(a, ws, pos); break;
+        default: apply_class_kernel<DT, SHAPE_GENERIC><<<grid, 256, 0, s>>>(a, ws, pos); break;
+    }
     return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32_t* class_tables,
+                         const int* class_begin, const int* class_count, cudaStream_t s) {
+    if (a_in.N == 0) return cudaSuccess;
+    const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
+    const unsigned grid = (unsigned)(a_in.num_sms * 4);
+    for (int cls = 0; cls < kNumClasses; ++cls) {
+        if (class_count[cls] == 0) continue;
+        ApplyArgs a = a_in;
+        a.cls = cls;
+        a.class_tables = class_tables + class_begin[cls];
+        a.class_count = class_count[cls];
+        const int dt = cls / NUM_SHAPES;
+        // an unaligned gradient buffer rules out vector loads: element-wise
+        const int code = a.grad_vec ? cls % NUM_SHAPES : SHAPE_GENERIC;
+        cudaError_t e;
+        if (dt == DT_F32)
+            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, s);
+        else if (dt == DT_F16)
+            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, s);
+        else
+            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace tbe

@@ -6,15 +6,18 @@
 // W_t[idx_i, j], fp32 accumulation for fp32/fp16/bf16 rows.
 //
 // Schedule.  A row of D elements is nvec = D*elem/16 vectors of 16 bytes.  A
-// "slot" of G lanes (G = next power of two >= nvec, at most 32) covers one
-// row, each lane loading V vectors (V > 1 only when nvec > 32), and a warp
-// holds 32/G slots, one bag each.  The slot walks its bag's lookups in chunks:
-// the chunk's indices/weights are loaded cooperatively (coalesced) one chunk
-// ahead, then broadcast by shuffles, and U rows are kept in flight per lane.
-// The warp -> (table, bag) map is a prefix over tables of ceil(B / (32/G_t))
-// warps, computed on the device whenever B changes.  Bags longer than
-// kLongBag are handed to a second kernel where a whole CTA splits the bag
-// into eight contiguous pieces and adds the pieces' sums in a fixed order.
+// "slot" of G lanes covers up to 32 vectors of a row, one vector per lane
+// (G = next power of two >= nvec, at most 32).  A warp holds 32/G slots, one
+// bag each; rows wider than 32 vectors are split into column blocks of 32
+// vectors, each handled by its own warp.  A slot walks its bag's lookups in
+// chunks: the chunk's indices and weights are loaded cooperatively
+// (coalesced) one chunk ahead, then broadcast by shuffles, with U rows in
+// flight per lane.  The warp -> (table, bag group, column block) map is a
+// prefix over tables of ceil(B / (32/G_t)) * blocks_t warps, computed on the
+// device whenever B changes.  Bags longer than kLongBag are queued for a
+// second kernel where a whole CTA splits the bag into eight contiguous pieces,
+// sums each with compensated (Kahan) fp32 addition, and adds the pieces in a
+// fixed order.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -24,19 +27,22 @@ struct VecTraits {
     static constexpr int E = (DT == DT_F32) ? 4 : 8;  // elements per 16-byte vector
 };
 
-// Accumulate s_i * row(idx_i) over lookups [start, end) into acc.  The calling
-// slot has G lanes (mask = its lanes); lane `sub` owns vectors sub + v*G.
-template <int G, int V, int DT, typename IDX>
-__device__ __forceinline__ void gather_accumulate(const uint4* __restrict__ tab, int nvec,
+// Accumulate s_i * row(idx_i) over lookups [start, end) into acc (and comp,
+// the Kahan compensation, when KAHAN).  The calling slot has G lanes (mask =
+// its lanes); lane `sub` owns vector vi of every row.
+template <int G, int DT, typename IDX, bool KAHAN>
+__device__ __forceinline__ void gather_accumulate(const uint4* __restrict__ tab, int nvec, int vi,
                                                   int64_t rows, const IDX* __restrict__ indices,
                                                   const float* __restrict__ weights, int64_t start,
                                                   int64_t end, int sub, unsigned mask,
-                                                  float (&acc)[V][VecTraits<DT>::E], bool& oob) {
+                                                  float (&acc)[VecTraits<DT>::E],
+                                                  float (&comp)[VecTraits<DT>::E], bool& oob) {
     constexpr int E = VecTraits<DT>::E;
     constexpr int J = G >= 4 ? 1 : 4 / G;  // indices held per lane per chunk
     constexpr int C = G * J;               // lookups per chunk
-    constexpr int U = V == 1 ? 4 : (V == 2 ? 2 : 1);  // lookups in flight per step
+    constexpr int U = 4;                   // rows in flight per lane
     static_assert(C % U == 0, "chunk must split into steps");
+    const bool active = vi < nvec;
 
     int cr[J];
     float cw[J];
@@ -73,24 +79,29 @@ __device__ __forceinline__ void gather_accumulate(const uint4* __restrict__ tab,
                     r[u] = __shfl_sync(mask, cr[(k0 + u) / G], (k0 + u) % G, G);
                     w[u] = __shfl_sync(mask, cw[(k0 + u) / G], (k0 + u) % G, G);
                 }
-                uint4 x[U][V];
+                uint4 x[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        const int vi = sub + v * G;
-                        x[u][v] = make_uint4(0u, 0u, 0u, 0u);
-                        if (r[u] >= 0 && vi < nvec) x[u][v] = __ldg(tab + (int64_t)r[u] * nvec + vi);
-                    }
+                    x[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r[u] >= 0 && active) x[u] = __ldg(tab + (int64_t)r[u] * nvec + vi);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
+                    float f[E];
+                    unpack16<DT>(x[u], f);
+                    if constexpr (KAHAN) {
+                        if (r[u] >= 0) {
 #pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        float f[E];
-                        unpack16<DT>(x[u][v], f);
+                            for (int e = 0; e < E; ++e) {
+                                const float y = fmaf(w[u], f[e], -comp[e]);
+                                const float t = acc[e] + y;
+                                comp[e] = (t - acc[e]) - y;
+                                acc[e] = t;
+                            }
+                        }
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) acc[v][e] = fmaf(w[u], f[e], acc[v][e]);
+                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w[u], f[e], acc[e]);
                     }
                 }
             }
@@ -103,103 +114,110 @@ __device__ __forceinline__ void gather_accumulate(const uint4* __restrict__ tab,
     }
 }
 
-// Write one pooled row (this lane's vectors), dividing by L for mean pooling.
-template <int G, int V, int DT>
-__device__ __forceinline__ void write_row(float* __restrict__ orow, const float (&acc)[V][VecTraits<DT>::E],
-                                          int nvec, int sub, int64_t L, bool mean, bool vec_out) {
+// Write this lane's vector vi of a pooled row, dividing by L for mean pooling.
+template <int DT>
+__device__ __forceinline__ void write_vec(float* __restrict__ orow, const float (&acc)[VecTraits<DT>::E],
+                                          int nvec, int vi, int64_t L, bool mean, bool vec_out) {
     constexpr int E = VecTraits<DT>::E;
+    if (vi >= nvec) return;
     const float Lf = (float)L;
     const bool div = mean && L > 0;
+    float o[E];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int vi = sub + v * G;
-        if (vi < nvec) {
-            float o[E];
+    for (int e = 0; e < E; ++e) o[e] = div ? __fdiv_rn(acc[e], Lf) : acc[e];
+    float* dst = orow + (int64_t)vi * E;
+    if (vec_out) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = div ? __fdiv_rn(acc[v][e], Lf) : acc[v][e];
-            float* dst = orow + (int64_t)vi * E;
-            if (vec_out) {
+        for (int q = 0; q < E / 4; ++q)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    } else {
 #pragma unroll
-                for (int q = 0; q < E / 4; ++q)
-                    reinterpret_cast<float4*>(dst)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) dst[e] = o[e];
-            }
-        }
+        for (int e = 0; e < E; ++e) dst[e] = o[e];
     }
 }
 
-template <int G, int V, int DT, typename IDX>
-__device__ __forceinline__ void pool_bag_vec(const TableDesc& td, const FwdArgs& a, int64_t start,
-                                             int64_t end, float* orow, int sub, unsigned mask,
-                                             bool& oob) {
-    float acc[V][VecTraits<DT>::E];
+template <int G, int DT, typename IDX>
+__device__ __forceinline__ void pool_bag_vec(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
+                                             float* orow, int vi, int sub, unsigned mask, bool& oob) {
+    constexpr int E = VecTraits<DT>::E;
+    float acc[E], comp[E];
 #pragma unroll
-    for (int v = 0; v < V; ++v)
-#pragma unroll
-        for (int e = 0; e < VecTraits<DT>::E; ++e) acc[v][e] = 0.f;
-    gather_accumulate<G, V, DT, IDX>(reinterpret_cast<const uint4*>(td.data), td.row_bytes >> 4,
-                                     td.rows, reinterpret_cast<const IDX*>(a.indices), a.weights,
-                                     start, end, sub, mask, acc, oob);
-    write_row<G, V, DT>(orow, acc, td.row_bytes >> 4, sub, end - start, a.mean != 0, a.vec_out != 0);
+    for (int e = 0; e < E; ++e) acc[e] = comp[e] = 0.f;
+    const int nvec = td.row_bytes >> 4;
+    gather_accumulate<G, DT, IDX, false>(reinterpret_cast<const uint4*>(td.data), nvec, vi, td.rows,
+                                         reinterpret_cast<const IDX*>(a.indices), a.weights, start, end, sub,
+                                         mask, acc, comp, oob);
+    write_vec<DT>(orow, acc, nvec, vi, end - start, a.mean != 0, a.vec_out != 0);
 }
 
 template <int DT, typename IDX>
-__device__ __forceinline__ void pool_bag_vec_dispatch(const TableDesc& td, const FwdArgs& a,
-                                                      int64_t start, int64_t end, float* orow,
-                                                      int sub, unsigned mask, bool& oob) {
+__device__ __forceinline__ void pool_bag_vec_dispatch(const TableDesc& td, const FwdArgs& a, int64_t start,
+                                                      int64_t end, float* orow, int vi, int sub, unsigned mask,
+                                                      bool& oob) {
     switch (td.lanes) {
-        case 1: pool_bag_vec<1, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-        case 2: pool_bag_vec<2, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-        case 4: pool_bag_vec<4, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-        case 8: pool_bag_vec<8, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-        case 16: pool_bag_vec<16, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-        default:
-            if (td.vecs == 1)
-                pool_bag_vec<32, 1, DT, IDX>(td, a, start, end, orow, sub, mask, oob);
-            else if (td.vecs == 2)
-                pool_bag_vec<32, 2, DT, IDX>(td, a, start, end, orow, sub, mask, oob);
-            else
-                pool_bag_vec<32, 4, DT, IDX>(td, a, start, end, orow, sub, mask, oob);
-            break;
+        case 1: pool_bag_vec<1, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+        case 2: pool_bag_vec<2, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+        case 4: pool_bag_vec<4, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+        case 8: pool_bag_vec<8, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+        case 16: pool_bag_vec<16, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+        default: pool_bag_vec<32, DT, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
     }
 }
 
 // Element-wise path (rows that are not whole 16-byte vectors): one warp per
 // bag, lane owns columns lane + 32q of each 128-column block.
-template <int DT, typename IDX>
-__device__ void pool_bag_scalar(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
-                                float* orow, int lane, bool& oob) {
+template <int DT, typename IDX, bool KAHAN>
+__device__ void sum_bag_scalar(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end, int cb,
+                               int lane, float (&acc)[4], bool& oob) {
     const IDX* indices = reinterpret_cast<const IDX*>(a.indices);
     const int D = td.dim;
-    const int64_t L = end - start;
-    for (int cb = 0; cb < D; cb += 128) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int64_t c0 = start; c0 < end; c0 += 32) {
-            const int64_t p = c0 + lane;
-            int r = -1;
-            float w = 1.f;
-            if (p < end) {
-                const int64_t x = ld_index(indices, p);
-                if (x >= 0 && x < td.rows)
-                    r = (int)x;
-                else
-                    oob = true;
-                if (a.weights) w = __ldg(a.weights + p);
-            }
-            const int n = (int)tmin<int64_t>(32, end - c0);
-            for (int k = 0; k < n; ++k) {
-                const int rk = __shfl_sync(0xffffffffu, r, k);
-                const float wk = __shfl_sync(0xffffffffu, w, k);
-                if (rk < 0) continue;
+    float comp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = cb + lane + 32 * q;
-                    if (col < D) acc[q] = fmaf(wk, load_elem<DT>(td.data, (int64_t)rk * D + col), acc[q]);
+    for (int q = 0; q < 4; ++q) acc[q] = 0.f;
+    for (int64_t c0 = start; c0 < end; c0 += 32) {
+        const int64_t p = c0 + lane;
+        int r = -1;
+        float w = 1.f;
+        if (p < end) {
+            const int64_t x = ld_index(indices, p);
+            if (x >= 0 && x < td.rows)
+                r = (int)x;
+            else
+                oob = true;
+            if (a.weights) w = __ldg(a.weights + p);
+        }
+        const int n = (int)tmin<int64_t>(32, end - c0);
+        for (int k = 0; k < n; ++k) {
+            const int rk = __shfl_sync(0xffffffffu, r, k);
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (rk < 0) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = cb + lane + 32 * q;
+                if (col < D) {
+                    const float f = load_elem<DT>(td.data, (int64_t)rk * D + col);
+                    if constexpr (KAHAN) {
+                        const float y = fmaf(wk, f, -comp[q]);
+                        const float t = acc[q] + y;
+                        comp[q] = (t - acc[q]) - y;
+                        acc[q] = t;
+                    } else {
+                        acc[q] = fmaf(wk, f, acc[q]);
+                    }
                 }
             }
         }
+    }
+}
+
+template <int DT, typename IDX>
+__device__ void pool_bag_scalar(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
+                                float* orow, int lane, bool& oob) {
+    const int D = td.dim;
+    const int64_t L = end - start;
+    for (int cb = 0; cb < D; cb += 128) {
+        float acc[4];
+        sum_bag_scalar<DT, IDX, false>(td, a, start, end, cb, lane, acc, oob);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int col = cb + lane + 32 * q;
@@ -241,15 +259,24 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(FwdArgs a) {
     }
     const int t = lo;
     const TableDesc td = a.tabs[t];
-    const int G = td.path == PATH_VEC ? td.lanes : 32;
+    const bool vec = td.path == PATH_VEC;
+    const int G = vec ? td.lanes : 32;
+    const int ncb = vec ? td.vecs : 1;  // column blocks of 32 vectors
     const int slot = lane / G, sub = lane % G;
-    const int b = (gw - td.warp_begin) * (32 / G) + slot;
+    const int w = gw - td.warp_begin;
+    const int cb = w % ncb;
+    const int b = (w / ncb) * (32 / G) + slot;
     if (b >= a.B) return;  // the whole slot leaves together
     const unsigned mask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (slot * G));
     const int64_t bag = (int64_t)t * a.B + b;
     int64_t start, end;
-    bag_range<IDX>(a, bag, start, end, sub == 0);
+    bag_range<IDX>(a, bag, start, end, sub == 0 && cb == 0);
+    float* orow = a.out + (int64_t)b * a.total_d + td.doff;
+    bool oob = false;
     if (end - start > kLongBag) {
+        // queued once (by column block 0) for the CTA kernel; if the queue is
+        // full, column block 0 pools every column block of the bag itself
+        if (cb != 0) return;
         int queued = 0;
         if (sub == 0) {
             const uint32_t k = atomicAdd(&a.blk->long_count[a.parity], 1u);
@@ -259,15 +286,25 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(FwdArgs a) {
             }
         }
         queued = __shfl_sync(mask, queued, 0, G);
-        if (queued) return;  // pooled by fwd_long_kernel
+        if (queued) return;
+        if (vec) {
+            for (int c = 0; c < ncb; ++c) {
+                switch (td.dtype) {
+                    case DT_F32: pool_bag_vec_dispatch<DT_F32, IDX>(td, a, start, end, orow, c * 32 + sub, sub, mask, oob); break;
+                    case DT_F16: pool_bag_vec_dispatch<DT_F16, IDX>(td, a, start, end, orow, c * 32 + sub, sub, mask, oob); break;
+                    default: pool_bag_vec_dispatch<DT_BF16, IDX>(td, a, start, end, orow, c * 32 + sub, sub, mask, oob); break;
+                }
+            }
+            if (__any_sync(mask, oob) && sub == 0) atomicOr(&a.blk->error, ERR_OOB);
+            return;
+        }
     }
-    float* orow = a.out + (int64_t)b * a.total_d + td.doff;
-    bool oob = false;
-    if (td.path == PATH_VEC) {
+    if (vec) {
+        const int vi = cb * 32 + sub;
         switch (td.dtype) {
-            case DT_F32: pool_bag_vec_dispatch<DT_F32, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-            case DT_F16: pool_bag_vec_dispatch<DT_F16, IDX>(td, a, start, end, orow, sub, mask, oob); break;
-            default: pool_bag_vec_dispatch<DT_BF16, IDX>(td, a, start, end, orow, sub, mask, oob); break;
+            case DT_F32: pool_bag_vec_dispatch<DT_F32, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+            case DT_F16: pool_bag_vec_dispatch<DT_F16, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
+            default: pool_bag_vec_dispatch<DT_BF16, IDX>(td, a, start, end, orow, vi, sub, mask, oob); break;
         }
     } else {
         switch (td.dtype) {
@@ -284,36 +321,39 @@ __global__ void __launch_bounds__(256) fwd_pool_kernel(FwdArgs a) {
 constexpr int kLongWarps = 8;
 constexpr int kLongMaxFloats = 1024;  // floats of one row held per warp in shared memory
 
-template <int V, int DT, typename IDX>
-__device__ void long_bag_vec(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
-                             float* orow, float (*part)[kLongMaxFloats], bool& oob) {
+template <int DT, typename IDX>
+__device__ void long_bag_vec(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end, float* orow,
+                             float (*part)[kLongMaxFloats], bool& oob) {
     constexpr int E = VecTraits<DT>::E;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = td.row_bytes >> 4;
     const int64_t L = end - start;
     const int64_t s0 = start + L * warp / kLongWarps;
     const int64_t s1 = start + L * (warp + 1) / kLongWarps;
-    float acc[V][E];
+    for (int cb = 0; cb * 32 < nvec; ++cb) {
+        const int vi = cb * 32 + lane;
+        float acc[E], comp[E];
 #pragma unroll
-    for (int v = 0; v < V; ++v)
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
-    gather_accumulate<32, V, DT, IDX>(reinterpret_cast<const uint4*>(td.data), nvec, td.rows,
-                                      reinterpret_cast<const IDX*>(a.indices), a.weights, s0, s1,
-                                      lane, 0xffffffffu, acc, oob);
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int vi = lane + 32 * v;
+        for (int e = 0; e < E; ++e) acc[e] = comp[e] = 0.f;
+        gather_accumulate<32, DT, IDX, true>(reinterpret_cast<const uint4*>(td.data), nvec, vi, td.rows,
+                                             reinterpret_cast<const IDX*>(a.indices), a.weights, s0, s1, lane,
+                                             0xffffffffu, acc, comp, oob);
         if (vi < nvec)
 #pragma unroll
-            for (int e = 0; e < E; ++e) part[warp][vi * E + e] = acc[v][e];
+            for (int e = 0; e < E; ++e) part[warp][vi * E + e] = acc[e] - comp[e];
     }
     __syncthreads();
     const int D = td.dim;
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float s = 0.f;
+        float s = 0.f, cmp = 0.f;
 #pragma unroll
-        for (int w = 0; w < kLongWarps; ++w) s += part[w][c];  // fixed order
+        for (int w = 0; w < kLongWarps; ++w) {  // fixed order
+            const float y = part[w][c] - cmp;
+            const float t = s + y;
+            cmp = (t - s) - y;
+            s = t;
+        }
+        s -= cmp;
         orow[c] = (a.mean && L > 0) ? __fdiv_rn(s, (float)L) : s;
     }
     __syncthreads();
@@ -323,70 +363,36 @@ template <int DT, typename IDX>
 __device__ void long_bag_scalar(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
                                 float* orow, float (*part)[kLongMaxFloats], bool& oob) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const IDX* indices = reinterpret_cast<const IDX*>(a.indices);
     const int D = td.dim;
     const int64_t L = end - start;
     const int64_t s0 = start + L * warp / kLongWarps;
     const int64_t s1 = start + L * (warp + 1) / kLongWarps;
     for (int cb = 0; cb < D; cb += 128) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int64_t c0 = s0; c0 < s1; c0 += 32) {
-            const int64_t p = c0 + lane;
-            int r = -1;
-            float w = 1.f;
-            if (p < s1) {
-                const int64_t x = ld_index(indices, p);
-                if (x >= 0 && x < td.rows)
-                    r = (int)x;
-                else
-                    oob = true;
-                if (a.weights) w = __ldg(a.weights + p);
-            }
-            const int n = (int)tmin<int64_t>(32, s1 - c0);
-            for (int k = 0; k < n; ++k) {
-                const int rk = __shfl_sync(0xffffffffu, r, k);
-                const float wk = __shfl_sync(0xffffffffu, w, k);
-                if (rk < 0) continue;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = cb + lane + 32 * q;
-                    if (col < D) acc[q] = fmaf(wk, load_elem<DT>(td.data, (int64_t)rk * D + col), acc[q]);
-                }
-            }
-        }
+        float acc[4];
+        sum_bag_scalar<DT, IDX, true>(td, a, s0, s1, cb, lane, acc, oob);
 #pragma unroll
         for (int q = 0; q < 4; ++q) part[warp][lane + 32 * q] = acc[q];
         __syncthreads();
         for (int c = threadIdx.x; c < 128 && cb + c < D; c += blockDim.x) {
-            float s = 0.f;
+            float s = 0.f, cmp = 0.f;
 #pragma unroll
-            for (int w = 0; w < kLongWarps; ++w) s += part[w][c];
+            for (int w = 0; w < kLongWarps; ++w) {
+                const float y = part[w][c] - cmp;
+                const float t = s + y;
+                cmp = (t - s) - y;
+                s = t;
+            }
+            s -= cmp;
             orow[cb + c] = (a.mean && L > 0) ? __fdiv_rn(s, (float)L) : s;
         }
         __syncthreads();
     }
 }
 
-template <int DT, typename IDX>
-__device__ void long_bag(const TableDesc& td, const FwdArgs& a, int64_t start, int64_t end,
-                         float* orow, float (*part)[kLongMaxFloats], bool& oob) {
-    if (td.path != PATH_VEC) {
-        long_bag_scalar<DT, IDX>(td, a, start, end, orow, part, oob);
-        return;
-    }
-    const int nvec = td.row_bytes >> 4;
-    if (nvec <= 32)
-        long_bag_vec<1, DT, IDX>(td, a, start, end, orow, part, oob);
-    else if (nvec <= 64)
-        long_bag_vec<2, DT, IDX>(td, a, start, end, orow, part, oob);
-    else
-        long_bag_vec<4, DT, IDX>(td, a, start, end, orow, part, oob);
-}
-
 template <typename IDX>
 __global__ void __launch_bounds__(256) fwd_long_kernel(FwdArgs a) {
     __shared__ float part[kLongWarps][kLongMaxFloats];
-    const uint32_t cnt = min(*(volatile uint32_t*)&a.blk->long_count[a.parity], (uint32_t)kLongBagCap);
+    const uint32_t cnt = tmin(*(volatile uint32_t*)&a.blk->long_count[a.parity], (uint32_t)kLongBagCap);
     bool oob = false;
     for (uint32_t i = blockIdx.x; i < cnt; i += gridDim.x) {
         const int64_t bag = (int64_t)a.blk->long_bags[a.parity][i];
@@ -396,10 +402,18 @@ __global__ void __launch_bounds__(256) fwd_long_kernel(FwdArgs a) {
         int64_t start, end;
         bag_range<IDX>(a, bag, start, end, false);
         float* orow = a.out + (int64_t)b * a.total_d + td.doff;
-        switch (td.dtype) {
-            case DT_F32: long_bag<DT_F32, IDX>(td, a, start, end, orow, part, oob); break;
-            case DT_F16: long_bag<DT_F16, IDX>(td, a, start, end, orow, part, oob); break;
-            default: long_bag<DT_BF16, IDX>(td, a, start, end, orow, part, oob); break;
+        if (td.path == PATH_VEC) {
+            switch (td.dtype) {
+                case DT_F32: long_bag_vec<DT_F32, IDX>(td, a, start, end, orow, part, oob); break;
+                case DT_F16: long_bag_vec<DT_F16, IDX>(td, a, start, end, orow, part, oob); break;
+                default: long_bag_vec<DT_BF16, IDX>(td, a, start, end, orow, part, oob); break;
+            }
+        } else {
+            switch (td.dtype) {
+                case DT_F32: long_bag_scalar<DT_F32, IDX>(td, a, start, end, orow, part, oob); break;
+                case DT_F16: long_bag_scalar<DT_F16, IDX>(td, a, start, end, orow, part, oob); break;
+                default: long_bag_scalar<DT_BF16, IDX>(td, a, start, end, orow, part, oob); break;
+            }
         }
     }
     if (oob) atomicOr(&a.blk->error, ERR_OOB);
@@ -409,15 +423,18 @@ __global__ void __launch_bounds__(256) fwd_long_kernel(FwdArgs a) {
 }
 
 // Warp map for batch size B: warp_begin[t] = sum over earlier non-histogram
-// tables of ceil(B / (32 / G_u)).  One small CTA, launched when B changes.
+// tables of ceil(B / (32 / G_u)) * blocks_u.  One small CTA, launched when B
+// changes.
 __global__ void fwd_schedule_kernel(TableDesc* tabs, int T, int B) {
     if (threadIdx.x != 0) return;
     int acc = 0;
     for (int t = 0; t < T; ++t) {
         tabs[t].warp_begin = acc;
         if (tabs[t].path == PATH_HIST) continue;
-        const int per = tabs[t].path == PATH_VEC ? 32 / tabs[t].lanes : 1;
-        acc += (B + per - 1) / per;
+        const bool vec = tabs[t].path == PATH_VEC;
+        const int per = vec ? 32 / tabs[t].lanes : 1;
+        const int blocks = vec ? tabs[t].vecs : 1;
+        acc += (B + per - 1) / per * blocks;
     }
 }
 

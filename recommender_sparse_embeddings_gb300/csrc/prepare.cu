@@ -55,6 +55,27 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_
 
 constexpr int kKeysWindow = kSortTile + 1;  // offsets staged per tile
 
+// Largest k in [0, nbags] with off[k] <= p, found by the whole block: each
+// round the threads test evenly spaced candidates of the remaining interval
+// and a block-wide count of "off[k] <= p" narrows it 256-fold, so two million
+// bags take three rounds of one load each.  Malformed (non-monotone) offsets
+// give some in-range answer.
+template <typename IDX>
+__device__ __forceinline__ int64_t block_find_bag(const IDX* off, int64_t nbags, int64_t p) {
+    int64_t lo = 0, hi = nbags + 1;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int64_t step = (hi - lo + blockDim.x - 1) / blockDim.x;
+        const int64_t k = lo + (int64_t)threadIdx.x * step;
+        const bool pred = k < hi && ld_index(off, k) <= p;
+        const int c = __syncthreads_count(pred);
+        const int64_t nlo = lo + (int64_t)(c > 0 ? c - 1 : 0) * step;
+        const int64_t nhi = tmin<int64_t>(hi, lo + (int64_t)(c > 0 ? c : 1) * step);
+        lo = nlo;
+        hi = tmax<int64_t>(nhi, nlo + 1);
+    }
+    return lo;
+}
+
 template <typename IDX>
 __device__ __forceinline__ int64_t upper_bound_global(const IDX* off, int64_t lo, int64_t hi, int64_t p) {
     // first k in [lo, hi) with off[k] > p (hi if none)
@@ -96,9 +117,13 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
         const int64_t p0 = tile * kSortTile;
         const int64_t p1 = min(p0 + (int64_t)kSortTile, a.N);
         __syncthreads();
-        if (threadIdx.x == 0) {
-            s_first = tmax<int64_t>(upper_bound_global(off, 0, nbags + 1, p0) - 1, 0);
-            s_last = tmax<int64_t>(upper_bound_global(off, 0, nbags + 1, p1 - 1) - 1, 0);
+        {
+            const int64_t f = block_find_bag(off, nbags, p0);
+            const int64_t l = block_find_bag(off, nbags, p1 - 1);
+            if (threadIdx.x == 0) {
+                s_first = f;
+                s_last = l;
+            }
         }
         __syncthreads();
         const int64_t bf = s_first, bl = min(s_last, nbags - 1);
@@ -310,12 +335,54 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(const uint32_t* __res
     }
 }
 
+// ---------------------------------------------------------- long runs
+
+// Registers every run of at least kLongRun lookups for the accumulate path:
+// ceil(len / kLongRun) consecutive chunk slots and a record (unique index,
+// first chunk, chunk count, chunks finished = 0), and finds where each
+// table's distinct keys start.  Depends only on the sorted keys, so it
+// belongs to the preparation step.
+__global__ void __launch_bounds__(256) classify_kernel(PrepArgs a, Workspace ws) {
+    const uint32_t N = (uint32_t)a.N, total_rows = a.total_rows;
+    const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], N);
+    // keys are sorted and each table owns a consecutive key range;
+    // ustart[T] ends the last table's range (skipped lookups come after)
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t <= a.T; t += gridDim.x * blockDim.x) {
+        const uint64_t target = t < a.T ? (uint64_t)a.tabs[t].rowbase : (uint64_t)total_rows;
+        uint32_t lo = 0, hi = U;
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if ((uint64_t)__ldg(ws.uniq + mid) < target)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        ws.ustart[t] = lo;
+    }
+    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < U; u += gridDim.x * blockDim.x) {
+        if (__ldg(ws.uniq + u) >= total_rows) continue;  // skipped lookups
+        const uint32_t s0 = __ldg(ws.runstart + u);
+        const uint32_t s1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), N);
+        if (s1 <= s0 || s1 - s0 < (uint32_t)kLongRun) continue;
+        const uint32_t nc = (s1 - s0 + kLongRun - 1) / kLongRun;
+        const uint32_t base = atomicAdd(&ws.counters[CTR_NCHUNK], nc);
+        const uint32_t li = atomicAdd(&ws.counters[CTR_NLONG], 1u);
+        if (li < ws.max_long && (int64_t)base + nc <= ws.max_chunks) {
+            ws.long_runs[4 * li + 0] = u;
+            ws.long_runs[4 * li + 1] = base;
+            ws.long_runs[4 * li + 2] = nc;
+            ws.long_runs[4 * li + 3] = 0;
+            for (uint32_t j = 0; j < nc; ++j) ws.chunk_run[base + j] = li;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launch
 
 cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     if (a.N == 0) {
         ws.sorted_buf = 0;
-        return cudaSuccess;
+        return cudaMemsetAsync(ws.ustart, 0, sizeof(uint32_t) * (a.T + 1), s);
     }
     const int tiles = (int)((a.N + kSortTile - 1) / kSortTile);
     int dev = 0, sms = 148;
@@ -347,6 +414,10 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     ws.sorted_buf = cur;
     rle_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, ws.uniq, ws.runstart, ws.rle_status,
                                               ws.counters, &a.blk->error);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const unsigned cgrid = (unsigned)tmax<int64_t>(1, tmin<int64_t>((a.N + 255) / 256, (int64_t)sms * 4));
+    classify_kernel<<<cgrid, 256, 0, s>>>(a, ws);
     return cudaGetLastError();
 }
 

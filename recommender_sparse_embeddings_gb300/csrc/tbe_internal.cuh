@@ -22,9 +22,9 @@ constexpr int kLongBag = 2048;
 constexpr int kLongBagCap = 1 << 16;
 // Runs of at least this many lookups take the chunked accumulate path.
 constexpr int kLongRun = 256;
-// Keys per tile of the sort and run-length kernels (256 threads x 16).
+// Keys per tile of the sort and run-length kernels (256 threads x 8).
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 16;
+constexpr int kSortItems = 8;
 constexpr int kSortTile = kSortThreads * kSortItems;
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
@@ -45,9 +45,11 @@ struct TableDesc {
     int32_t dtype;      // DT_*
     int32_t row_bytes;  // dim * element size
     int32_t path;       // PATH_*
-    int32_t lanes;      // lanes per row in the vector path (power of 2, <= 32)
-    int32_t vecs;       // 16-byte vectors per lane per row (vector path, 1..4)
+    int32_t lanes;      // lanes per row slice in the vector path (power of 2, <= 32)
+    int32_t vecs;       // column blocks of 32 vectors per row (vector path, 1..4)
     int32_t warp_begin; // first warp of this table in the forward warp map
+    int32_t cls;        // backward class: dtype * NUM_SHAPES + row shape code
+    int32_t pad_;
 };
 
 // Device-resident descriptor block owned by a handle.
@@ -207,6 +209,7 @@ struct Workspace {
     uint32_t* runstart;   // [N+1]
     uint32_t* long_runs;  // [max_long][4]: unique index, first chunk, chunk count, chunks done
     uint32_t* chunk_run;  // [max_chunks]: long-run index of each chunk
+    uint32_t* ustart;     // [T+1]: first distinct-key index of each table (ustart[T]: end)
     float* partial;       // [max_chunks][max_dim]
     int64_t max_long;
     int64_t max_chunks;
@@ -241,6 +244,12 @@ struct PrepArgs {
     int key_bits;
 };
 
+// Backward row-shape codes: dim 32, 64, 128, 256 with aligned rows and
+// gradient columns get vector lanes (VW columns per lane, NB blocks of 32*VW);
+// every other table is element-wise (code 0).
+enum : int { SHAPE_GENERIC = 0, SHAPE_D32 = 1, SHAPE_D64 = 2, SHAPE_D128 = 3, SHAPE_D256 = 4, NUM_SHAPES = 5 };
+constexpr int kNumClasses = 3 * NUM_SHAPES;
+
 cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s);
 
 struct ApplyArgs {
@@ -260,8 +269,14 @@ struct ApplyArgs {
     float eps;
     float* state;
     int num_sms;
+    const int32_t* class_tables;  // tables of the launched class (device)
+    int class_count;
+    int cls;
 };
 
-cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, cudaStream_t s);
+// One launch per backward class present: class_tables lists the tables of
+// every class (device, grouped by class); class_begin/class_count index it.
+cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, const int32_t* class_tables,
+                         const int* class_begin, const int* class_count, cudaStream_t s);
 
 }  // namespace tbe
