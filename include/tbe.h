@@ -50,8 +50,9 @@
  * 1 without weights), times 1/L for mean pooling (L = the bag's CSR length);
  * an empty bag pools to 0.
  *
- * Limits: sum of all tables' rows < 2^32 - 1; every table's rows < 2^31;
- * N < 2^30 lookups per call; T*B < 2^31; dim in [1, 4096].
+ * Limits: at most 4096 tables; sum of all tables' rows < 2^32 - 1; every
+ * table's rows < 2^31; N < 2^30 lookups per call; T*B < 2^31; dim in
+ * [1, 4096].
  */
 #ifndef TBE_GB300_H
 #define TBE_GB300_H

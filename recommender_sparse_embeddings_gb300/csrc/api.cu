@@ -179,6 +179,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     if (!out) return TBE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
+    if (num_tables > kMaxTables) return TBE_ERR_UNSUPPORTED;
     if (pooling != TBE_POOL_SUM && pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
     if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM)) return TBE_ERR_INVALID_ARG;
     tbe_handle* h = new (std::nothrow) tbe_handle();

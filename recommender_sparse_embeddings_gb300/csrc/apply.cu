@@ -202,51 +202,27 @@ __device__ __forceinline__ float optimizer_step(const ApplyArgs& a, int dim, con
 
 // ------------------------------------------------------------- short runs
 
-// Per-lookup metadata of one 32-lookup chunk, lane k holding lookup c0+k:
-// slot = position of its key among the keys of the current piece, or -1 when
-// the lookup is past the end or belongs to a key outside the piece;
-// b = bag row within the table; s = scale.
+// Metadata of 32 sorted lookups, lane k holding lookup w + k: b = bag row
+// within the table (-1 past the batch's lookups or if the bag is out of
+// range), s = scale.
 struct Meta {
-    int slot;
     int b;
     float s;
 };
 
-// Largest batch row l (0..15) whose first sorted slot rs_l <= i; rs of row l
-// is held by lane l (lane n holds the end of the last row, later lanes N).
-__device__ __forceinline__ int row_in_batch(uint32_t rs, uint32_t i) {
-    int lo = 0, hi = kBatchRows - 1;
-#pragma unroll
-    for (int step = 0; step < 4; ++step) {
-        const int mid = (lo + hi + 1) >> 1;
-        const uint32_t v = __shfl_sync(0xffffffffu, rs, mid);
-        if (v <= i)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ void load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                          uint32_t rs, uint32_t piece, uint32_t c0, uint32_t E1, int64_t tB,
-                                          int lane, Meta& m) {
-    const uint32_t i = c0 + lane;
-    const int r = row_in_batch(rs, i < E1 ? i : (E1 > 0 ? E1 - 1 : 0));
-    m.slot = -1;
-    m.b = 0;
-    m.s = 1.f;
-    if (i < E1 && ((piece >> r) & 1u)) {
+__device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                          uint32_t w, uint32_t Eend, int64_t tB, int lane) {
+    const uint32_t i = w + lane;
+    Meta m{-1, 1.f};
+    if (i < Eend) {
         const uint32_t pos = __ldg(pos_sorted + i);
         if (pos < (uint32_t)a.N) {
             const int64_t bag = (int64_t)__ldg(ws.bag + pos);
-            if (bag >= tB && bag < tB + a.B) {
-                m.slot = __popc(piece & ((1u << r) - 1u));
-                m.b = (int)(bag - tB);
-                if (a.has_scale) m.s = __ldg(ws.scale + pos);
-            }
+            if (bag >= tB && bag < tB + a.B) m.b = (int)(bag - tB);
+            if (a.has_scale) m.s = __ldg(ws.scale + pos);
         }
     }
+    return m;
 }
 
 // Gradient rows in flight per lane (GROUP) and keys per piece (R), whose
@@ -263,61 +239,91 @@ struct ShortTune {
     static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
 };
 
+// A sliding window over the batch's sorted lookups: metadata of lookups
+// [w0, w0 + 64) in two 32-lookup halves; the next half is fetched as soon as
+// the stream passes the middle, so it is in flight 32 lookups ahead.
+struct MetaWindow {
+    uint32_t w0;
+    Meta m0, m1;
+};
+
+// One batch: distinct keys [u0, u0 + n) of table t (n <= kBatchRows).  Short
+// keys are taken in pieces of at most R consecutive keys (a long or skipped
+// key ends a piece, so a piece's lookups are exactly its keys' sorted slots);
+// each piece's table rows are read first, then its lookups stream through
+// the window and each is added to its key's sum, then each key gets its
+// optimizer step.
 template <int DT, int VW, int NB>
-__device__ __forceinline__ void short_piece(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                            const TableDesc& td, int t, uint32_t rs, uint32_t key, float mstate,
-                                            uint32_t piece, int lane) {
+__device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                                const TableDesc& td, int t, uint32_t rs, uint32_t key, float mstate,
+                                                uint32_t rows, int lane) {
     using Tn = ShortTune<DT, VW, NB>;
     using S = Slice<DT, VW, NB>;
     constexpr int R = Tn::R;
     constexpr int GROUP = Tn::GROUP;
     constexpr int WORDS = S::WORDS;
     const int64_t tB = (int64_t)t * a.B;
-    const int first = __ffs(piece) - 1;
-    const int last = 31 - __clz(piece);
-    const uint32_t E0 = __shfl_sync(0xffffffffu, rs, first);
-    const uint32_t E1 = __shfl_sync(0xffffffffu, rs, last + 1);
+    const int lastrow = 31 - __clz(rows);
+    const uint32_t Eend = __shfl_sync(0xffffffffu, rs, lastrow + 1);
 
-    // old values of the piece's rows (slot s = s-th set bit of piece), read
-    // now so the loads overlap the gradient gather below
-    uint32_t wrow[R][WORDS];
+    MetaWindow win;
+    win.w0 = 0xffffffffu;
+    while (rows) {
+        // the next piece: consecutive short keys [f, f + nk)
+        const int f = __ffs(rows) - 1;
+        int nk = 1;
 #pragma unroll
-    for (int s = 0; s < R; ++s) {
-        uint32_t m = piece;  // drop the s lowest set bits: the next one is slot s
-#pragma unroll
-        for (int k = 0; k < s; ++k) m &= m - 1u;
-        const int r = m ? __ffs(m) - 1 : 0;
-        const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
-        if (m) S::load(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
-    }
+        for (int k = 1; k < R; ++k)
+            if (nk == k && ((rows >> (f + k)) & 1u)) nk = k + 1;
+        rows &= ~(((1u << nk) - 1u) << f);
+        const uint32_t E0 = __shfl_sync(0xffffffffu, rs, f);
+        const uint32_t E1 = __shfl_sync(0xffffffffu, rs, f + nk);
 
-    float acc[R][NB][VW];
+        // table rows of the piece (their loads overlap the stream below)
+        uint32_t wrow[R][WORDS];
 #pragma unroll
-    for (int s = 0; s < R; ++s)
+        for (int s = 0; s < R; ++s) {
+            const uint32_t kr = __shfl_sync(0xffffffffu, key, (f + s) & 31);
+            if (s < nk) S::load(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
+        }
+        // window at the piece's first lookup
+        if (win.w0 == 0xffffffffu || E0 < win.w0 || E0 >= win.w0 + 64) {
+            win.w0 = E0;
+            win.m0 = load_meta(a, ws, pos_sorted, E0, Eend, tB, lane);
+            win.m1 = load_meta(a, ws, pos_sorted, E0 + 32, Eend, tB, lane);
+        }
+        float acc[R][NB][VW];
 #pragma unroll
-        for (int q = 0; q < NB; ++q)
+        for (int s = 0; s < R; ++s)
 #pragma unroll
-            for (int v = 0; v < VW; ++v) acc[s][q][v] = 0.f;
+            for (int q = 0; q < NB; ++q)
+#pragma unroll
+                for (int v = 0; v < VW; ++v) acc[s][q][v] = 0.f;
 
-    // stream the piece's lookups in sorted order
-    Meta cm;
-    load_meta(a, ws, pos_sorted, rs, piece, E0, E1, tB, lane, cm);
-    for (uint32_t c0 = E0; c0 < E1; c0 += 32) {
-        Meta nm;
-        load_meta(a, ws, pos_sorted, rs, piece, c0 + 32, E1, tB, lane, nm);
-        const int n = (int)tmin<uint32_t>(32u, E1 - c0);
-        for (int k0 = 0; k0 < n; k0 += GROUP) {
+        for (uint32_t i = E0; i < E1; i += GROUP) {
+            while (i >= win.w0 + 32) {  // slide: keep [w0, w0 + 64) ahead of i
+                win.m0 = win.m1;
+                win.w0 += 32;
+                win.m1 = load_meta(a, ws, pos_sorted, win.w0 + 32, Eend, tB, lane);
+            }
             int sl[GROUP];
             float ss[GROUP];
             float g[GROUP][NB][VW];
 #pragma unroll
             for (int u = 0; u < GROUP; ++u) {
-                const int src = (k0 + u) & 31;
-                sl[u] = __shfl_sync(0xffffffffu, cm.slot, src);
-                const int b = __shfl_sync(0xffffffffu, cm.b, src);
-                ss[u] = __shfl_sync(0xffffffffu, cm.s, src);
-                if (k0 + u >= n) sl[u] = -1;
-                const float* grow = a.grad + (int64_t)b * a.total_d + td.doff;
+                const uint32_t e = i + u - win.w0;  // 0..63
+                const int src = (int)(e & 31u);
+                const bool hi = e >= 32u;
+                const int b0 = __shfl_sync(0xffffffffu, win.m0.b, src);
+                const int b1 = __shfl_sync(0xffffffffu, win.m1.b, src);
+                const float s0 = __shfl_sync(0xffffffffu, win.m0.s, src);
+                const float s1 = __shfl_sync(0xffffffffu, win.m1.s, src);
+                const int b = hi ? b1 : b0;
+                ss[u] = hi ? s1 : s0;
+                // slot of lookup i+u: how many of the piece's later keys start at or before it
+                const int slot = __popc(__ballot_sync(0xffffffffu, lane > f && lane < f + nk && rs <= i + u));
+                sl[u] = (i + u < E1 && b >= 0) ? slot : -1;
+                const float* grow = a.grad + (int64_t)(b < 0 ? 0 : b) * a.total_d + td.doff;
 #pragma unroll
                 for (int q = 0; q < NB; ++q) {
                     if (sl[u] >= 0) {
@@ -341,21 +347,17 @@ __device__ __forceinline__ void short_piece(const ApplyArgs& a, const Workspace&
                         for (int v = 0; v < VW; ++v) acc[s][q][v] = fmaf(w, g[u][q][v], acc[s][q][v]);
                 }
         }
-        cm = nm;
-    }
-
-    // one optimizer step per key of the piece
-    uint32_t m = piece;
+        // one optimizer step per key of the piece
 #pragma unroll
-    for (int s = 0; s < R; ++s) {
-        if (m) {
-            const int r = __ffs(m) - 1;
-            m &= m - 1u;
-            const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
-            const float m_old = __shfl_sync(0xffffffffu, mstate, r);
-            const float mnew = optimizer_step<DT, VW, NB>(a, td.dim, acc[s], wrow[s], m_old);
-            S::store(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
-            if (a.opt == 2 && lane == r) a.state[kr] = mnew;
+        for (int s = 0; s < R; ++s) {
+            if (s < nk) {
+                const int r = f + s;
+                const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
+                const float m_old = __shfl_sync(0xffffffffu, mstate, r);
+                const float mnew = optimizer_step<DT, VW, NB>(a, td.dim, acc[s], wrow[s], m_old);
+                S::store(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
+                if (a.opt == 2 && lane == r) a.state[kr] = mnew;
+            }
         }
     }
 }
@@ -456,24 +458,9 @@ __device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace&
             const uint32_t s1 = __shfl_sync(0xffffffffu, rs, r + 1);
             generic_row<DT>(a, ws, pos_sorted, td, t, kr, s0, s1, nullptr, 0, lane);
         }
-    } else {
-        constexpr int VW = ShapeOf<CODE>::VW, NB = ShapeOf<CODE>::NB;
-        constexpr int R = ShortTune<DT, VW, NB>::R;
-        // pieces of at most R consecutive short keys: a long or skipped key
-        // between two short ones ends the piece, so a piece's lookups are
-        // exactly the sorted slots of its own keys
-        while (rows) {
-            const uint32_t low = rows & (0u - rows);
-            uint32_t piece = low;
-#pragma unroll
-            for (int k = 1; k < R; ++k) {
-                const uint32_t bit = low << k;  // next key up (0 past bit 31)
-                if (!(rows & bit)) break;
-                piece |= bit;
-            }
-            rows &= ~piece;
-            short_piece<DT, VW, NB>(a, ws, pos_sorted, td, t, rs, key, mstate, piece, lane);
-        }
+    } else if (rows) {
+        short_batch_vec<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, ws, pos_sorted, td, t, rs, key, mstate,
+                                                                  rows, lane);
     }
 }
 
@@ -484,7 +471,7 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
                                                const TableDesc& td, int t, uint32_t s0, uint32_t s1,
                                                float* part_row, int lane) {
     using S = Slice<DT, VW, NB>;
-    constexpr int GROUP = NB == 2 ? 2 : 4;
+    constexpr int GROUP = VW * NB >= 8 ? 2 : 4;  // gradient rows in flight per lane
     const int64_t tB = (int64_t)t * a.B;
     Kahan acc[NB][VW];
 #pragma unroll
@@ -559,12 +546,24 @@ __device__ __forceinline__ void long_combine(const ApplyArgs& a, const TableDesc
     for (int q = 0; q < NB; ++q)
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    for (uint32_t j = 0; j < nc; ++j) {
-        const float* p = part0 + (int64_t)j * a.max_dim;
+    constexpr int PF = 2;  // partial rows in flight
+    for (uint32_t j0 = 0; j0 < nc; j0 += PF) {
+        float x[PF][NB][VW];
 #pragma unroll
-        for (int q = 0; q < NB; ++q)
+        for (int k = 0; k < PF; ++k) {
+            const float* p = part0 + (int64_t)(j0 + k < nc ? j0 + k : j0) * a.max_dim;
 #pragma unroll
-            for (int v = 0; v < VW; ++v) acc[q][v].add(__ldcg(p + S::col(lane, q) + v));
+            for (int q = 0; q < NB; ++q)
+#pragma unroll
+                for (int v = 0; v < VW; ++v) x[k][q][v] = __ldcg(p + S::col(lane, q) + v);
+        }
+#pragma unroll
+        for (int k = 0; k < PF; ++k)
+            if (j0 + k < nc)
+#pragma unroll
+                for (int q = 0; q < NB; ++q)
+#pragma unroll
+                    for (int v = 0; v < VW; ++v) acc[q][v].add(x[k][q][v]);
     }
     float g[NB][VW];
 #pragma unroll
@@ -636,50 +635,101 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 
 // All work of one backward class (table dtype DT, row shape CODE): first the
 // long-run chunks whose table is in the class, then the short-run batches of
-// the class's tables.  Work items go to warps round-robin.
+// the class's tables, kBatchRows distinct keys each.  Warps take items one at
+// a time from an atomic counter (heavier chunks first), so no warp idles
+// while work is left; the last warp to finish resets the counter, so apply
+// can run again on the same prepared workspace.
 template <int DT, int CODE>
 __global__ void __launch_bounds__(256) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
+    __shared__ uint32_t s_bbase[kMaxTables + 1];  // first batch item of each class table
+    __shared__ uint32_t s_warp[8];
     a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], (uint32_t)a.N);
     const uint32_t nchunks = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
     const uint32_t nlong = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NLONG], (uint32_t)ws.max_long);
 
-    for (int64_t c = gw; c < nchunks; c += nw) {
-        const uint32_t li = __ldg(ws.chunk_run + c);
-        if (li >= nlong) continue;
-        const uint32_t u = __ldg(ws.long_runs + 4 * li), base = __ldg(ws.long_runs + 4 * li + 1),
-                       nc = __ldg(ws.long_runs + 4 * li + 2);
-        if (u >= U || c < base || c - base >= nc) continue;
-        const uint32_t key = __ldg(ws.uniq + u);
-        const int t = table_of(a.tabs, a.T, key);
-        if (a.tabs[t].cls != a.cls) continue;
-        const TableDesc td = a.tabs[t];
-        const uint32_t r0 = __ldg(ws.runstart + u);
-        const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
-        const uint32_t s0 = r0 + ((uint32_t)c - base) * kLongRun;
-        const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
-        long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, (uint32_t)c, li, base, nc, lane);
+    // batch counts of the class's tables, exclusive-scanned by the block
+    uint32_t carry = 0;
+    for (int base = 0; base < a.class_count; base += 256) {
+        const int k = base + threadIdx.x;
+        uint32_t nb = 0;
+        if (k < a.class_count) {
+            const int t = a.class_tables[k];
+            const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
+            const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
+            nb = (ue - us + kBatchRows - 1) / kBatchRows;
+        }
+        uint32_t x = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        uint32_t before = 0, total = 0;
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) before += s_warp[w];
+            total += s_warp[w];
+        }
+        if (k < a.class_count) s_bbase[k] = carry + before + x - nb;
+        carry += total;
+        __syncthreads();
     }
+    if (threadIdx.x == 0) s_bbase[a.class_count] = carry;
+    __syncthreads();
+    const uint32_t items = nchunks + carry;
 
-    // batch items: tables of the class in order, kBatchRows keys per item;
-    // item i of the whole class goes to warp i mod nw
-    int64_t off = 0;
-    for (int k = 0; k < a.class_count; ++k) {
-        const int t = a.class_tables[k];
-        const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
-        const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
-        const int64_t nb = (ue - us + kBatchRows - 1) / kBatchRows;
-        if (nb == 0) continue;
-        const TableDesc td = a.tabs[t];
-        const int64_t first = off + (((gw - off) % nw) + nw) % nw;
-        for (int64_t i = first; i < off + nb; i += nw) {
-            const uint32_t u0 = us + (uint32_t)(i - off) * kBatchRows;
+    for (;;) {
+        uint32_t item = 0;
+        if (lane == 0) item = atomicAdd(&ws.counters[CTR_WORK + a.cls], 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= items) break;
+        if (item < nchunks) {
+            const uint32_t c = item;
+            const uint32_t li = __ldg(ws.chunk_run + c);
+            if (li >= nlong) continue;
+            const uint32_t u = __ldg(ws.long_runs + 4 * li), base = __ldg(ws.long_runs + 4 * li + 1),
+                           nc = __ldg(ws.long_runs + 4 * li + 2);
+            if (u >= U || c < base || c - base >= nc) continue;
+            const uint32_t key = __ldg(ws.uniq + u);
+            const int t = table_of(a.tabs, a.T, key);
+            if (a.tabs[t].cls != a.cls) continue;
+            const TableDesc td = a.tabs[t];
+            const uint32_t r0 = __ldg(ws.runstart + u);
+            const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
+            const uint32_t s0 = r0 + (c - base) * kLongRun;
+            const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
+            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, c, li, base, nc, lane);
+        } else {
+            const uint32_t j = item - nchunks;
+            int lo = 0, hi = a.class_count - 1;  // last class table with s_bbase <= j
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_bbase[mid] <= j)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const int t = a.class_tables[lo];
+            const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
+            const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
+            const uint32_t u0 = us + (j - s_bbase[lo]) * kBatchRows;
+            if (u0 >= ue) continue;
+            const TableDesc td = a.tabs[t];
             short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kBatchRows, ue - u0), lane);
         }
-        off += nb;
+    }
+    // every warp has taken its last item: the last one to leave resets the
+    // counters for the next apply call on this workspace
+    if (lane == 0) {
+        const uint32_t total_warps = gridDim.x * (blockDim.x >> 5);
+        const uint32_t done = atomicAdd(&ws.counters[CTR_EXIT + a.cls], 1u);
+        if (done == total_warps - 1) {
+            atomicExch(&ws.counters[CTR_WORK + a.cls], 0u);
+            atomicExch(&ws.counters[CTR_EXIT + a.cls], 0u);
+        }
     }
 }
 

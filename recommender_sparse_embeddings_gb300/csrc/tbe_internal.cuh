@@ -16,6 +16,8 @@ enum : uint32_t { ERR_OOB = 1u, ERR_OFFSETS = 2u, ERR_TIMEOUT = 4u };
 // Forward gather schedule of one table.
 enum : int32_t { PATH_VEC = 0, PATH_SCALAR = 1, PATH_HIST = 2 };
 
+// Most tables one handle may hold.
+constexpr int kMaxTables = 4096;
 // Bags longer than this are pooled by a whole CTA instead of one slot.
 constexpr int kLongBag = 2048;
 // Capacity of the long-bag list held in the descriptor block.
@@ -225,6 +227,8 @@ enum : int {
     CTR_NCHUNK = 2,     // number of chunks of long runs
     CTR_RLE_TILE = 3,   // tile claim counter of the run-length kernel
     CTR_PASS_TILE = 4,  // tile claim counters of the sort passes [4]
+    CTR_WORK = 8,       // apply work-item counters, one per backward class [15]
+    CTR_EXIT = 24,      // apply finished-warp counters, one per backward class [15]
     CTR_HAS_SCALE = 63, // nonzero when prepare wrote the per-lookup scale array
     CTR_COUNT = 64,
 };
