@@ -256,6 +256,13 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+def backward_classes(specs) -> int:
+    """Backward apply launches one kernel per (dtype, row shape) class; the
+    bench's tables and gradient are aligned, so the shape is the dim when it
+    is 32, 64, 128 or 256, and element-wise otherwise."""
+    return len({(s.dtype, s.dim if s.dim in (32, 64, 128, 256) else 0) for s in specs})
+
+
 def _mean_bag_length(spec) -> float:
     kind = spec.length[0]
     if kind == "fixed":
@@ -308,18 +315,23 @@ def run_ours(args):
     def prep():
         tbe.tbe_backward_prepare(h, ind, off, B, ws, w)
 
+    def fwd_prep():
+        # forward and the backward preparation of the same batch, side by side
+        tbe.tbe_forward_prepare(h, ind, off, B, ws, w, out)
+
     def apply(g=grad):
         tbe.tbe_backward_apply(h, N, B, g, ws, cfg.optimizer, cfg.lr, cfg.eps, state)
 
     for _ in range(args.warmup):
         flush.zero_()
-        fwd(); prep(); apply()
+        fwd_prep(); apply()
     torch.cuda.synchronize()
     rc = tbe.tbe_get_error(h)
     if rc != tbe.TBE_OK:
         raise RuntimeError(f"device error during warm-up: {tbe.tbe_strerror(rc)}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # timed region: one step = forward + preparation (concurrent), then apply
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
@@ -327,18 +339,16 @@ def run_ours(args):
         for k in range(args.steps):
             flush.zero_()
             e = ev[k]
-            e[0].record(stream); fwd()
-            e[1].record(stream); prep()
-            e[2].record(stream); apply()
-            e[3].record(stream)
+            e[0].record(stream); fwd_prep()
+            e[1].record(stream); apply()
+            e[2].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
         barrier()
-    seg = {"forward": 0.0, "prepare": 0.0, "apply": 0.0}
+    seg = {"forward+prepare": 0.0, "apply": 0.0}
     for e in ev:
-        seg["forward"] += e[0].elapsed_time(e[1])
-        seg["prepare"] += e[1].elapsed_time(e[2])
-        seg["apply"] += e[2].elapsed_time(e[3])
+        seg["forward+prepare"] += e[0].elapsed_time(e[1])
+        seg["apply"] += e[1].elapsed_time(e[2])
     local_ms = sum(seg.values())
     total_ms = reduce_max(local_ms, dev)
     units = reduce_sum(float(N) * args.steps, dev)
@@ -346,19 +356,37 @@ def run_ours(args):
     if rc != tbe.TBE_OK:
         raise RuntimeError(f"device error in timed region: {tbe.tbe_strerror(rc)}")
 
+    # per-call breakdown (a separate run, each call timed alone)
+    nb_steps = min(args.steps, 200)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb_steps)]
+    for k in range(nb_steps):
+        flush.zero_()
+        e = evb[k]
+        e[0].record(stream); fwd()
+        e[1].record(stream); prep()
+        e[2].record(stream); apply()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    brk = {"forward": 0.0, "prepare": 0.0, "apply": 0.0}
+    for e in evb:
+        brk["forward"] += e[0].elapsed_time(e[1]) / nb_steps
+        brk["prepare"] += e[1].elapsed_time(e[2]) / nb_steps
+        brk["apply"] += e[2].elapsed_time(e[3]) / nb_steps
+
     # U (distinct keys) for the byte count: read once after the run
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
     passes = (max(1, (h.total_rows).bit_length()) + 7) // 8
     nbytes = algorithmic_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize, w is not None,
                                cfg.optimizer, U, passes)
+    nbytes["forward+prepare"] = nbytes["forward"] + nbytes["prepare"]
     ms_step = total_ms / args.steps
     value = units / (total_ms / 1e3)
     peak, peak_src = measured_hbm_peak()
     seg_ms = {k: v / args.steps for k, v in seg.items()}
     dominant = max(seg_ms, key=seg_ms.get)
     achieved = nbytes[dominant] / (seg_ms[dominant] / 1e3) / 1e9
-    launches_per_step = 2 + (2 + passes) + 2  # fwd pool+long, keys+passes+rle, short+chunks
+    launches_per_step = 2 + (2 + passes) + backward_classes(specs)  # pool+long, keys+passes+rle, apply
 
     # end-to-end through the public API: inputs from pinned host memory every
     # step, pooled output read back every step
@@ -379,9 +407,8 @@ def run_ours(args):
             if d_w is not None:
                 d_w.copy_(h_w, non_blocking=True)
             d_grad.copy_(h_grad, non_blocking=True)
-            tbe.tbe_forward(h, d_ind, d_off, B, d_w, out)
+            tbe.tbe_forward_prepare(h, d_ind, d_off, B, ws, d_w, out)
             h_out.copy_(out, non_blocking=True)
-            tbe.tbe_backward_prepare(h, d_ind, d_off, B, ws, d_w)
             tbe.tbe_backward_apply(h, N, B, d_grad, ws, cfg.optimizer, cfg.lr, cfg.eps, state)
 
         for _ in range(max(1, args.warmup)):
@@ -432,11 +459,13 @@ def run_ours(args):
                        "N_lookups": N, "unique_rows": U, "index_dtype": args.index_dtype,
                        "optimizer": cfg.optimizer, "parallelism": f"replicas x{world}",
                        "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
-            "fwd": {"lookups_per_s": units / (reduce_max(seg["forward"], dev) / 1e3),
-                    "gbs": nbytes["forward"] / (seg_ms["forward"] / 1e3) / 1e9,
-                    "frac": nbytes["forward"] / (seg_ms["forward"] / 1e3) / 1e9 / peak},
+            "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
+                    "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
+                    "frac": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9 / peak,
+                    "ms": brk["forward"]},
             "step_gbs": nbytes["step"] / (ms_step / 1e3) / 1e9,
             "segments_ms": seg_ms,
+            "breakdown_ms_sequential": brk,
             "algorithmic_bytes": nbytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": profile_traffic(dominant),

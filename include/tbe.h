@@ -174,6 +174,19 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
                          const float* per_sample_weights, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Forward and backward preparation of one batch, run side by side (kimbodo
+ * "Kimbodo Engineering Perspective": moving transpose, sort and run-length
+ * encoding into forward).  The forward pass is queued on `stream`, the
+ * preparation on a high-priority second stream owned by the handle that
+ * starts after the work already queued on `stream`; `stream` then waits for
+ * the preparation, so anything queued on it afterwards (tbe_backward_apply)
+ * sees both results.  Arguments and results as tbe_forward plus
+ * tbe_backward_prepare; argument errors are reported before anything is
+ * queued. */
+int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                        int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                        float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Backward from a prepared workspace: per unique (table,row) sums
  * s_i * grad_out[bag_i, Doff_t : Doff_t+dim_t] in fp32 (runs of fewer than 256
  * lookups stream through one warp; longer runs are split into 256-lookup

@@ -90,6 +90,7 @@ def load_library():
         "tbe_backward_workspace_bytes": ([P, i64, i32], ctypes.c_size_t),
         "tbe_backward_workspace_layout": ([P, i64, i32, ctypes.POINTER(WorkspaceLayout)], ctypes.c_int),
         "tbe_backward_prepare": ([P, P, P, i32, i64, i32, P, P, ctypes.c_size_t, P], ctypes.c_int),
+        "tbe_forward_prepare": ([P, P, P, i32, i64, i32, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
         "tbe_backward_apply": ([P, i64, i32, P, ctypes.POINTER(_Optimizer), P, ctypes.c_size_t, P],
                                ctypes.c_int),
         "tbe_backward_sgd": ([P, P, P, i32, i64, i32, P, P, f32, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -240,6 +241,19 @@ def tbe_backward_prepare(h: Handle, indices, offsets, batch_size: int, workspace
         h.ptr, _ptr(indices), _ptr(offsets), _index_dtype(indices, offsets), indices.numel(),
         batch_size, _ptr(per_sample_weights), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "tbe_backward_prepare")
+
+
+def tbe_forward_prepare(h: Handle, indices, offsets, batch_size: int, workspace: torch.Tensor,
+                        per_sample_weights=None, out: Optional[torch.Tensor] = None, stream=None):
+    """Forward pass and backward preparation of one batch, run side by side."""
+    if out is None:
+        out = torch.empty((batch_size, h.total_dim), dtype=torch.float32, device=offsets.device)
+    rc = load_library().tbe_forward_prepare(
+        h.ptr, _ptr(indices), _ptr(offsets), _index_dtype(indices, offsets), indices.numel(),
+        batch_size, _ptr(per_sample_weights), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(rc, "tbe_forward_prepare")
+    return out
 
 
 def tbe_backward_apply(h: Handle, num_indices: int, batch_size: int, grad_out: torch.Tensor,

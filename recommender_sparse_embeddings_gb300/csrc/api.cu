@@ -36,6 +36,8 @@ struct tbe_handle {
     int last_B = -1;
     int parity = 0;
     int vec_out = 0;
+    cudaStream_t side = nullptr;  // preparation stream of tbe_forward_prepare
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace {
@@ -280,12 +282,26 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         delete h;
         return TBE_ERR_CUDA;
     }
+    {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, greatest);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            tbe_destroy(h);
+            return TBE_ERR_CUDA;
+        }
+    }
     *out = h;
     return TBE_OK;
 }
 
 void tbe_destroy(tbe_handle* h) {
     if (!h) return;
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->side) cudaStreamDestroy(h->side);
     if (h->dev) cudaFree(h->dev);
     delete h;
 }
@@ -382,6 +398,30 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     a.total_rows = (uint32_t)h->total_rows;
     a.key_bits = h->key_bits;
     return cuda_status(launch_prepare(a, w, s));
+}
+
+int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                        int64_t num_indices, int32_t batch_size, const float* per_sample_weights, float* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
+    if (rc) return rc;
+    if (!workspace || (batch_size > 0 && !out)) return TBE_ERR_INVALID_ARG;
+    if (workspace_bytes < make_layout(h, num_indices, kLayoutWithScale).total) return TBE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // fork: the side stream starts after everything already queued on s
+    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return TBE_ERR_CUDA;
+    if (cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess) return TBE_ERR_CUDA;
+    rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size, per_sample_weights,
+                              workspace, workspace_bytes, h->side);
+    // the forward pass runs on s meanwhile
+    if (rc == TBE_OK)
+        rc = tbe_forward(h, indices, offsets, index_dtype, num_indices, batch_size, per_sample_weights, out, stream);
+    // join: later work on s waits for the preparation (also after an error,
+    // so s never runs ahead of work already queued on the side stream)
+    const bool joined = cudaEventRecord(h->ev_join, h->side) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, h->ev_join, 0) == cudaSuccess;
+    if (rc) return rc;
+    return joined ? TBE_OK : TBE_ERR_CUDA;
 }
 
 int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, const float* grad_out,

@@ -14,7 +14,8 @@
 //     digit's run is written contiguously.  The first pass generates the
 //     values (positions) instead of reading them.
 //  3. rle_kernel: head flags of the sorted keys, a tile scan with look-back,
-//     and the distinct keys with their first sorted slot (runstart[U] = N).
+//     the distinct keys with their first sorted slot (runstart[U] = N), the
+//     registration of long runs and the first distinct key of each table.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -277,15 +278,38 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(const uint32_t* 
 
 // --------------------------------------------------------- run-length code
 
-__global__ void __launch_bounds__(kSortThreads) rle_kernel(const uint32_t* __restrict__ skeys, uint32_t N,
-                                                           uint32_t* __restrict__ uniq,
-                                                           uint32_t* __restrict__ runstart,
-                                                           uint32_t* status, uint32_t* counters,
-                                                           uint32_t* err) {
+// Table of a key: the last table whose row base is <= key, or T for the key
+// of skipped lookups (>= the sum of all rows).
+__device__ __forceinline__ int key_table(const PrepArgs& a, uint32_t key) {
+    if (key >= a.total_rows) return a.T;
+    int lo = 0, hi = a.T - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((uint64_t)a.tabs[mid].rowbase <= key)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Run-length encoding of the sorted keys, tile by tile with a warp-parallel
+// look-back for the running count of distinct keys.  Besides uniq/runstart
+// it does the two jobs the apply step needs from the run boundaries:
+//  - registers every run of at least kLongRun lookups for the accumulate
+//    path (a run starting at p is long iff the key at p + 255 equals the key
+//    at p; its end is then found by an exponential then binary search):
+//    ceil(len / kLongRun) consecutive chunk slots and a record (unique index,
+//    first chunk, chunk count, chunks finished = 0);
+//  - ustart[t]: the first distinct-key index of every table (keys are sorted
+//    and each table owns a consecutive key range), ustart[T] the end.
+__global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace ws, const uint32_t* __restrict__ skeys) {
     __shared__ uint32_t s_scan[8];
     __shared__ uint32_t s_tile, s_prefix;
-    const int tid = threadIdx.x;
-    if (tid == 0) s_tile = atomicAdd(&counters[CTR_RLE_TILE], 1u);
+    const uint32_t N = (uint32_t)a.N;
+    uint32_t* err = &a.blk->error;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) s_tile = atomicAdd(&ws.counters[CTR_RLE_TILE], 1u);
     __syncthreads();
     const uint32_t tile = s_tile;
     const uint32_t p0 = tile * kSortTile + tid * kSortItems;
@@ -315,65 +339,63 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(const uint32_t* __res
     }
     uint32_t tile_total;
     const uint32_t excl = block_exclusive_scan_256(__popc(heads), s_scan, &tile_total);
-    if (tid == 0) s_prefix = lookback(status, (int)tile, 1, tile_total, err);
+    if (tid < 32) {
+        const uint32_t pre = lookback_warp(ws.rle_status, (int)tile, tile_total, err, lane);
+        if (tid == 0) s_prefix = pre;
+    }
     __syncthreads();
+    const uint32_t U = tmin<uint32_t>(s_prefix + tile_total, N);
     uint32_t u = s_prefix + excl;
 #pragma unroll
     for (int q = 0; q < kSortItems; ++q) {
-        if (heads & (1u << q)) {
-            if (u < N) {  // holds unless a look-back ran out (then ERR_TIMEOUT is set)
-                uniq[u] = k[q];
-                runstart[u] = p0 + q;
+        if (!(heads & (1u << q))) continue;
+        const uint32_t p = p0 + q, key = k[q];
+        if (u < N) {  // holds unless a look-back ran out (then ERR_TIMEOUT is set)
+            ws.uniq[u] = key;
+            ws.runstart[u] = p;
+            // tables whose key range starts after the previous key and at or
+            // before this one begin at u
+            const int tprev = p > 0 ? key_table(a, q > 0 ? k[q - 1] : prev) : -1;
+            const int tk = key_table(a, key);
+            for (int t2 = tprev + 1; t2 <= tk; ++t2) ws.ustart[t2] = u;
+            // long run: registered for the accumulate path
+            if (key < a.total_rows && p + (kLongRun - 1) < N && __ldg(skeys + p + kLongRun - 1) == key) {
+                uint32_t lo = p + kLongRun - 1, step = kLongRun;  // skeys[lo] == key
+                while (lo + step < N && __ldg(skeys + lo + step) == key) {
+                    lo += step;
+                    step *= 2;
+                }
+                uint32_t hi = tmin<uint32_t>(lo + step, N);  // first differing slot is in (lo, hi]
+                while (hi - lo > 1) {
+                    const uint32_t mid = lo + (hi - lo) / 2;
+                    if (__ldg(skeys + mid) == key)
+                        lo = mid;
+                    else
+                        hi = mid;
+                }
+                const uint32_t len = hi - p;
+                const uint32_t nc = (len + kLongRun - 1) / kLongRun;
+                const uint32_t base = atomicAdd(&ws.counters[CTR_NCHUNK], nc);
+                const uint32_t li = atomicAdd(&ws.counters[CTR_NLONG], 1u);
+                if (li < ws.max_long && (int64_t)base + nc <= ws.max_chunks) {
+                    ws.long_runs[4 * li + 0] = u;
+                    ws.long_runs[4 * li + 1] = base;
+                    ws.long_runs[4 * li + 2] = nc;
+                    ws.long_runs[4 * li + 3] = 0;
+                    for (uint32_t j = 0; j < nc; ++j) ws.chunk_run[base + j] = li;
+                }
             }
-            ++u;
         }
+        ++u;
+    }
+    // the thread holding the last position ends the table ranges
+    if (N > 0 && p0 <= N - 1 && N - 1 < p0 + kSortItems) {
+        const int tlast = key_table(a, skeys[N - 1]);
+        for (int t2 = tlast + 1; t2 <= a.T; ++t2) ws.ustart[t2] = U;
     }
     if (tid == 0 && (uint64_t)(tile + 1) * kSortTile >= N) {
-        const uint32_t U = tmin<uint32_t>(s_prefix + tile_total, N);
-        counters[CTR_U] = U;
-        runstart[U] = N;
-    }
-}
-
-// ---------------------------------------------------------- long runs
-
-// Registers every run of at least kLongRun lookups for the accumulate path:
-// ceil(len / kLongRun) consecutive chunk slots and a record (unique index,
-// first chunk, chunk count, chunks finished = 0), and finds where each
-// table's distinct keys start.  Depends only on the sorted keys, so it
-// belongs to the preparation step.
-__global__ void __launch_bounds__(256) classify_kernel(PrepArgs a, Workspace ws) {
-    const uint32_t N = (uint32_t)a.N, total_rows = a.total_rows;
-    const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], N);
-    // keys are sorted and each table owns a consecutive key range;
-    // ustart[T] ends the last table's range (skipped lookups come after)
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t <= a.T; t += gridDim.x * blockDim.x) {
-        const uint64_t target = t < a.T ? (uint64_t)a.tabs[t].rowbase : (uint64_t)total_rows;
-        uint32_t lo = 0, hi = U;
-        while (lo < hi) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if ((uint64_t)__ldg(ws.uniq + mid) < target)
-                lo = mid + 1;
-            else
-                hi = mid;
-        }
-        ws.ustart[t] = lo;
-    }
-    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < U; u += gridDim.x * blockDim.x) {
-        if (__ldg(ws.uniq + u) >= total_rows) continue;  // skipped lookups
-        const uint32_t s0 = __ldg(ws.runstart + u);
-        const uint32_t s1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), N);
-        if (s1 <= s0 || s1 - s0 < (uint32_t)kLongRun) continue;
-        const uint32_t nc = (s1 - s0 + kLongRun - 1) / kLongRun;
-        const uint32_t base = atomicAdd(&ws.counters[CTR_NCHUNK], nc);
-        const uint32_t li = atomicAdd(&ws.counters[CTR_NLONG], 1u);
-        if (li < ws.max_long && (int64_t)base + nc <= ws.max_chunks) {
-            ws.long_runs[4 * li + 0] = u;
-            ws.long_runs[4 * li + 1] = base;
-            ws.long_runs[4 * li + 2] = nc;
-            ws.long_runs[4 * li + 3] = 0;
-            for (uint32_t j = 0; j < nc; ++j) ws.chunk_run[base + j] = li;
-        }
+        ws.counters[CTR_U] = U;
+        ws.runstart[U] = N;
     }
 }
 
@@ -412,12 +434,7 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         cur ^= 1;
     }
     ws.sorted_buf = cur;
-    rle_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, ws.uniq, ws.runstart, ws.rle_status,
-                                              ws.counters, &a.blk->error);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const unsigned cgrid = (unsigned)tmax<int64_t>(1, tmin<int64_t>((a.N + 255) / 256, (int64_t)sms * 4));
-    classify_kernel<<<cgrid, 256, 0, s>>>(a, ws);
+    rle_kernel<<<tiles, kSortThreads, 0, s>>>(a, ws, ws.keys[cur]);
     return cudaGetLastError();
 }
 

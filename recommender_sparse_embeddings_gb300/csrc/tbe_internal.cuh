@@ -142,9 +142,10 @@ __device__ __forceinline__ void st_volatile_u32(uint32_t* p, uint32_t v) {
 // Decoupled look-back for one running count: publishes this tile's aggregate,
 // walks back over earlier tiles until one with an inclusive prefix, then
 // publishes this tile's inclusive prefix.  Returns the exclusive prefix.
-// Every earlier tile was claimed (atomic tile counter) by a CTA that is
-// already resident and publishes its aggregate without waiting, so each wait
-// ends; the spin is still bounded and raises ERR_TIMEOUT if it runs out.
+// Four predecessors are read per round trip.  Every earlier tile was claimed
+// (atomic tile counter) by a CTA that is already resident and publishes its
+// aggregate without waiting, so each wait ends; the spin is still bounded
+// and raises ERR_TIMEOUT if it runs out.
 __device__ __forceinline__ uint32_t lookback(uint32_t* status, int tile, uint32_t stride,
                                              uint32_t aggregate, uint32_t* err) {
     if (tile == 0) {
@@ -156,21 +157,76 @@ __device__ __forceinline__ uint32_t lookback(uint32_t* status, int tile, uint32_
     int j = tile - 1;
     int spins = 0;
     while (j >= 0) {
-        const uint32_t s = ld_volatile_u32(status + (size_t)j * stride);
-        const uint32_t f = s & ~kCountMask;
-        if (f == 0) {
+        uint32_t sv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sv[k] = j - k >= 0 ? ld_volatile_u32(status + (size_t)(j - k) * stride) : 0u;
+        int used = 0;
+        bool done = false, stall = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (done || stall) continue;
+            const uint32_t f = sv[k] & ~kCountMask;
+            if (f == 0) {
+                stall = true;
+                continue;
+            }
+            excl += sv[k] & kCountMask;
+            ++used;
+            if (f == kFlagPrefix) done = true;
+        }
+        if (done) break;
+        j -= used;
+        if (stall) {
             if (++spins > kSpinLimit) {
                 atomicOr(err, ERR_TIMEOUT);
                 break;
             }
             __nanosleep(100);
-            continue;
         }
-        excl += s & kCountMask;
-        if (f == kFlagPrefix) break;
-        --j;
     }
     st_volatile_u32(status + (size_t)tile * stride, kFlagPrefix | ((excl + aggregate) & kCountMask));
+    return excl;
+}
+
+// The same for one count per tile (stride 1), done by a whole warp: the
+// lanes read 32 predecessors at once, so a chain of t tiles takes t/32 round
+// trips.  All lanes of the warp must call it; all get the exclusive prefix.
+__device__ __forceinline__ uint32_t lookback_warp(uint32_t* status, int tile, uint32_t aggregate,
+                                                  uint32_t* err, int lane) {
+    if (tile == 0) {
+        if (lane == 0) st_volatile_u32(status, kFlagPrefix | aggregate);
+        return 0;
+    }
+    if (lane == 0) st_volatile_u32(status + tile, kFlagAgg | aggregate);
+    uint32_t excl = 0;
+    int top = tile - 1;  // nearest predecessor not yet counted
+    int spins = 0;
+    while (top >= 0) {
+        const int idx = top - lane;
+        // below tile 0 reads as an empty prefix (never reached past tile 0,
+        // which always holds one)
+        const uint32_t sv = idx >= 0 ? ld_volatile_u32(status + idx) : kFlagPrefix;
+        const uint32_t f = sv & ~kCountMask;
+        const unsigned pre = __ballot_sync(0xffffffffu, f == kFlagPrefix);
+        const unsigned inval = __ballot_sync(0xffffffffu, f == 0);
+        const int first_pre = pre ? __ffs(pre) - 1 : 32;
+        const unsigned need = first_pre == 32 ? 0xffffffffu : (0xffffffffu >> (31 - first_pre));
+        if (inval & need) {  // a tile before the nearest prefix is not ready yet
+            if (++spins > kSpinLimit) {
+                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(100);
+            continue;
+        }
+        uint32_t c = ((need >> lane) & 1u) ? (sv & kCountMask) : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        excl += c;
+        if (first_pre < 32) break;
+        top -= 32;
+    }
+    if (lane == 0) st_volatile_u32(status + tile, kFlagPrefix | ((excl + aggregate) & kCountMask));
     return excl;
 }
 

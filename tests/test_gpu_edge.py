@@ -233,3 +233,41 @@ def test_workspace_too_small_is_rejected_before_launch():
         tbe.tbe_backward_sgd(h, ind, off, 1, torch.ones((1, 16), device=DEV), 0.1, small)
     assert e.value.code == tbe.TBE_ERR_WORKSPACE_TOO_SMALL
     h.close()
+
+
+@pytest.mark.parametrize("cid", [2, 3])
+def test_forward_prepare_side_by_side(cid):
+    """tbe_forward_prepare (forward and preparation on two streams) gives the
+    forward output, sort and run-length results, and after apply the tables,
+    of the separate calls and the oracle."""
+    import workloads
+    cfg = workloads.get_config(cid).scaled(B=200, rows_div=1000, rows_min=64)
+    specs = workloads.realize_tables(cfg)
+    tables = [t.to(DEV) for t in workloads.make_tables(cfg, "cpu", specs)]
+    batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
+    grad = workloads.make_grad(cfg, "cpu", specs)
+    cpu_tables = [t.cpu() for t in tables]
+    before = [table_bits(t) for t in tables]
+    h = tbe.tbe_create(tables, cfg.pooling)
+    ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
+    w = None if batch.weights is None else batch.weights.to(DEV)
+    ws = tbe.make_workspace(h, batch.N, cfg.B)
+    out = tbe.tbe_forward_prepare(h, ind, off, cfg.B, ws, w)
+    state = torch.zeros(h.total_rows, dtype=torch.float32, device=DEV) if cfg.optimizer == "adagrad" else None
+    tbe.tbe_backward_apply(h, batch.N, cfg.B, grad.to(DEV), ws, cfg.optimizer, cfg.lr, cfg.eps, state)
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    ref, _ = oracle_forward(cpu_tables, batch.indices, batch.offsets, cfg.B, batch.weights, cfg.pooling)
+    assert_close(out.cpu().numpy(), ref, what="fused forward", **FP32_TOL)
+    lay = tbe.tbe_backward_workspace_layout(h, batch.N, cfg.B)
+    keys, _ = oracle.make_keys([t.shape[0] for t in cpu_tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
+    r = oracle.sort_rle(keys)
+    got = ws[lay.sorted_keys:lay.sorted_keys + 4 * batch.N].view(torch.int32).cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(got.astype(np.int64), r["sorted_keys"])
+    ref_tabs, ref_state = oracle_backward(cpu_tables, batch.indices, batch.offsets, cfg.B, grad, cfg.optimizer,
+                                          cfg.lr, cfg.eps, batch.weights, cfg.pooling,
+                                          None if state is None else torch.zeros(h.total_rows))
+    assert_tables_match(tables, ref_tabs, before, touched_rows(cpu_tables, batch.indices, batch.offsets, cfg.B),
+                        what="fused then apply")
+    if state is not None:
+        assert_close(state.cpu().numpy(), ref_state, what="fused state", **FP32_TOL)
+    h.close()
