@@ -300,7 +300,7 @@ def run_ours(args):
     batch = workloads.make_batch(cfg, dev, idx_dtype, specs)
     grad = workloads.make_grad(cfg, dev, specs)
     T, B, N = len(specs), cfg.B, batch.N
-    h = tbe.tbe_create(tables, cfg.pooling)
+    h = tbe.tbe_create(tables, cfg.pooling, tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0)
     ws = tbe.make_workspace(h, N, B, dev)
     out = torch.empty((B, h.total_dim), dtype=torch.float32, device=dev)
     state = (torch.zeros(h.total_rows, dtype=torch.float32, device=dev)
@@ -453,6 +453,7 @@ def run_ours(args):
             "dtype": "f32" if all(s.dtype == "f32" for s in specs) else "mixed(f32 accumulate)",
             "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
                     "pages' production shard configurations)",
+            "paths": sorted(set(tbe.tbe_table_paths(h))),
             "config": {"workload": cfg.description + (
                            f" (first {T} of the tables)" if args.tables else ""),
                        "config_id": cfg.cfg_id, "T": T, "B": B,
@@ -533,6 +534,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-histogram", action="store_true",
+                   help="keep small tables on the gather path (no tensor-core histogram path)")
     p.add_argument("--tables", type=int, default=0,
                    help="use only the first K tables of the workload (profiling cases)")
     args = p.parse_args(argv)

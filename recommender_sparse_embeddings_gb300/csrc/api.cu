@@ -26,6 +26,9 @@ struct tbe_handle {
     DevBlock* blk = nullptr;
     TableDesc* dtabs = nullptr;
     int32_t* dclass_tables = nullptr;
+    int32_t* dhist_tables = nullptr;  // histogram-path tables: f16 ones, then bf16 ones
+    int n_hist_f16 = 0, n_hist_bf16 = 0;
+    size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
     int class_begin[kNumClasses] = {};
     int class_count[kNumClasses] = {};
     int total_d = 0;
@@ -46,6 +49,19 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t tabs_offset() { return align_up(sizeof(DevBlock)); }
 size_t class_list_offset(int T) { return align_up(tabs_offset() + sizeof(TableDesc) * T); }
+size_t hist_list_offset(int T) { return align_up(class_list_offset(T) + sizeof(int32_t) * T); }
+
+// Small tables the tensor-core histogram path can take: 16-bit rows whose
+// dim is a multiple of 16 in [16, 256] (the MMA's N), 16-byte aligned data,
+// at most max_rows rows (the MMA's K, padded to 16), and H plus W^T within
+// the shared memory of one CTA.
+bool hist_eligible(const TableDesc& d, int64_t max_rows, size_t smem_limit) {
+    if (d.dtype != TBE_F16 && d.dtype != TBE_BF16) return false;
+    if (d.dim % 16 != 0 || d.dim < 16 || d.dim > 256) return false;
+    if (((uintptr_t)d.data % 16) != 0) return false;
+    if (d.rows > max_rows) return false;
+    return hist_smem_bytes(d.rows, d.dim) + 4096 <= smem_limit;
+}
 
 // Backward class of a table: dtype and row shape (vector lanes for dim 32,
 // 64, 128, 256 when rows and gradient columns are aligned for them).
@@ -250,6 +266,29 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         delete h;
         return TBE_ERR_CUDA;
     }
+    std::vector<int32_t> hist_f16, hist_bf16;
+    if (!(flags & TBE_FLAG_NO_HISTOGRAM)) {
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
+            optin = 0;
+        // default: tables of at most 512 rows; forced: up to 1024
+        const int64_t max_rows = (flags & TBE_FLAG_FORCE_HISTOGRAM) ? 1024 : 512;
+        for (int t = 0; t < num_tables; ++t) {
+            TableDesc& d = h->tabs[t];
+            if (!hist_eligible(d, max_rows, (size_t)optin)) continue;
+            d.path = PATH_HIST;
+            const size_t sm = hist_smem_bytes(d.rows, d.dim);
+            if (d.dtype == TBE_F16) {
+                hist_f16.push_back(t);
+                h->hist_smem_f16 = std::max(h->hist_smem_f16, sm);
+            } else {
+                hist_bf16.push_back(t);
+                h->hist_smem_bf16 = std::max(h->hist_smem_bf16, sm);
+            }
+        }
+    }
+    h->n_hist_f16 = (int)hist_f16.size();
+    h->n_hist_bf16 = (int)hist_bf16.size();
     std::vector<int32_t> order;
     {
         std::vector<std::vector<int32_t>> by_class(kNumClasses);
@@ -263,7 +302,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
             order.insert(order.end(), by_class[c].begin(), by_class[c].end());
         }
     }
-    const size_t bytes = class_list_offset(num_tables) + sizeof(int32_t) * num_tables;
+    const size_t bytes = hist_list_offset(num_tables) + sizeof(int32_t) * num_tables;
     e = cudaMalloc(&h->dev, bytes);
     if (e != cudaSuccess) {
         delete h;
@@ -272,11 +311,17 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     h->blk = static_cast<DevBlock*>(h->dev);
     h->dtabs = reinterpret_cast<TableDesc*>(static_cast<char*>(h->dev) + tabs_offset());
     h->dclass_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + class_list_offset(num_tables));
+    h->dhist_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + hist_list_offset(num_tables));
     e = cudaMemset(h->dev, 0, tabs_offset());
     if (e == cudaSuccess)
         e = cudaMemcpy(h->dtabs, h->tabs.data(), sizeof(TableDesc) * num_tables, cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
         e = cudaMemcpy(h->dclass_tables, order.data(), sizeof(int32_t) * num_tables, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !hist_f16.empty())
+        e = cudaMemcpy(h->dhist_tables, hist_f16.data(), sizeof(int32_t) * hist_f16.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !hist_bf16.empty())
+        e = cudaMemcpy(h->dhist_tables + hist_f16.size(), hist_bf16.data(), sizeof(int32_t) * hist_bf16.size(),
+                       cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(h->dev);
         delete h;
@@ -342,6 +387,9 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
     a.parity = h->parity;
     a.num_sms = h->num_sms;
     rc = cuda_status(launch_forward(a, s));
+    if (rc == TBE_OK && h->n_hist_f16 + h->n_hist_bf16 > 0)
+        rc = cuda_status(launch_hist(a, h->dhist_tables, h->n_hist_f16, h->hist_smem_f16,
+                                     h->dhist_tables + h->n_hist_f16, h->n_hist_bf16, h->hist_smem_bf16, s));
     if (rc == TBE_OK) h->parity ^= 1;
     return rc;
 }

@@ -1,0 +1,407 @@
+// Small-table forward path on the tensor cores (kimbodo "What Happened":
+// eligible small tables use a histogram and tensor-core path).
+//
+// For a table with few rows, pooling is a dense product: with
+//   H[b, r] = sum over the lookups i of bag b with idx_i = r of s_i
+// (s_i = per-sample weight, times 1/L for mean pooling), the pooled rows are
+//   out[b, Doff : Doff + D] = H[b, :] . W   (H: B x R, W: R x D).
+// A CTA of 4 warps keeps W^T (D x R, zero-padded in R to Kp) in shared memory
+// and, for each tile of 128 bags, builds H (128 x Kp) in shared memory with
+// 16-bit atomic adds, issues Kp/16 tcgen05.mma (kind::f16, M=128, N=D, K=16,
+// fp32 accumulation in tensor memory), waits on an mbarrier that
+// tcgen05.commit arrives on, and reads the accumulator back with tcgen05.ld
+// (warp w owns tensor-memory lanes 32w..32w+31, i.e. bags 32w..32w+31 of the
+// tile).  H and W^T use the no-swizzle K-major layout of 8x16-byte core
+// matrices: element (m, k) of an operand with row stride SBO bytes per 8
+// rows sits at (m/8)*SBO + (k/8)*128 + (m%8)*16 + (k%8)*2.
+//
+// Both operands are fp16 (the tensor cores take A and B in one type): fp16
+// tables as they are, bf16 tables converted (exact within fp16's normal
+// range), H entries as fp16 sums of lookup scales.  Products and sums are
+// fp32.  A value that does not fit fp16 (a bf16 entry or an H sum beyond
+// 65504) sends the tile to an fp32 gather instead.
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+constexpr int kHistM = 128;          // bags per tile (MMA M)
+constexpr int kHistThreads = 512;    // 16 warps; warp w reads tensor-memory lanes 32*(w%4)..
+constexpr int kHistTilesPerCta = 8;  // bag tiles per CTA (W^T is loaded once)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// tcgen05 shared-memory matrix descriptor: start address, leading (K)
+// and stride (M/N) byte offsets, fixed version bits 46-48 = 0b001, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the same
+// 16-bit type (0 = f16, 1 = bf16), both K-major, N >> 3 at bit 17, M >> 4 at
+// bit 24.
+__host__ __device__ inline uint32_t mma_idesc(int bf16, int M, int N) {
+    return (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for mbarrier phase `parity`; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (int i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tcgen05_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tcgen05_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// Byte offset of element (m, k) in the no-swizzle K-major core-matrix layout.
+__device__ __forceinline__ uint32_t core_off(int m, int k, uint32_t sbo) {
+    return (uint32_t)(m >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(m & 7) * 16u + (uint32_t)(k & 7) * 2u;
+}
+
+constexpr float kHalfMax = 65504.f;
+
+// Fallback for a tile whose values do not fit the fp16 operands: warp per
+// bag, lanes over columns, fp32 accumulation straight from the table.
+template <int DT, typename IDX>
+__device__ void hist_tile_gather(const FwdArgs& a, const TableDesc& td, int t, int b0, int nb, int warp,
+                                 int lane, bool& oob) {
+    const IDX* off = reinterpret_cast<const IDX*>(a.offsets);
+    const IDX* ind = reinterpret_cast<const IDX*>(a.indices);
+    const int D = td.dim;
+    for (int m = warp; m < nb; m += kHistThreads / 32) {
+        const int b = b0 + m;
+        const int64_t bag = (int64_t)t * a.B + b;
+        int64_t start = ld_index(off, bag), end = ld_index(off, bag + 1);
+        if (start < 0 || end < start || end > a.N) start = end = 0;
+        float* orow = a.out + (int64_t)b * a.total_d + td.doff;
+        for (int c0 = 0; c0 < D; c0 += 256) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int64_t p = start; p < end; ++p) {
+                const int64_t x = ld_index(ind, p);
+                if (x < 0 || x >= td.rows) {
+                    oob = true;
+                    continue;
+                }
+                const float s = a.weights ? __ldg(a.weights + p) : 1.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + lane + 32 * j;
+                    if (c < D) acc[j] = fmaf(s, load_elem<DT>(td.data, x * D + c), acc[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + lane + 32 * j;
+                if (c < D) orow[c] = (a.mean && end > start) ? __fdiv_rn(acc[j], (float)(end - start)) : acc[j];
+            }
+        }
+    }
+}
+
+template <int DT, typename IDX>
+__global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const int32_t* hist_tables,
+                                                             int ctas_per_table) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_ovf, s_wovf;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t = hist_tables[blockIdx.x / ctas_per_table];
+    const int cta = blockIdx.x % ctas_per_table;
+    const TableDesc td = a.tabs[t];
+    const int R = (int)td.rows, D = td.dim;
+    const int Kp = (R + 15) & ~15;
+    const uint32_t sbo = (uint32_t)(Kp / 8) * 128u;  // bytes per 8 rows of H (bags) and of W^T (columns)
+    unsigned char* Hs = smem_raw;
+    unsigned char* Ws = smem_raw + (size_t)kHistM * Kp * 2;
+    int64_t* s_off = reinterpret_cast<int64_t*>(Ws + (size_t)D * Kp * 2);  // the CTA's bag offsets
+    const int ntiles = (a.B + kHistM - 1) / kHistM;
+    const int tile0 = cta * kHistTilesPerCta;
+    if (tile0 >= ntiles) return;  // whole CTA leaves before allocating anything
+    const int tile1 = tile0 + kHistTilesPerCta < ntiles ? tile0 + kHistTilesPerCta : ntiles;
+    const int bag_lo = tile0 * kHistM;
+    const int bag_hi = tile1 * kHistM < a.B ? tile1 * kHistM : a.B;
+    const IDX* off = reinterpret_cast<const IDX*>(a.offsets);
+    const IDX* ind = reinterpret_cast<const IDX*>(a.indices);
+    const uint32_t ncols = D <= 32 ? 32u : (D <= 64 ? 64u : (D <= 128 ? 128u : 256u));
+    bool oob = false, bad_off = false, timed_out = false;
+
+    if (warp == 0) tmem_alloc(&s_tmem, ncols);
+    if (tid == 0) {
+        s_ovf = 0;
+        s_wovf = 0;
+        mbar_init(&s_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // bag offsets of the CTA's tiles
+    for (int i = tid; i <= bag_hi - bag_lo; i += kHistThreads) s_off[i] = ld_index(off, (int64_t)t * a.B + bag_lo + i);
+    // W^T as fp16: element (n, k) = W[k][n], zero for k >= R
+    const unsigned short* W = reinterpret_cast<const unsigned short*>(td.data);
+    int ovf = 0;
+    for (int e = tid; e < Kp * (D / 8); e += kHistThreads) {
+        const int k = e / (D / 8), n8 = (e % (D / 8)) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k < R) v = __ldg(reinterpret_cast<const uint4*>(W + (int64_t)k * D + n8));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t bits = (w4[j >> 1] >> (16 * (j & 1))) & 0xffffu;
+            if constexpr (DT == DT_BF16) {
+                // bf16 -> fp16 is exact inside fp16's normal range; a finite
+                // value beyond it would become inf: take the fallback
+                const float f = bf16_bits_to_float(bits);
+                if (fabsf(f) > kHalfMax && isfinite(f)) ovf = 1;
+                bits = __half_as_ushort(__float2half_rn(f));
+            }
+            *reinterpret_cast<unsigned short*>(Ws + core_off(n8 + j, k, sbo)) = (unsigned short)bits;
+        }
+    }
+    if (ovf) s_wovf = 1;
+    tcgen05_before_sync();
+    __syncthreads();
+    tcgen05_after_sync();
+    const uint32_t tmem = s_tmem;
+    const uint32_t idesc = mma_idesc(0, kHistM, D);  // fp16 x fp16 -> fp32
+    const uint32_t hbase = smem_u32(Hs), wbase = smem_u32(Ws);
+    const bool mean = a.mean != 0;
+    const bool wovf = s_wovf != 0;
+    uint32_t phase = 0;
+
+    for (int tile = tile0; tile < tile1; ++tile) {
+        const int b0 = tile * kHistM;
+        const int nb = b0 + kHistM < a.B ? kHistM : a.B - b0;
+        const int64_t* toff = s_off + (b0 - bag_lo);  // toff[0..nb]
+        if (wovf) {  // the table does not fit fp16: every tile by fp32 gather
+            hist_tile_gather<DT, IDX>(a, td, t, b0, nb, warp, lane, oob);
+            continue;
+        }
+        // zero H
+        for (int e = tid; e < kHistM * Kp * 2 / 16; e += kHistThreads)
+            reinterpret_cast<uint4*>(Hs)[e] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        // histogram of the tile: its lookups are the contiguous range
+        // [toff[0], toff[nb]); each thread takes every 512th, four in flight
+        const int64_t P0 = toff[0], P1 = toff[nb];
+        const bool range_ok = P0 >= 0 && P1 >= P0 && P1 <= a.N;
+        if (!range_ok) bad_off = true;
+        for (int64_t pb = P0 + tid; range_ok && pb < P1; pb += 4 * kHistThreads) {
+            int64_t x[4];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t p = pb + (int64_t)u * kHistThreads;
+                x[u] = -1;
+                w[u] = 1.f;
+                if (p < P1) {
+                    x[u] = ld_index(ind, p);
+                    if (a.weights) w[u] = __ldg(a.weights + p);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t p = pb + (int64_t)u * kHistThreads;
+                if (p >= P1) continue;
+                // bag of position p: last m with toff[m] <= p
+                int lo = 0, hi = nb - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (toff[mid] <= p)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                const int64_t L = toff[lo + 1] - toff[lo];
+                if (L <= 0) {  // malformed offsets: p belongs to no bag
+                    bad_off = true;
+                    continue;
+                }
+                if (x[u] < 0 || x[u] >= R) {
+                    oob = true;
+                    continue;
+                }
+                float s = w[u];
+                if (mean) s = __fdiv_rn(s, (float)L);
+                const __half old =
+                    atomicAdd(reinterpret_cast<__half*>(Hs + core_off(lo, (int)x[u], sbo)), __float2half_rn(s));
+                if (!(fabsf(__half2float(old) + s) <= kHalfMax)) s_ovf = 1;
+            }
+        }
+        fence_proxy_async_smem();  // generic-proxy writes of H -> tensor cores
+        tcgen05_before_sync();
+        __syncthreads();
+        tcgen05_after_sync();
+        if (s_ovf) {  // uniform: written before the barrier above
+            hist_tile_gather<DT, IDX>(a, td, t, b0, nb, warp, lane, oob);
+            __syncthreads();
+            if (tid == 0) s_ovf = 0;
+            __syncthreads();
+            continue;
+        }
+        if (tid == 0) {
+            for (int j = 0; j < Kp / 16; ++j)
+                mma_f16(tmem, smem_desc(hbase + 256u * j, 128u, sbo), smem_desc(wbase + 256u * j, 128u, sbo), idesc,
+                        j > 0 ? 1u : 0u);
+            mma_commit(&s_bar);
+        }
+        // every thread waits; the block agrees on the outcome so all threads
+        // take the same path through the barriers below
+        const bool ok = mbar_wait(&s_bar, phase);
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            break;
+        }
+        phase ^= 1u;
+        tcgen05_after_sync();
+        // accumulator -> output: warp w reads tensor-memory lanes 32*(w%4)..
+        // (bags of the tile) and the 16-column chunks c = w/4, w/4 + 4, ...
+        const int lg = warp & 3;
+        const int b = b0 + lg * 32 + lane;
+        float* orow = a.out + (int64_t)b * a.total_d + td.doff;
+        for (int c = (warp >> 2) * 16; c < D; c += (kHistThreads / 128) * 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)c, v);  // whole warp, aligned
+            if (b < a.B) {
+                if (a.vec_out) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<float4*>(orow + c)[q] =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) orow[c + q] = v[q];
+                }
+            }
+        }
+        tcgen05_before_sync();
+        __syncthreads();  // accumulator read and H consumed before the next tile
+        tcgen05_after_sync();
+    }
+    if (timed_out) {
+        if (tid == 0) atomicOr(&a.blk->error, ERR_TIMEOUT);
+        mbar_wait(&s_bar, phase);  // a second bounded wait for the MMAs in flight
+    }
+    if (oob) atomicOr(&a.blk->error, ERR_OOB);
+    if (bad_off) atomicOr(&a.blk->error, ERR_OFFSETS);
+    tcgen05_before_sync();
+    __syncthreads();
+    tcgen05_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+// Shared memory of the histogram kernel for a table of R rows and dim D.
+size_t hist_smem_bytes(int64_t R, int D) {
+    const int64_t Kp = (R + 15) & ~int64_t(15);
+    return (size_t)(kHistM + D) * Kp * 2 + sizeof(int64_t) * (kHistTilesPerCta * kHistM + 1);
+}
+
+int hist_ctas_per_table(int B) {
+    const int ntiles = (B + kHistM - 1) / kHistM;
+    return (ntiles + kHistTilesPerCta - 1) / kHistTilesPerCta;
+}
+
+template <int DT, typename IDX>
+static cudaError_t launch_hist_t(const FwdArgs& a, const int32_t* hist_tables, int nhist, size_t smem,
+                                 cudaStream_t s) {
+    static size_t configured = 0;  // largest dynamic shared memory set so far
+    if (smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(hist_kernel<DT, IDX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const int per = hist_ctas_per_table(a.B);
+    hist_kernel<DT, IDX><<<(unsigned)(nhist * per), kHistThreads, smem, s>>>(a, hist_tables, per);
+    return cudaGetLastError();
+}
+
+// One launch per table dtype (f16, bf16) that has histogram tables.
+cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_f16, size_t smem_f16,
+                        const int32_t* hist_tables_bf16, int n_bf16, size_t smem_bf16, cudaStream_t s) {
+    if (a.B == 0) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (n_f16 > 0)
+        e = a.idx64 ? launch_hist_t<DT_F16, int64_t>(a, hist_tables_f16, n_f16, smem_f16, s)
+                    : launch_hist_t<DT_F16, int32_t>(a, hist_tables_f16, n_f16, smem_f16, s);
+    if (e == cudaSuccess && n_bf16 > 0)
+        e = a.idx64 ? launch_hist_t<DT_BF16, int64_t>(a, hist_tables_bf16, n_bf16, smem_bf16, s)
+                    : launch_hist_t<DT_BF16, int32_t>(a, hist_tables_bf16, n_bf16, smem_bf16, s);
+    return e;
+}
+
+}  // namespace tbe

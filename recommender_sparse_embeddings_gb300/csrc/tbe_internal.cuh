@@ -254,6 +254,11 @@ struct FwdArgs {
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 
+// Small-table tensor-core path (hist.cu).
+size_t hist_smem_bytes(int64_t rows, int dim);
+cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_f16, size_t smem_f16,
+                        const int32_t* hist_tables_bf16, int n_bf16, size_t smem_bf16, cudaStream_t s);
+
 struct Workspace {
     uint32_t* counters;   // [64]
     uint32_t* hist;       // [kMaxPasses][kRadix]

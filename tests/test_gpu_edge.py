@@ -118,7 +118,7 @@ def test_mixed_classes_empty_bags_and_weights(index_dtype):
     total_d = sum(d for _, d, _ in specs)
     for pooling in ("sum", "mean"):
         tables = make_tables(specs, seed=5)
-        h = tbe.tbe_create(tables, pooling)
+        h = tbe.tbe_create(tables, pooling, tbe.TBE_FLAG_NO_HISTOGRAM)
         out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, w.to(DEV))
         assert tbe.tbe_get_error(h) == tbe.TBE_OK
         ref, _ = oracle_forward(tables, ind, off, B, w, pooling)
@@ -191,7 +191,7 @@ def test_out_of_range_indices_are_skipped_and_reported():
     tables = make_tables([(50, 64, torch.float32), (30, 32, torch.bfloat16)], seed=15)
     bags = [[[1, 2, -1, 49], [50, 3], []], [[0, 29, 30], [1000], [5]]]
     ind, off, B = csr(bags)
-    h = tbe.tbe_create(tables, "sum")
+    h = tbe.tbe_create(tables, "sum", tbe.TBE_FLAG_NO_HISTOGRAM)
     out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B)
     assert tbe.tbe_get_error(h) == tbe.TBE_ERR_INDEX_OOB
     assert tbe.tbe_get_error(h) == tbe.TBE_OK  # reading clears the flag
@@ -248,7 +248,7 @@ def test_forward_prepare_side_by_side(cid):
     grad = workloads.make_grad(cfg, "cpu", specs)
     cpu_tables = [t.cpu() for t in tables]
     before = [table_bits(t) for t in tables]
-    h = tbe.tbe_create(tables, cfg.pooling)
+    h = tbe.tbe_create(tables, cfg.pooling, tbe.TBE_FLAG_NO_HISTOGRAM)
     ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
     w = None if batch.weights is None else batch.weights.to(DEV)
     ws = tbe.make_workspace(h, batch.N, cfg.B)
