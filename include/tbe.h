@@ -192,7 +192,12 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
  * lookups stream through one warp; longer runs are split into 256-lookup
  * chunks whose partial sums are added in a fixed order), then applies the
  * optimizer once to that row.  grad_out: device fp32 [batch_size, sum of
- * dims].  num_indices and batch_size must equal the prepare call's. */
+ * dims].  num_indices and batch_size must equal the prepare call's.  When
+ * the handle's tables fall into more than one backward class (dtype x row
+ * shape), the class kernels run on side streams owned by the handle that
+ * start after the work already queued on `stream`, and `stream` waits for
+ * all of them before its next work (a fork and join that stream capture
+ * records as well). */
 int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size,
                        const float* grad_out, const tbe_optimizer* opt, void* workspace,
                        size_t workspace_bytes, void* stream);

@@ -31,6 +31,8 @@ struct tbe_handle {
     size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
     int class_begin[kNumClasses] = {};
     int class_count[kNumClasses] = {};
+    int class_slot[kNumClasses] = {};  // per-class chunk list of each present class
+    int num_classes = 0;
     int total_d = 0;
     int max_dim = 0;
     uint64_t total_rows = 0;
@@ -41,6 +43,10 @@ struct tbe_handle {
     int vec_out = 0;
     cudaStream_t side = nullptr;  // preparation stream of tbe_forward_prepare
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    // streams the backward class kernels run on side by side
+    cudaStream_t apply_streams[kApplyStreams] = {};
+    cudaEvent_t ev_apply_fork = nullptr;
+    cudaEvent_t ev_apply_join[kApplyStreams] = {};
 };
 
 namespace {
@@ -64,20 +70,22 @@ bool hist_eligible(const TableDesc& d, int64_t max_rows, size_t smem_limit) {
 }
 
 // Backward class of a table: dtype and row shape (vector lanes for dim 32,
-// 64, 128, 256 when rows and gradient columns are aligned for them).
+// 64, 128, 256 when rows and gradient columns are 16-byte aligned, which the
+// vector classes' 16-byte gradient loads need).
 int backward_class(const TableDesc& d, int total_d) {
     const bool rows16 = ((uintptr_t)d.data % 16) == 0;
     const bool a4 = rows16 && d.doff % 4 == 0 && total_d % 4 == 0;
-    const bool a2 = rows16 && d.doff % 2 == 0 && total_d % 2 == 0;
     int shape = SHAPE_GENERIC;
-    if (d.dim == 32)
-        shape = SHAPE_D32;
-    else if (d.dim == 64 && a2)
-        shape = SHAPE_D64;
-    else if (d.dim == 128 && a4)
-        shape = SHAPE_D128;
-    else if (d.dim == 256 && a4)
-        shape = SHAPE_D256;
+    if (a4) {
+        if (d.dim == 32)
+            shape = SHAPE_D32;
+        else if (d.dim == 64)
+            shape = SHAPE_D64;
+        else if (d.dim == 128)
+            shape = SHAPE_D128;
+        else if (d.dim == 256)
+            shape = SHAPE_D256;
+    }
     return d.dtype * NUM_SHAPES + shape;
 }
 
@@ -87,9 +95,13 @@ int next_pow2(int x) {
     return p;
 }
 
+// Floats per partial-sum row: the widest dim rounded up to 16 bytes, so the
+// vector classes read partial rows with 16-byte loads.
+int part_stride(const tbe_handle* h) { return (h->max_dim + 3) / 4 * 4; }
+
 struct Layout {
     size_t counters, hist, status, rle_status, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
-        long_runs, chunk_run, ustart, partial, total;
+        long_runs, cls_chunks, ustart, partial, total;
     size_t zero_bytes;  // counters..rle_status are zeroed per call
     int64_t max_long, max_chunks;
     int tiles;
@@ -121,9 +133,9 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     L.uniq = take(sizeof(uint32_t) * n);
     L.runstart = take(sizeof(uint32_t) * (n + 1));
     L.long_runs = take(sizeof(uint32_t) * 4 * L.max_long);
-    L.chunk_run = take(sizeof(uint32_t) * L.max_chunks);
+    L.cls_chunks = take(sizeof(uint2) * (size_t)std::max(h->num_classes, 1) * L.max_chunks);
     L.ustart = take(sizeof(uint32_t) * (h->T + 1));
-    L.partial = take(sizeof(float) * (size_t)L.max_chunks * h->max_dim);
+    L.partial = take(sizeof(float) * (size_t)L.max_chunks * part_stride(h));
     L.total = o;
     return L;
 }
@@ -148,7 +160,7 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.uniq = reinterpret_cast<uint32_t*>(p + L.uniq);
     w.runstart = reinterpret_cast<uint32_t*>(p + L.runstart);
     w.long_runs = reinterpret_cast<uint32_t*>(p + L.long_runs);
-    w.chunk_run = reinterpret_cast<uint32_t*>(p + L.chunk_run);
+    w.cls_chunks = reinterpret_cast<uint2*>(p + L.cls_chunks);
     w.ustart = reinterpret_cast<uint32_t*>(p + L.ustart);
     w.partial = reinterpret_cast<float*>(p + L.partial);
     w.max_long = L.max_long;
@@ -299,8 +311,10 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         for (int c = 0; c < kNumClasses; ++c) {
             h->class_begin[c] = (int)order.size();
             h->class_count[c] = (int)by_class[c].size();
+            h->class_slot[c] = by_class[c].empty() ? -1 : h->num_classes++;
             order.insert(order.end(), by_class[c].begin(), by_class[c].end());
         }
+        for (int t = 0; t < num_tables; ++t) h->tabs[t].cslot = h->class_slot[h->tabs[t].cls];
     }
     const size_t bytes = hist_list_offset(num_tables) + sizeof(int32_t) * num_tables;
     e = cudaMalloc(&h->dev, bytes);
@@ -333,6 +347,11 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, greatest);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_apply_fork, cudaEventDisableTiming);
+        for (int i = 0; i < kApplyStreams && e == cudaSuccess; ++i) {
+            e = cudaStreamCreateWithFlags(&h->apply_streams[i], cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_apply_join[i], cudaEventDisableTiming);
+        }
         if (e != cudaSuccess) {
             tbe_destroy(h);
             return TBE_ERR_CUDA;
@@ -347,6 +366,11 @@ void tbe_destroy(tbe_handle* h) {
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
     if (h->side) cudaStreamDestroy(h->side);
+    if (h->ev_apply_fork) cudaEventDestroy(h->ev_apply_fork);
+    for (int i = 0; i < kApplyStreams; ++i) {
+        if (h->ev_apply_join[i]) cudaEventDestroy(h->ev_apply_join[i]);
+        if (h->apply_streams[i]) cudaStreamDestroy(h->apply_streams[i]);
+    }
     if (h->dev) cudaFree(h->dev);
     delete h;
 }
@@ -493,7 +517,7 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.grad = grad_out;
     a.grad_vec = ((uintptr_t)grad_out % 16) == 0;
     a.total_d = h->total_d;
-    a.max_dim = h->max_dim;
+    a.part_stride = part_stride(h);
     a.total_rows = (uint32_t)h->total_rows;
     a.has_scale = 0;
     a.opt = opt->kind;
@@ -501,8 +525,9 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.eps = opt->eps;
     a.state = opt->state;
     a.num_sms = h->num_sms;
-    return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count,
-                                    static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count, h->class_slot,
+                                    static_cast<cudaStream_t>(stream), h->apply_streams, h->ev_apply_fork,
+                                    h->ev_apply_join));
 }
 
 int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,

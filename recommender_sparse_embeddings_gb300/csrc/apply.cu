@@ -5,33 +5,40 @@
 // 256 lookups).
 //
 // One kernel per backward class (table dtype x row shape) present in the
-// handle, so each kernel's registers are sized for one shape only.  A class
-// kernel walks a work list: first the 256-lookup chunks of long runs whose
-// table is in the class (registered by the preparation step), then batches
-// of kBatchRows consecutive distinct keys of the class's tables.  Work items
-// go to warps round-robin.
+// handle, so each kernel's registers are sized for one shape only; the class
+// kernels run side by side on the handle's apply streams.  A class kernel
+// walks a work list: first the 256-lookup chunks of its class's long runs
+// (listed per class by the preparation step), then batches of kBatchRows
+// consecutive distinct keys of the class's tables.  Warps take work items
+// from a per-class atomic counter.
 //
 //  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
 //    batch into pieces of at most R keys and walks each piece's sorted lookups
 //    as one stream: positions, bags and scales are fetched 32 lookups at a
-//    time one chunk ahead, gradient rows GROUP at a time, and each lookup is
+//    time one chunk ahead, gradient rows several at a time, and each lookup is
 //    added to its key's sum.  The piece's table rows are read before the
 //    stream starts so the read overlaps the gradient gather; after the stream
 //    each key gets its optimizer step and its row is stored.  Sums are plain
-//    fp32 in lookup order (at most 255 terms).
+//    fp32 (at most 255 terms).
 //  Long runs, "accumulate": a warp sums one 256-lookup chunk with compensated
 //    (Kahan) fp32 addition and writes the partial; the warp that completes the
-//    last chunk of a run (atomic count after a fence) adds the partials in
-//    chunk order with Kahan addition, updates the row, and resets the count
+//    last chunk of a run (atomic count after a fence) adds the partials in a
+//    fixed order with Kahan addition, updates the row, and resets the count
 //    so the prepared workspace can be applied again.
 //
-// Lanes own columns: lane l holds columns blk*32*VW + l*VW + [0, VW) of each
-// of NB blocks, so gradient rows are read with 4- to 16-byte loads.
+// Lanes own columns: a row is read by a group of LPR lanes (8 for dim 32, 16
+// for dim 64, 32 otherwise), lane l holding columns blk*LPR*4 + (l%LPR)*4 +
+// [0, 4) of each column block, so every gradient load is 16 bytes wide; the
+// 32/LPR groups of a warp take different lookups of the same keys and add
+// their sums at the end.
 #include "tbe_internal.cuh"
 
 namespace tbe {
 
 constexpr int kBatchRows = 16;  // distinct keys per short-run work item
+// Resident CTAs of 256 threads per SM the class kernels are built for (80
+// registers a thread); the grid is one wave of them.
+constexpr int kApplyCtasPerSm = 3;
 
 struct Kahan {
     float s, c;
@@ -62,10 +69,17 @@ __device__ __forceinline__ int table_of(const TableDesc* tabs, int T, uint32_t k
     return lo;
 }
 
+// Row shapes of the vector classes.  A row is read by a group of LPR lanes,
+// each lane holding VW = 4 consecutive columns (16-byte gradient loads) of
+// each of NB column blocks of LPR*4 columns; a warp holds NG = 32/LPR groups,
+// which take different lookups of the same keys and add their sums up at the
+// end.  Small rows thus still keep 16 bytes per lane in flight per load.
 template <int CODE>
 struct ShapeOf {
-    static constexpr int VW = CODE == SHAPE_D64 ? 2 : (CODE == SHAPE_D128 || CODE == SHAPE_D256 ? 4 : 1);
+    static constexpr int VW = 4;
+    static constexpr int LPR = CODE == SHAPE_D32 ? 8 : (CODE == SHAPE_D64 ? 16 : 32);
     static constexpr int NB = CODE == SHAPE_D256 ? 2 : 1;
+    static constexpr int NG = 32 / LPR;
 };
 
 // ------------------------------------------------------- row slice helpers
@@ -73,12 +87,12 @@ struct ShapeOf {
 // A lane's slice of one table row: NB blocks of VW consecutive elements,
 // kept as raw 32-bit words (w[WORDS]) until needed.  Static helpers over a
 // plain word array keep the slices in registers.
-template <int DT, int VW, int NB>
+template <int DT, int VW, int NB, int LPR>
 struct Slice {
     static constexpr int WPB = DT == DT_F32 ? VW : (VW + 1) / 2;  // words per block
     static constexpr int WORDS = WPB * NB;
 
-    __device__ __forceinline__ static int col(int lane, int q) { return q * 32 * VW + lane * VW; }
+    __device__ __forceinline__ static int col(int lane, int q) { return q * LPR * VW + (lane & (LPR - 1)) * VW; }
 
     __device__ __forceinline__ static void load(uint32_t (&w)[WORDS], const void* base, int64_t row, int dim,
                                                 int lane) {
@@ -86,26 +100,11 @@ struct Slice {
         for (int q = 0; q < NB; ++q) {
             const int64_t k = row * dim + col(lane, q);
             if constexpr (DT == DT_F32) {
-                const float* p = reinterpret_cast<const float*>(base) + k;
-                if constexpr (VW == 4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(p);
-                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y; w[q * WPB + 2] = v.z; w[q * WPB + 3] = v.w;
-                } else if constexpr (VW == 2) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(p);
-                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y;
-                } else {
-                    w[q * WPB] = *reinterpret_cast<const uint32_t*>(p);
-                }
+                const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(base) + k);
+                w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y; w[q * WPB + 2] = v.z; w[q * WPB + 3] = v.w;
             } else {
-                const unsigned short* p = reinterpret_cast<const unsigned short*>(base) + k;
-                if constexpr (VW == 4) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(p);
-                    w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y;
-                } else if constexpr (VW == 2) {
-                    w[q * WPB] = *reinterpret_cast<const uint32_t*>(p);
-                } else {
-                    w[q * WPB] = *p;
-                }
+                const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(base) + k);
+                w[q * WPB + 0] = v.x; w[q * WPB + 1] = v.y;
             }
         }
     }
@@ -115,23 +114,12 @@ struct Slice {
 #pragma unroll
         for (int q = 0; q < NB; ++q) {
             const int64_t k = row * dim + col(lane, q);
-            if constexpr (DT == DT_F32) {
-                float* p = reinterpret_cast<float*>(base) + k;
-                if constexpr (VW == 4)
-                    *reinterpret_cast<uint4*>(p) = make_uint4(w[q * WPB], w[q * WPB + 1], w[q * WPB + 2], w[q * WPB + 3]);
-                else if constexpr (VW == 2)
-                    *reinterpret_cast<uint2*>(p) = make_uint2(w[q * WPB], w[q * WPB + 1]);
-                else
-                    *reinterpret_cast<uint32_t*>(p) = w[q * WPB];
-            } else {
-                unsigned short* p = reinterpret_cast<unsigned short*>(base) + k;
-                if constexpr (VW == 4)
-                    *reinterpret_cast<uint2*>(p) = make_uint2(w[q * WPB], w[q * WPB + 1]);
-                else if constexpr (VW == 2)
-                    *reinterpret_cast<uint32_t*>(p) = w[q * WPB];
-                else
-                    *p = (unsigned short)w[q * WPB];
-            }
+            if constexpr (DT == DT_F32)
+                *reinterpret_cast<uint4*>(reinterpret_cast<float*>(base) + k) =
+                    make_uint4(w[q * WPB], w[q * WPB + 1], w[q * WPB + 2], w[q * WPB + 3]);
+            else
+                *reinterpret_cast<uint2*>(reinterpret_cast<unsigned short*>(base) + k) =
+                    make_uint2(w[q * WPB], w[q * WPB + 1]);
         }
     }
 
@@ -156,27 +144,29 @@ struct Slice {
     }
 };
 
-// Loads the lane's VW gradient floats starting at p.
-template <int VW>
-__device__ __forceinline__ void ld_grad(const float* p, float* f) {
-    if constexpr (VW == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-    } else if constexpr (VW == 2) {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(p));
-        f[0] = v.x; f[1] = v.y;
-    } else {
-        f[0] = __ldg(p);
-    }
+// Loads the lane's 4 gradient floats starting at p.
+__device__ __forceinline__ void ld_grad4(const float* p, float* f) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+
+// Sums x over the NG row groups of the warp (butterfly over the lane bits
+// above the group's own; every group ends with the same bits).
+template <int LPR>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
 }
 
 // Optimizer step for one row given its gradient g (this lane's columns);
 // `row` holds the old values and receives the new ones.  `m_old` is the row's
-// Adagrad state (ignored by SGD); the new state is returned.
-template <int DT, int VW, int NB>
+// Adagrad state (ignored by SGD); the new state is returned.  Every row group
+// holding the same g computes the same result.
+template <int DT, int VW, int NB, int LPR>
 __device__ __forceinline__ float optimizer_step(const ApplyArgs& a, int dim, const float (&g)[NB][VW],
-                                                uint32_t (&row)[Slice<DT, VW, NB>::WORDS], float m_old) {
-    using S = Slice<DT, VW, NB>;
+                                                uint32_t (&row)[Slice<DT, VW, NB, LPR>::WORDS], float m_old) {
+    using S = Slice<DT, VW, NB, LPR>;
     if (a.opt == 2) {
         float sq = 0.f;
 #pragma unroll
@@ -184,7 +174,7 @@ __device__ __forceinline__ float optimizer_step(const ApplyArgs& a, int dim, con
 #pragma unroll
             for (int v = 0; v < VW; ++v) sq = fmaf(g[q][v], g[q][v], sq);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        for (int o = LPR / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
         const float m = m_old + __fdiv_rn(sq, (float)dim);
         const float denom = sqrtf(m) + a.eps;
 #pragma unroll
@@ -225,17 +215,16 @@ __device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& w
     return m;
 }
 
-// Gradient rows in flight per lane (GROUP) and keys per piece (R), whose
-// table-row slices and gradient sums stay in registers.  Sized so the live
-// words R * (row words + columns) + GROUP * columns stay within 32 per lane,
-// which keeps the kernels near 64 registers (4 CTAs of 256 threads per SM).
-template <int DT, int VW, int NB>
+// Gradient rows in flight per row group (GROUP; NG*GROUP lookups per warp
+// step, 2 KB of gradient per warp) and keys per piece (R), whose table-row
+// slices and gradient sums stay in registers: R * (row words + columns) +
+// GROUP * columns live words per lane, at most about 40.
+template <int DT, int NB>
 struct ShortTune {
-    static constexpr int WORDS = Slice<DT, VW, NB>::WORDS;
-    static constexpr int COLS = VW * NB;
-    static constexpr int G0 = 16 / COLS;
-    static constexpr int GROUP = G0 > 8 ? 8 : (G0 < 2 ? 2 : G0);
-    static constexpr int R0 = (32 - GROUP * COLS) / (WORDS + COLS);
+    static constexpr int WORDS = Slice<DT, 4, NB, 32>::WORDS;
+    static constexpr int COLS = 4 * NB;
+    static constexpr int GROUP = 4 / NB;
+    static constexpr int R0 = (40 - GROUP * COLS) / (WORDS + COLS);
     static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
 };
 
@@ -251,17 +240,22 @@ struct MetaWindow {
 // keys are taken in pieces of at most R consecutive keys (a long or skipped
 // key ends a piece, so a piece's lookups are exactly its keys' sorted slots);
 // each piece's table rows are read first, then its lookups stream through
-// the window and each is added to its key's sum, then each key gets its
-// optimizer step.
-template <int DT, int VW, int NB>
+// the window, NG*GROUP per step (row group g takes lookups g, g + NG, ...),
+// and each is added to its key's sum; the groups' sums are added up and each
+// key gets its optimizer step.
+template <int DT, int CODE>
 __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                                 const TableDesc& td, int t, uint32_t rs, uint32_t key, float mstate,
                                                 uint32_t rows, int lane) {
-    using Tn = ShortTune<DT, VW, NB>;
-    using S = Slice<DT, VW, NB>;
+    using Sh = ShapeOf<CODE>;
+    constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
+    using Tn = ShortTune<DT, NB>;
+    using S = Slice<DT, VW, NB, LPR>;
     constexpr int R = Tn::R;
     constexpr int GROUP = Tn::GROUP;
     constexpr int WORDS = S::WORDS;
+    constexpr int STEP = NG * GROUP;
+    const int grp = lane / LPR;
     const int64_t tB = (int64_t)t * a.B;
     const int lastrow = 31 - __clz(rows);
     const uint32_t Eend = __shfl_sync(0xffffffffu, rs, lastrow + 1);
@@ -278,6 +272,13 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
         rows &= ~(((1u << nk) - 1u) << f);
         const uint32_t E0 = __shfl_sync(0xffffffffu, rs, f);
         const uint32_t E1 = __shfl_sync(0xffffffffu, rs, f + nk);
+        // first slots of the piece's later keys (a lookup's slot counts them)
+        uint32_t pr[R];
+#pragma unroll
+        for (int k = 1; k < R; ++k) {
+            const uint32_t x = __shfl_sync(0xffffffffu, rs, (f + k) & 31);
+            pr[k] = k < nk ? x : 0xffffffffu;
+        }
 
         // table rows of the piece (their loads overlap the stream below)
         uint32_t wrow[R][WORDS];
@@ -300,7 +301,7 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
 #pragma unroll
                 for (int v = 0; v < VW; ++v) acc[s][q][v] = 0.f;
 
-        for (uint32_t i = E0; i < E1; i += GROUP) {
+        for (uint32_t i = E0; i < E1; i += STEP) {
             while (i >= win.w0 + 32) {  // slide: keep [w0, w0 + 64) ahead of i
                 win.m0 = win.m1;
                 win.w0 += 32;
@@ -311,7 +312,8 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
             float g[GROUP][NB][VW];
 #pragma unroll
             for (int u = 0; u < GROUP; ++u) {
-                const uint32_t e = i + u - win.w0;  // 0..63
+                const uint32_t li = i + (uint32_t)(u * NG + grp);  // this group's lookup
+                const uint32_t e = li - win.w0;                     // 0..63 (STEP <= 32)
                 const int src = (int)(e & 31u);
                 const bool hi = e >= 32u;
                 const int b0 = __shfl_sync(0xffffffffu, win.m0.b, src);
@@ -320,14 +322,15 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
                 const float s1 = __shfl_sync(0xffffffffu, win.m1.s, src);
                 const int b = hi ? b1 : b0;
                 ss[u] = hi ? s1 : s0;
-                // slot of lookup i+u: how many of the piece's later keys start at or before it
-                const int slot = __popc(__ballot_sync(0xffffffffu, lane > f && lane < f + nk && rs <= i + u));
-                sl[u] = (i + u < E1 && b >= 0) ? slot : -1;
+                int slot = 0;
+#pragma unroll
+                for (int k = 1; k < R; ++k) slot += pr[k] <= li ? 1 : 0;
+                sl[u] = (li < E1 && b >= 0) ? slot : -1;
                 const float* grow = a.grad + (int64_t)(b < 0 ? 0 : b) * a.total_d + td.doff;
 #pragma unroll
                 for (int q = 0; q < NB; ++q) {
                     if (sl[u] >= 0) {
-                        ld_grad<VW>(grow + S::col(lane, q), g[u][q]);
+                        ld_grad4(grow + S::col(lane, q), g[u][q]);
                     } else {
 #pragma unroll
                         for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
@@ -347,15 +350,21 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
                         for (int v = 0; v < VW; ++v) acc[s][q][v] = fmaf(w, g[u][q][v], acc[s][q][v]);
                 }
         }
-        // one optimizer step per key of the piece
+        // one optimizer step per key of the piece; group 0 stores the rows
 #pragma unroll
         for (int s = 0; s < R; ++s) {
             if (s < nk) {
+                if constexpr (NG > 1) {
+#pragma unroll
+                    for (int q = 0; q < NB; ++q)
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) acc[s][q][v] = group_sum<LPR>(acc[s][q][v]);
+                }
                 const int r = f + s;
                 const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
                 const float m_old = __shfl_sync(0xffffffffu, mstate, r);
-                const float mnew = optimizer_step<DT, VW, NB>(a, td.dim, acc[s], wrow[s], m_old);
-                S::store(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
+                const float mnew = optimizer_step<DT, VW, NB, LPR>(a, td.dim, acc[s], wrow[s], m_old);
+                if (grp == 0) S::store(wrow[s], td.data, (int64_t)kr - td.rowbase, td.dim, lane);
                 if (a.opt == 2 && lane == r) a.state[kr] = mnew;
             }
         }
@@ -392,7 +401,7 @@ __device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace&
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int c = cb + lane + 32 * j;
-                        if (c < D) acc[j].add(__ldcg(partial_src + (int64_t)ch * a.max_dim + c));
+                        if (c < D) acc[j].add(__ldcg(partial_src + (int64_t)ch * a.part_stride + c));
                     }
             } else {
                 for (uint32_t i = s0; i < s1; ++i) {
@@ -459,19 +468,25 @@ __device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace&
             generic_row<DT>(a, ws, pos_sorted, td, t, kr, s0, s1, nullptr, 0, lane);
         }
     } else if (rows) {
-        short_batch_vec<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, ws, pos_sorted, td, t, rs, key, mstate,
-                                                                  rows, lane);
+        short_batch_vec<DT, CODE>(a, ws, pos_sorted, td, t, rs, key, mstate, rows, lane);
     }
 }
 
 // -------------------------------------------------------------- long runs
 
-template <int DT, int VW, int NB>
+// Partial sum of one chunk, lookups [s0, s1) of one key: row group g adds
+// lookups g, g + NG, ... with compensated addition, GROUP gradient rows in
+// flight; the groups' sums are added and group 0 writes the partial row.
+template <int DT, int CODE>
 __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                                const TableDesc& td, int t, uint32_t s0, uint32_t s1,
                                                float* part_row, int lane) {
-    using S = Slice<DT, VW, NB>;
-    constexpr int GROUP = VW * NB >= 8 ? 2 : 4;  // gradient rows in flight per lane
+    using Sh = ShapeOf<CODE>;
+    constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
+    using S = Slice<DT, VW, NB, LPR>;
+    constexpr int GROUP = 4 / NB;  // gradient rows in flight per row group
+    constexpr int STEP = NG * GROUP;
+    const int grp = lane / LPR;
     const int64_t tB = (int64_t)t * a.B;
     Kahan acc[NB][VW];
 #pragma unroll
@@ -499,21 +514,23 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
         float ns;
         meta(c0 + 32, nb, ns);
         const int n = (int)tmin<uint32_t>(32u, s1 - c0);
-        for (int k0 = 0; k0 < n; k0 += GROUP) {
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += STEP) {
+            if (k0 >= n) break;
             int bb[GROUP];
             float ss[GROUP];
             float g[GROUP][NB][VW];
 #pragma unroll
             for (int u = 0; u < GROUP; ++u) {
-                const int src = (k0 + u) & 31;
-                bb[u] = __shfl_sync(0xffffffffu, cb, src);
-                ss[u] = __shfl_sync(0xffffffffu, cs, src);
-                if (k0 + u >= n) bb[u] = -1;
+                const int e = k0 + u * NG + grp;  // this group's lookup within the 32
+                bb[u] = __shfl_sync(0xffffffffu, cb, e);
+                ss[u] = __shfl_sync(0xffffffffu, cs, e);
+                if (e >= n) bb[u] = -1;
                 const float* grow = a.grad + (int64_t)(bb[u] < 0 ? 0 : bb[u]) * a.total_d + td.doff;
 #pragma unroll
                 for (int q = 0; q < NB; ++q) {
                     if (bb[u] >= 0) {
-                        ld_grad<VW>(grow + S::col(lane, q), g[u][q]);
+                        ld_grad4(grow + S::col(lane, q), g[u][q]);
                     } else {
 #pragma unroll
                         for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
@@ -534,48 +551,63 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) part_row[S::col(lane, q) + v] = acc[q][v].value();
+        for (int v = 0; v < VW; ++v) {
+            float x = acc[q][v].value();
+            if constexpr (NG > 1) x = group_sum<LPR>(x);
+            if (grp == 0) part_row[S::col(lane, q) + v] = x;
+        }
 }
 
-template <int DT, int VW, int NB>
+// The run's gradient: its nc partial rows added in chunk order (row group g
+// takes chunks g, g + NG, ..., PF rows in flight; compensated addition; the
+// groups' sums added last), then the row's optimizer step.
+template <int DT, int CODE>
 __device__ __forceinline__ void long_combine(const ApplyArgs& a, const TableDesc& td, uint32_t key,
                                              const float* part0, uint32_t nc, int lane) {
-    using S = Slice<DT, VW, NB>;
+    using Sh = ShapeOf<CODE>;
+    constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
+    using S = Slice<DT, VW, NB, LPR>;
+    const int grp = lane / LPR;
     Kahan acc[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    constexpr int PF = 2;  // partial rows in flight
-    for (uint32_t j0 = 0; j0 < nc; j0 += PF) {
-        float x[PF][NB][VW];
+    constexpr int PF = 8 / NB;  // partial rows in flight per row group
+    for (uint32_t j0 = 0; j0 < nc; j0 += PF * NG) {
+        float4 x[PF][NB];
 #pragma unroll
         for (int k = 0; k < PF; ++k) {
-            const float* p = part0 + (int64_t)(j0 + k < nc ? j0 + k : j0) * a.max_dim;
+            const uint32_t j = j0 + (uint32_t)(k * NG + grp);
+            const float* p = part0 + (int64_t)(j < nc ? j : 0) * a.part_stride;
 #pragma unroll
-            for (int q = 0; q < NB; ++q)
-#pragma unroll
-                for (int v = 0; v < VW; ++v) x[k][q][v] = __ldcg(p + S::col(lane, q) + v);
+            for (int q = 0; q < NB; ++q) x[k][q] = __ldcg(reinterpret_cast<const float4*>(p + S::col(lane, q)));
         }
 #pragma unroll
         for (int k = 0; k < PF; ++k)
-            if (j0 + k < nc)
+            if (j0 + (uint32_t)(k * NG + grp) < nc)
 #pragma unroll
-                for (int q = 0; q < NB; ++q)
-#pragma unroll
-                    for (int v = 0; v < VW; ++v) acc[q][v].add(x[k][q][v]);
+                for (int q = 0; q < NB; ++q) {
+                    acc[q][0].add(x[k][q].x);
+                    acc[q][1].add(x[k][q].y);
+                    acc[q][2].add(x[k][q].z);
+                    acc[q][3].add(x[k][q].w);
+                }
     }
     float g[NB][VW];
 #pragma unroll
     for (int q = 0; q < NB; ++q)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) g[q][v] = acc[q][v].value();
+        for (int v = 0; v < VW; ++v) {
+            g[q][v] = acc[q][v].value();
+            if constexpr (NG > 1) g[q][v] = group_sum<LPR>(g[q][v]);
+        }
     uint32_t row[S::WORDS];
     const int64_t r = (int64_t)key - td.rowbase;
     S::load(row, td.data, r, td.dim, lane);
     const float m_old = a.opt == 2 ? a.state[key] : 0.f;
-    const float m = optimizer_step<DT, VW, NB>(a, td.dim, g, row, m_old);
-    S::store(row, td.data, r, td.dim, lane);
+    const float m = optimizer_step<DT, VW, NB, LPR>(a, td.dim, g, row, m_old);
+    if (grp == 0) S::store(row, td.data, r, td.dim, lane);
     if (a.opt == 2 && lane == 0) a.state[key] = m;
 }
 
@@ -583,7 +615,7 @@ template <int DT, int CODE>
 __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                           const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
                                           uint32_t chunk, uint32_t li, uint32_t base, uint32_t nc, int lane) {
-    float* part_row = ws.partial + (int64_t)chunk * a.max_dim;
+    float* part_row = ws.partial + (int64_t)chunk * a.part_stride;
     // 1) this chunk's partial sum
     if constexpr (CODE == SHAPE_GENERIC) {
         const int D = td.dim;
@@ -612,7 +644,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
             }
         }
     } else {
-        long_chunk_vec<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
+        long_chunk_vec<DT, CODE>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
     }
     // 2) the warp that finishes a run's last chunk combines all of them
     __threadfence();
@@ -622,11 +654,11 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
     done = __shfl_sync(0xffffffffu, done, 0);
     if (done != nc - 1) return;
     __threadfence();
-    const float* part0 = ws.partial + (int64_t)base * a.max_dim;
+    const float* part0 = ws.partial + (int64_t)base * a.part_stride;
     if constexpr (CODE == SHAPE_GENERIC)
         generic_row<DT>(a, ws, pos_sorted, td, t, key, 0, 0, part0, nc, lane);
     else
-        long_combine<DT, ShapeOf<CODE>::VW, ShapeOf<CODE>::NB>(a, td, key, part0, nc, lane);
+        long_combine<DT, CODE>(a, td, key, part0, nc, lane);
     // every chunk of this run has been counted: reset for the next apply call
     if (lane == 0) ws.long_runs[4 * li + 3] = 0;
 }
@@ -640,13 +672,14 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 // while work is left; the last warp to finish resets the counter, so apply
 // can run again on the same prepared workspace.
 template <int DT, int CODE>
-__global__ void __launch_bounds__(256) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
+__global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
     __shared__ uint32_t s_bbase[kMaxTables + 1];  // first batch item of each class table
     __shared__ uint32_t s_warp[8];
     a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], (uint32_t)a.N);
-    const uint32_t nchunks = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
+    const uint32_t nchunks =
+        tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_CLS_CHUNK + a.cslot], (uint32_t)ws.max_chunks);
     const uint32_t nlong = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NLONG], (uint32_t)ws.max_long);
 
     // batch counts of the class's tables, exclusive-scanned by the block
@@ -687,21 +720,21 @@ __global__ void __launch_bounds__(256) apply_class_kernel(ApplyArgs a, Workspace
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= items) break;
         if (item < nchunks) {
-            const uint32_t c = item;
-            const uint32_t li = __ldg(ws.chunk_run + c);
+            const uint2 e = __ldg(ws.cls_chunks + (int64_t)a.cslot * ws.max_chunks + item);
+            const uint32_t li = e.x, jc = e.y;
             if (li >= nlong) continue;
             const uint32_t u = __ldg(ws.long_runs + 4 * li), base = __ldg(ws.long_runs + 4 * li + 1),
                            nc = __ldg(ws.long_runs + 4 * li + 2);
-            if (u >= U || c < base || c - base >= nc) continue;
+            if (u >= U || jc >= nc) continue;
             const uint32_t key = __ldg(ws.uniq + u);
             const int t = table_of(a.tabs, a.T, key);
             if (a.tabs[t].cls != a.cls) continue;
             const TableDesc td = a.tabs[t];
             const uint32_t r0 = __ldg(ws.runstart + u);
             const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
-            const uint32_t s0 = r0 + (c - base) * kLongRun;
+            const uint32_t s0 = r0 + jc * kLongRun;
             const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
-            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, c, li, base, nc, lane);
+            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, base + jc, li, base, nc, lane);
         } else {
             const uint32_t j = item - nchunks;
             int lo = 0, hi = a.class_count - 1;  // last class table with s_bbase <= j
@@ -747,27 +780,50 @@ static cudaError_t launch_dtype(const ApplyArgs& a, const Workspace& ws, const u
 }
 
 cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, cudaStream_t s) {
+                         const int* class_begin, const int* class_count, const int* class_slot, cudaStream_t s,
+                         const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join) {
     if (a_in.N == 0) return cudaSuccess;
     const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
-    const unsigned grid = (unsigned)(a_in.num_sms * 4);
+    const unsigned grid = (unsigned)(a_in.num_sms * kApplyCtasPerSm);
+    int present = 0;
+    for (int cls = 0; cls < kNumClasses; ++cls) present += class_count[cls] > 0;
+    // more than one class: fork onto the side streams, which start after
+    // everything already queued on s
+    const bool fork = present > 1;
+    if (fork) {
+        cudaError_t e = cudaEventRecord(ev_fork, s);
+        for (int i = 0; i < kApplyStreams && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(streams[i], ev_fork, 0);
+        if (e != cudaSuccess) return e;
+    }
+    int k = 0;
     for (int cls = 0; cls < kNumClasses; ++cls) {
         if (class_count[cls] == 0) continue;
         ApplyArgs a = a_in;
         a.cls = cls;
+        a.cslot = class_slot[cls];
         a.class_tables = class_tables + class_begin[cls];
         a.class_count = class_count[cls];
         const int dt = cls / NUM_SHAPES;
         // an unaligned gradient buffer rules out vector loads: element-wise
         const int code = a.grad_vec ? cls % NUM_SHAPES : SHAPE_GENERIC;
+        cudaStream_t cs = fork ? streams[k % kApplyStreams] : s;
+        ++k;
         cudaError_t e;
         if (dt == DT_F32)
-            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, s);
+            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, cs);
         else if (dt == DT_F16)
-            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, s);
+            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, cs);
         else
-            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, s);
+            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, cs);
         if (e != cudaSuccess) return e;
+    }
+    if (fork) {
+        // join: s waits for every side stream
+        for (int i = 0; i < kApplyStreams; ++i) {
+            cudaError_t e = cudaEventRecord(ev_join[i], streams[i]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_join[i], 0);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -382,7 +382,12 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
                     ws.long_runs[4 * li + 1] = base;
                     ws.long_runs[4 * li + 2] = nc;
                     ws.long_runs[4 * li + 3] = 0;
-                    for (uint32_t j = 0; j < nc; ++j) ws.chunk_run[base + j] = li;
+                    // the chunks join the list of the table's backward class
+                    // (at most the registered total, so within max_chunks)
+                    const int slot = a.tabs[tk].cslot;
+                    const uint32_t lc = atomicAdd(&ws.counters[CTR_CLS_CHUNK + slot], nc);
+                    uint2* list = ws.cls_chunks + (int64_t)slot * ws.max_chunks + lc;
+                    for (uint32_t j = 0; j < nc; ++j) list[j] = make_uint2(li, j);
                 }
             }
         }

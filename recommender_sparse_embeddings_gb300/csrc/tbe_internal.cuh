@@ -51,7 +51,7 @@ struct TableDesc {
     int32_t vecs;       // column blocks of 32 vectors per row (vector path, 1..4)
     int32_t warp_begin; // first warp of this table in the forward warp map
     int32_t cls;        // backward class: dtype * NUM_SHAPES + row shape code
-    int32_t pad_;
+    int32_t cslot;      // index of the table's backward class among the handle's classes
 };
 
 // Device-resident descriptor block owned by a handle.
@@ -271,9 +271,9 @@ struct Workspace {
     uint32_t* uniq;       // [N]
     uint32_t* runstart;   // [N+1]
     uint32_t* long_runs;  // [max_long][4]: unique index, first chunk, chunk count, chunks done
-    uint32_t* chunk_run;  // [max_chunks]: long-run index of each chunk
+    uint2* cls_chunks;    // [classes][max_chunks]: (long-run index, chunk within the run) per class
     uint32_t* ustart;     // [T+1]: first distinct-key index of each table (ustart[T]: end)
-    float* partial;       // [max_chunks][max_dim]
+    float* partial;       // [max_chunks][part_stride]
     int64_t max_long;
     int64_t max_chunks;
     int tiles;
@@ -290,6 +290,7 @@ enum : int {
     CTR_PASS_TILE = 4,  // tile claim counters of the sort passes [4]
     CTR_WORK = 8,       // apply work-item counters, one per backward class [15]
     CTR_EXIT = 24,      // apply finished-warp counters, one per backward class [15]
+    CTR_CLS_CHUNK = 40, // chunks registered per backward class slot [15]
     CTR_HAS_SCALE = 63, // nonzero when prepare wrote the per-lookup scale array
     CTR_COUNT = 64,
 };
@@ -326,7 +327,7 @@ struct ApplyArgs {
     const float* grad;
     int grad_vec;  // grad is 16-byte aligned (vector loads allowed)
     int total_d;
-    int max_dim;
+    int part_stride;  // floats per partial-sum row (multiple of 4)
     uint32_t total_rows;
     int has_scale;  // filled in on the device from CTR_HAS_SCALE
     int opt;
@@ -337,11 +338,20 @@ struct ApplyArgs {
     const int32_t* class_tables;  // tables of the launched class (device)
     int class_count;
     int cls;
+    int cslot;  // the class's slot in the per-class chunk lists
 };
 
+// Streams the backward class kernels are spread over: each class kernel
+// takes its work from its own counter, so they may run side by side and one
+// class's tail overlaps the next class's work.
+constexpr int kApplyStreams = 4;
+
 // One launch per backward class present: class_tables lists the tables of
-// every class (device, grouped by class); class_begin/class_count index it.
+// every class (device, grouped by class); class_begin/class_count index it
+// and class_slot gives each class's per-class chunk list.  With more than one
+// class, the launches fork from s onto the given streams and s waits for all.
 cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, cudaStream_t s);
+                         const int* class_begin, const int* class_count, const int* class_slot, cudaStream_t s,
+                         const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join);
 
 }  // namespace tbe
