@@ -376,7 +376,9 @@ def run_ours(args):
     # U (distinct keys) for the byte count: read once after the run
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
-    passes = (max(1, (h.total_rows).bit_length()) + 7) // 8
+    # radix passes of the sort: 8-bit digits, or 9-bit ones when they save a pass
+    key_bits = max(1, h.total_rows.bit_length())
+    passes = min((key_bits + 7) // 8, (key_bits + 8) // 9)
     nbytes = algorithmic_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize, w is not None,
                                cfg.optimizer, U, passes)
     nbytes["forward+prepare"] = nbytes["forward"] + nbytes["prepare"]
@@ -386,7 +388,14 @@ def run_ours(args):
     seg_ms = {k: v / args.steps for k, v in seg.items()}
     dominant = max(seg_ms, key=seg_ms.get)
     achieved = nbytes[dominant] / (seg_ms[dominant] / 1e3) / 1e9
-    launches_per_step = 2 + (2 + passes) + backward_classes(specs)  # pool+long, keys+passes+rle, apply
+    # our kernels per step: forward (gather pool if any gather table, long
+    # bags, one histogram launch per dtype with histogram tables), prepare
+    # (bag marks, keys, one per radix pass, run-length, long runs), apply
+    # (one per backward class)
+    paths = tbe.tbe_table_paths(h)
+    hist_dtypes = {s.dtype for s, p in zip(specs, paths) if p == "histogram"}
+    fwd_launches = (1 if any(p != "histogram" for p in paths) else 0) + 1 + len(hist_dtypes)
+    launches_per_step = fwd_launches + (2 + passes + 2) + backward_classes(specs)
 
     # end-to-end through the public API: inputs from pinned host memory every
     # step, pooled output read back every step
@@ -453,7 +462,7 @@ def run_ours(args):
             "dtype": "f32" if all(s.dtype == "f32" for s in specs) else "mixed(f32 accumulate)",
             "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
                     "pages' production shard configurations)",
-            "paths": sorted(set(tbe.tbe_table_paths(h))),
+            "paths": sorted(set(paths)),
             "config": {"workload": cfg.description + (
                            f" (first {T} of the tables)" if args.tables else ""),
                        "config_id": cfg.cfg_id, "T": T, "B": B,

@@ -31,12 +31,11 @@ struct tbe_handle {
     size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
     int class_begin[kNumClasses] = {};
     int class_count[kNumClasses] = {};
-    int class_slot[kNumClasses] = {};  // per-class chunk list of each present class
-    int num_classes = 0;
     int total_d = 0;
     int max_dim = 0;
     uint64_t total_rows = 0;
     int key_bits = 1;
+    int digit_bits = 8;
     int passes = 1;
     int last_B = -1;
     int parity = 0;
@@ -100,10 +99,10 @@ int next_pow2(int x) {
 int part_stride(const tbe_handle* h) { return (h->max_dim + 3) / 4 * 4; }
 
 struct Layout {
-    size_t counters, hist, status, rle_status, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
-        long_runs, cls_chunks, ustart, partial, total;
-    size_t zero_bytes;  // counters..rle_status are zeroed per call
-    int64_t max_long, max_chunks;
+    size_t counters, hist, status, rle_status, run_status, tile_bag, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
+        chunk_info, chunk_done, cstart, ustart, partial, total;
+    size_t zero_bytes;  // counters..tile_bag are zeroed per call
+    int64_t max_chunks;
     int tiles;
 };
 
@@ -111,7 +110,6 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     Layout L{};
     const int64_t n = std::max<int64_t>(N, 1);
     L.tiles = (int)((N + kSortTile - 1) / kSortTile);
-    L.max_long = N / kLongRun + 1;
     L.max_chunks = 2 * (N / kLongRun) + 2;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -120,9 +118,11 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
         return at;
     };
     L.counters = take(sizeof(uint32_t) * CTR_COUNT);
-    L.hist = take(sizeof(uint32_t) * kMaxPasses * kRadix);
-    L.status = take(sizeof(uint32_t) * (size_t)h->passes * std::max(L.tiles, 1) * kRadix);
+    L.hist = take(sizeof(uint32_t) * kMaxPasses * kMaxRadix);
+    L.status = take(sizeof(uint32_t) * (size_t)h->passes * std::max(L.tiles, 1) * ((size_t)1 << h->digit_bits));
     L.rle_status = take(sizeof(uint32_t) * std::max(L.tiles, 1));
+    L.run_status = take(sizeof(uint32_t) * std::max(L.tiles, 1));
+    L.tile_bag = take(sizeof(uint32_t) * std::max(L.tiles, 1));
     L.zero_bytes = o;
     L.keys0 = take(sizeof(uint32_t) * n);
     L.keys1 = take(sizeof(uint32_t) * n);
@@ -132,8 +132,9 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     L.scale = scale ? take(sizeof(float) * n) : 0;
     L.uniq = take(sizeof(uint32_t) * n);
     L.runstart = take(sizeof(uint32_t) * (n + 1));
-    L.long_runs = take(sizeof(uint32_t) * 4 * L.max_long);
-    L.cls_chunks = take(sizeof(uint2) * (size_t)std::max(h->num_classes, 1) * L.max_chunks);
+    L.chunk_info = take(sizeof(uint2) * L.max_chunks);
+    L.chunk_done = take(sizeof(uint32_t) * L.max_chunks);
+    L.cstart = take(sizeof(uint32_t) * (h->T + 1));
     L.ustart = take(sizeof(uint32_t) * (h->T + 1));
     L.partial = take(sizeof(float) * (size_t)L.max_chunks * part_stride(h));
     L.total = o;
@@ -151,6 +152,7 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.hist = reinterpret_cast<uint32_t*>(p + L.hist);
     w.status = reinterpret_cast<uint32_t*>(p + L.status);
     w.rle_status = reinterpret_cast<uint32_t*>(p + L.rle_status);
+    w.tile_bag = reinterpret_cast<uint32_t*>(p + L.tile_bag);
     w.keys[0] = reinterpret_cast<uint32_t*>(p + L.keys0);
     w.keys[1] = reinterpret_cast<uint32_t*>(p + L.keys1);
     w.vals[0] = reinterpret_cast<uint32_t*>(p + L.vals0);
@@ -159,14 +161,16 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.scale = scale ? reinterpret_cast<float*>(p + L.scale) : nullptr;
     w.uniq = reinterpret_cast<uint32_t*>(p + L.uniq);
     w.runstart = reinterpret_cast<uint32_t*>(p + L.runstart);
-    w.long_runs = reinterpret_cast<uint32_t*>(p + L.long_runs);
-    w.cls_chunks = reinterpret_cast<uint2*>(p + L.cls_chunks);
+    w.chunk_info = reinterpret_cast<uint2*>(p + L.chunk_info);
+    w.chunk_done = reinterpret_cast<uint32_t*>(p + L.chunk_done);
+    w.cstart = reinterpret_cast<uint32_t*>(p + L.cstart);
+    w.run_status = reinterpret_cast<uint32_t*>(p + L.run_status);
     w.ustart = reinterpret_cast<uint32_t*>(p + L.ustart);
     w.partial = reinterpret_cast<float*>(p + L.partial);
-    w.max_long = L.max_long;
     w.max_chunks = L.max_chunks;
     w.tiles = L.tiles;
     w.passes = h->passes;
+    w.digit_bits = h->digit_bits;
     // the sort ping-pongs once per pass, starting from buffer 0
     w.sorted_buf = h->passes % 2;
     return w;
@@ -270,7 +274,11 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     int bits = 1;
     while (bits < 32 && (uint64_t(1) << bits) <= h->total_rows) ++bits;  // values 0..total_rows
     h->key_bits = bits;
-    h->passes = (bits + kRadixBits - 1) / kRadixBits;
+    // 8-bit digits, or 9-bit ones when they save a pass
+    h->digit_bits = (bits + kMaxRadixBits - 1) / kMaxRadixBits < (bits + kRadixBits - 1) / kRadixBits
+                        ? kMaxRadixBits
+                        : kRadixBits;
+    h->passes = (bits + h->digit_bits - 1) / h->digit_bits;
 
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
@@ -311,10 +319,8 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         for (int c = 0; c < kNumClasses; ++c) {
             h->class_begin[c] = (int)order.size();
             h->class_count[c] = (int)by_class[c].size();
-            h->class_slot[c] = by_class[c].empty() ? -1 : h->num_classes++;
             order.insert(order.end(), by_class[c].begin(), by_class[c].end());
         }
-        for (int t = 0; t < num_tables; ++t) h->tabs[t].cslot = h->class_slot[h->tabs[t].cls];
     }
     const size_t bytes = hist_list_offset(num_tables) + sizeof(int32_t) * num_tables;
     e = cudaMalloc(&h->dev, bytes);
@@ -469,6 +475,7 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     a.mean = h->pooling == TBE_POOL_MEAN;
     a.total_rows = (uint32_t)h->total_rows;
     a.key_bits = h->key_bits;
+    a.digit_bits = h->digit_bits;
     return cuda_status(launch_prepare(a, w, s));
 }
 
@@ -525,7 +532,7 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.eps = opt->eps;
     a.state = opt->state;
     a.num_sms = h->num_sms;
-    return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count, h->class_slot,
+    return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count,
                                     static_cast<cudaStream_t>(stream), h->apply_streams, h->ev_apply_fork,
                                     h->ev_apply_join));
 }

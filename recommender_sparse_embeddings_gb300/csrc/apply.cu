@@ -7,10 +7,10 @@
 // One kernel per backward class (table dtype x row shape) present in the
 // handle, so each kernel's registers are sized for one shape only; the class
 // kernels run side by side on the handle's apply streams.  A class kernel
-// walks a work list: first the 256-lookup chunks of its class's long runs
-// (listed per class by the preparation step), then batches of kBatchRows
-// consecutive distinct keys of the class's tables.  Warps take work items
-// from a per-class atomic counter.
+// walks a work list table by table: the 256-lookup chunks of the table's
+// long runs (numbered in key order by the preparation step), then batches of
+// kBatchRows consecutive distinct keys.  Warps take work items from a
+// per-class atomic counter.
 //
 //  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
 //    batch into pieces of at most R keys and walks each piece's sorted lookups
@@ -57,17 +57,6 @@ struct Kahan {
     __device__ __forceinline__ float value() const { return s - c; }
 };
 
-__device__ __forceinline__ int table_of(const TableDesc* tabs, int T, uint32_t key) {
-    int lo = 0, hi = T - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((uint64_t)tabs[mid].rowbase <= key)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
 
 // Row shapes of the vector classes.  A row is read by a group of LPR lanes,
 // each lane holding VW = 4 consecutive columns (16-byte gradient loads) of
@@ -614,7 +603,7 @@ __device__ __forceinline__ void long_combine(const ApplyArgs& a, const TableDesc
 template <int DT, int CODE>
 __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                           const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
-                                          uint32_t chunk, uint32_t li, uint32_t base, uint32_t nc, int lane) {
+                                          uint32_t chunk, uint32_t base, uint32_t nc, int lane) {
     float* part_row = ws.partial + (int64_t)chunk * a.part_stride;
     // 1) this chunk's partial sum
     if constexpr (CODE == SHAPE_GENERIC) {
@@ -650,7 +639,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
     __threadfence();
     __syncwarp();
     uint32_t done = 0;
-    if (lane == 0) done = atomicAdd(&ws.long_runs[4 * li + 3], 1u);
+    if (lane == 0) done = atomicAdd(ws.chunk_done + base, 1u);
     done = __shfl_sync(0xffffffffu, done, 0);
     if (done != nc - 1) return;
     __threadfence();
@@ -660,40 +649,44 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
     else
         long_combine<DT, CODE>(a, td, key, part0, nc, lane);
     // every chunk of this run has been counted: reset for the next apply call
-    if (lane == 0) ws.long_runs[4 * li + 3] = 0;
+    if (lane == 0) ws.chunk_done[base] = 0;
 }
 
 // ------------------------------------------------------------------ kernel
 
-// All work of one backward class (table dtype DT, row shape CODE): first the
-// long-run chunks whose table is in the class, then the short-run batches of
-// the class's tables, kBatchRows distinct keys each.  Warps take items one at
-// a time from an atomic counter (heavier chunks first), so no warp idles
-// while work is left; the last warp to finish resets the counter, so apply
-// can run again on the same prepared workspace.
+// All work of one backward class (table dtype DT, row shape CODE), table by
+// table in key order: each class table's long-run chunks (one consecutive
+// range cstart[t] .. cstart[t+1]), then its short-run batches of kBatchRows
+// distinct keys.  Neighbouring work items thus read gradient columns of the
+// same table, which keeps them in L2.  Warps take items one at a time from an
+// atomic counter, so no warp idles while work is left; the last warp to
+// finish resets the counter, so apply can run again on the same prepared
+// workspace.
 template <int DT, int CODE>
 __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
-    __shared__ uint32_t s_bbase[kMaxTables + 1];  // first batch item of each class table
+    __shared__ uint32_t s_ibase[kMaxTables + 1];  // first work item of each class table
     __shared__ uint32_t s_warp[8];
     a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], (uint32_t)a.N);
     const uint32_t nchunks =
-        tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_CLS_CHUNK + a.cslot], (uint32_t)ws.max_chunks);
-    const uint32_t nlong = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NLONG], (uint32_t)ws.max_long);
+        tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
+    const uint32_t N = (uint32_t)a.N;
 
-    // batch counts of the class's tables, exclusive-scanned by the block
+    // work items (chunks + batches) of the class's tables, exclusive-scanned
     uint32_t carry = 0;
     for (int base = 0; base < a.class_count; base += 256) {
         const int k = base + threadIdx.x;
-        uint32_t nb = 0;
+        uint32_t ni = 0;
         if (k < a.class_count) {
             const int t = a.class_tables[k];
             const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
             const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
-            nb = (ue - us + kBatchRows - 1) / kBatchRows;
+            const uint32_t cs = tmin<uint32_t>(__ldg(ws.cstart + t), nchunks);
+            const uint32_t ce = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.cstart + t + 1), cs), nchunks);
+            ni = (ce - cs) + (ue - us + kBatchRows - 1) / kBatchRows;
         }
-        uint32_t x = nb;
+        uint32_t x = ni;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
@@ -706,51 +699,55 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
             if (w < warp) before += s_warp[w];
             total += s_warp[w];
         }
-        if (k < a.class_count) s_bbase[k] = carry + before + x - nb;
+        if (k < a.class_count) s_ibase[k] = carry + before + x - ni;
         carry += total;
         __syncthreads();
     }
-    if (threadIdx.x == 0) s_bbase[a.class_count] = carry;
+    if (threadIdx.x == 0) s_ibase[a.class_count] = carry;
     __syncthreads();
-    const uint32_t items = nchunks + carry;
+    const uint32_t items = carry;
 
     for (;;) {
         uint32_t item = 0;
         if (lane == 0) item = atomicAdd(&ws.counters[CTR_WORK + a.cls], 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= items) break;
-        if (item < nchunks) {
-            const uint2 e = __ldg(ws.cls_chunks + (int64_t)a.cslot * ws.max_chunks + item);
-            const uint32_t li = e.x, jc = e.y;
-            if (li >= nlong) continue;
-            const uint32_t u = __ldg(ws.long_runs + 4 * li), base = __ldg(ws.long_runs + 4 * li + 1),
-                           nc = __ldg(ws.long_runs + 4 * li + 2);
-            if (u >= U || jc >= nc) continue;
-            const uint32_t key = __ldg(ws.uniq + u);
-            const int t = table_of(a.tabs, a.T, key);
-            if (a.tabs[t].cls != a.cls) continue;
-            const TableDesc td = a.tabs[t];
+        int lo = 0, hi = a.class_count - 1;  // last class table with s_ibase <= item
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_ibase[mid] <= item)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int t = a.class_tables[lo];
+        const TableDesc td = a.tabs[t];
+        const uint32_t j = item - s_ibase[lo];
+        const uint32_t cs = tmin<uint32_t>(__ldg(ws.cstart + t), nchunks);
+        const uint32_t ce = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.cstart + t + 1), cs), nchunks);
+        if (j < ce - cs) {
+            // one 256-lookup chunk of a long run of this table
+            const uint32_t g = cs + j;
+            const uint2 e = __ldg(ws.chunk_info + g);
+            const uint32_t u = e.x, g0 = e.y;
+            if (u >= U || g < g0) continue;
             const uint32_t r0 = __ldg(ws.runstart + u);
-            const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), (uint32_t)a.N);
+            const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), N);
+            if (r1 <= r0) continue;
+            const uint32_t nc = (r1 - r0 + kLongRun - 1) / kLongRun;
+            const uint32_t jc = g - g0;
+            const uint32_t key = __ldg(ws.uniq + u);
+            if (jc >= nc || g0 + nc > nchunks || key < (uint64_t)td.rowbase ||
+                (uint64_t)key >= (uint64_t)td.rowbase + (uint64_t)td.rows)
+                continue;
             const uint32_t s0 = r0 + jc * kLongRun;
             const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
-            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, base + jc, li, base, nc, lane);
+            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, g, g0, nc, lane);
         } else {
-            const uint32_t j = item - nchunks;
-            int lo = 0, hi = a.class_count - 1;  // last class table with s_bbase <= j
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (s_bbase[mid] <= j)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            const int t = a.class_tables[lo];
             const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
             const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
-            const uint32_t u0 = us + (j - s_bbase[lo]) * kBatchRows;
+            const uint32_t u0 = us + (j - (ce - cs)) * kBatchRows;
             if (u0 >= ue) continue;
-            const TableDesc td = a.tabs[t];
             short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kBatchRows, ue - u0), lane);
         }
     }
@@ -780,7 +777,7 @@ static cudaError_t launch_dtype(const ApplyArgs& a, const Workspace& ws, const u
 }
 
 cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, const int* class_slot, cudaStream_t s,
+                         const int* class_begin, const int* class_count, cudaStream_t s,
                          const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join) {
     if (a_in.N == 0) return cudaSuccess;
     const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
@@ -800,7 +797,6 @@ cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32
         if (class_count[cls] == 0) continue;
         ApplyArgs a = a_in;
         a.cls = cls;
-        a.cslot = class_slot[cls];
         a.class_tables = class_tables + class_begin[cls];
         a.class_count = class_count[cls];
         const int dt = cls / NUM_SHAPES;

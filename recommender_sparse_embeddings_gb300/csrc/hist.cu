@@ -5,13 +5,14 @@
 //   H[b, r] = sum over the lookups i of bag b with idx_i = r of s_i
 // (s_i = per-sample weight, times 1/L for mean pooling), the pooled rows are
 //   out[b, Doff : Doff + D] = H[b, :] . W   (H: B x R, W: R x D).
-// A CTA of 4 warps keeps W^T (D x R, zero-padded in R to Kp) in shared memory
-// and, for each tile of 128 bags, builds H (128 x Kp) in shared memory with
-// 16-bit atomic adds, issues Kp/16 tcgen05.mma (kind::f16, M=128, N=D, K=16,
-// fp32 accumulation in tensor memory), waits on an mbarrier that
+// A CTA of 16 warps keeps W^T (D x R, zero-padded in R to Kp) in shared
+// memory and, for each tile of 128 bags, builds H (128 x Kp) in shared memory
+// with 16-bit atomic adds, issues Kp/16 tcgen05.mma (kind::f16, M=128, N=D,
+// K=16, fp32 accumulation in tensor memory), waits on an mbarrier that
 // tcgen05.commit arrives on, and reads the accumulator back with tcgen05.ld
-// (warp w owns tensor-memory lanes 32w..32w+31, i.e. bags 32w..32w+31 of the
-// tile).  H and W^T use the no-swizzle K-major layout of 8x16-byte core
+// (warp w may read tensor-memory lanes 32*(w%4) .. +31, i.e. bags 32*(w%4) ..
+// +31 of the tile; the four warps sharing a lane quarter split the columns
+// in 16-column steps).  H and W^T use the no-swizzle K-major layout of 8x16-byte core
 // matrices: element (m, k) of an operand with row stride SBO bytes per 8
 // rows sits at (m/8)*SBO + (k/8)*128 + (m%8)*16 + (k%8)*2.
 //

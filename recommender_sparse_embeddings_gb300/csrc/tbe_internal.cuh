@@ -24,12 +24,16 @@ constexpr int kLongBag = 2048;
 constexpr int kLongBagCap = 1 << 16;
 // Runs of at least this many lookups take the chunked accumulate path.
 constexpr int kLongRun = 256;
-// Keys per tile of the sort and run-length kernels (256 threads x 8).
+// Keys per tile of the key, sort and run-length kernels (256 threads x 16).
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 8;
+constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;
+// Radix digits are 8 bits, or 9 when that saves a pass (keys of 17-18 or
+// 25-27 bits); arrays are sized for the larger.
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
+constexpr int kMaxRadixBits = 9;
+constexpr int kMaxRadix = 1 << kMaxRadixBits;
 constexpr int kMaxPasses = 4;
 // Decoupled look-back status words: 2 flag bits + 30 count bits.
 constexpr uint32_t kFlagAgg = 1u << 30;
@@ -51,7 +55,7 @@ struct TableDesc {
     int32_t vecs;       // column blocks of 32 vectors per row (vector path, 1..4)
     int32_t warp_begin; // first warp of this table in the forward warp map
     int32_t cls;        // backward class: dtype * NUM_SHAPES + row shape code
-    int32_t cslot;      // index of the table's backward class among the handle's classes
+    int32_t pad_;
 };
 
 // Device-resident descriptor block owned by a handle.
@@ -139,44 +143,71 @@ __device__ __forceinline__ void st_volatile_u32(uint32_t* p, uint32_t v) {
     asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Decoupled look-back for one running count: publishes this tile's aggregate,
-// walks back over earlier tiles until one with an inclusive prefix, then
-// publishes this tile's inclusive prefix.  Returns the exclusive prefix.
-// Four predecessors are read per round trip.  Every earlier tile was claimed
-// (atomic tile counter) by a CTA that is already resident and publishes its
-// aggregate without waiting, so each wait ends; the spin is still bounded
-// and raises ERR_TIMEOUT if it runs out.
-__device__ __forceinline__ uint32_t lookback(uint32_t* status, int tile, uint32_t stride,
-                                             uint32_t aggregate, uint32_t* err) {
+// Decoupled look-back for D running counts of one thread (counts d0 ..
+// d0+D-1 of a tile's status row): publishes this tile's aggregates, walks
+// back over earlier tiles until one with an inclusive prefix, then publishes
+// this tile's inclusive prefixes; excl receives the exclusive prefixes.
+// Eight status words (8/D predecessors per count) are read per round trip.  Every earlier tile
+// was claimed (atomic tile counter) by a CTA that is already resident and
+// publishes its aggregates without waiting, so each wait ends; the spin is
+// still bounded and raises ERR_TIMEOUT if it runs out.
+constexpr int kLookbackWidth = 8;
+
+template <int D>
+__device__ __forceinline__ void lookback(uint32_t* status, int tile, uint32_t stride, int d0,
+                                         const uint32_t (&aggregate)[D], uint32_t (&excl)[D], uint32_t* err) {
+    uint32_t* row = status + (size_t)tile * stride + d0;
+#pragma unroll
+    for (int i = 0; i < D; ++i) excl[i] = 0;
     if (tile == 0) {
-        st_volatile_u32(status, kFlagPrefix | aggregate);
-        return 0;
+#pragma unroll
+        for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagPrefix | aggregate[i]);
+        return;
     }
-    st_volatile_u32(status + (size_t)tile * stride, kFlagAgg | aggregate);
-    uint32_t excl = 0;
-    int j = tile - 1;
+#pragma unroll
+    for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagAgg | aggregate[i]);
+    int j[D];
+    bool done[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        j[i] = tile - 1;
+        done[i] = false;
+    }
+    constexpr int W = kLookbackWidth / D;  // predecessors per count per round trip
     int spins = 0;
-    while (j >= 0) {
-        uint32_t sv[4];
+    for (;;) {
+        uint32_t sv[D][W];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sv[k] = j - k >= 0 ? ld_volatile_u32(status + (size_t)(j - k) * stride) : 0u;
-        int used = 0;
-        bool done = false, stall = false;
+        for (int i = 0; i < D; ++i)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (done || stall) continue;
-            const uint32_t f = sv[k] & ~kCountMask;
-            if (f == 0) {
-                stall = true;
-                continue;
+            for (int k = 0; k < W; ++k)
+                sv[i][k] = (!done[i] && j[i] - k >= 0)
+                               ? ld_volatile_u32(status + (size_t)(j[i] - k) * stride + d0 + i)
+                               : 0u;
+        bool all_done = true, any_stall = false;
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            if (done[i]) continue;
+            int used = 0;
+            bool stall = false;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (done[i] || stall) continue;
+                const uint32_t f = sv[i][k] & ~kCountMask;
+                if (f == 0) {
+                    stall = true;
+                    continue;
+                }
+                excl[i] += sv[i][k] & kCountMask;
+                ++used;
+                if (f == kFlagPrefix) done[i] = true;
             }
-            excl += sv[k] & kCountMask;
-            ++used;
-            if (f == kFlagPrefix) done = true;
+            j[i] -= used;
+            all_done = all_done && done[i];
+            any_stall = any_stall || (stall && !done[i]);
         }
-        if (done) break;
-        j -= used;
-        if (stall) {
+        if (all_done) break;
+        if (any_stall) {
             if (++spins > kSpinLimit) {
                 atomicOr(err, ERR_TIMEOUT);
                 break;
@@ -184,8 +215,8 @@ __device__ __forceinline__ uint32_t lookback(uint32_t* status, int tile, uint32_
             __nanosleep(100);
         }
     }
-    st_volatile_u32(status + (size_t)tile * stride, kFlagPrefix | ((excl + aggregate) & kCountMask));
-    return excl;
+#pragma unroll
+    for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagPrefix | ((excl[i] + aggregate[i]) & kCountMask));
 }
 
 // The same for one count per tile (stride 1), done by a whole warp: the
@@ -261,36 +292,38 @@ cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_
 
 struct Workspace {
     uint32_t* counters;   // [64]
-    uint32_t* hist;       // [kMaxPasses][kRadix]
-    uint32_t* status;     // [kMaxPasses][tiles][kRadix]
+    uint32_t* hist;       // [kMaxPasses][kMaxRadix]
+    uint32_t* status;     // [passes][tiles][1 << digit_bits]
     uint32_t* rle_status; // [tiles]
+    uint32_t* tile_bag;   // [tiles]: first bag of each key tile (zeroed per call)
     uint32_t* keys[2];    // [N] ping-pong
     uint32_t* vals[2];    // [N] ping-pong
     uint32_t* bag;        // [N] flat bag of each position
     float* scale;         // [N] s_i of each position (weights and/or mean)
     uint32_t* uniq;       // [N]
     uint32_t* runstart;   // [N+1]
-    uint32_t* long_runs;  // [max_long][4]: unique index, first chunk, chunk count, chunks done
-    uint2* cls_chunks;    // [classes][max_chunks]: (long-run index, chunk within the run) per class
+    uint2* chunk_info;    // [max_chunks]: (distinct-key index u of the run, first chunk of the run)
+    uint32_t* chunk_done; // [max_chunks]: chunks of the run finished, kept at the run's first chunk
+    uint32_t* cstart;     // [T+1]: first chunk of each table's long runs (cstart[T]: total)
+    uint32_t* run_status; // [tiles]: look-back status of the chunk scan (zeroed per call)
     uint32_t* ustart;     // [T+1]: first distinct-key index of each table (ustart[T]: end)
     float* partial;       // [max_chunks][part_stride]
-    int64_t max_long;
     int64_t max_chunks;
     int tiles;
     int passes;
+    int digit_bits;       // 8 or 9
     int sorted_buf;       // which ping-pong buffer holds the sorted result
 };
 
 // Counter slots inside Workspace::counters.
 enum : int {
     CTR_U = 0,          // number of distinct keys
-    CTR_NLONG = 1,      // number of long runs
+    CTR_RUN_TILE = 1,   // tile claim counter of the chunk scan
     CTR_NCHUNK = 2,     // number of chunks of long runs
     CTR_RLE_TILE = 3,   // tile claim counter of the run-length kernel
     CTR_PASS_TILE = 4,  // tile claim counters of the sort passes [4]
     CTR_WORK = 8,       // apply work-item counters, one per backward class [15]
     CTR_EXIT = 24,      // apply finished-warp counters, one per backward class [15]
-    CTR_CLS_CHUNK = 40, // chunks registered per backward class slot [15]
     CTR_HAS_SCALE = 63, // nonzero when prepare wrote the per-lookup scale array
     CTR_COUNT = 64,
 };
@@ -308,6 +341,7 @@ struct PrepArgs {
     int mean;
     uint32_t total_rows;  // sentinel key for skipped lookups
     int key_bits;
+    int digit_bits;  // radix digit width (8 or 9)
 };
 
 // Backward row-shape codes: dim 32, 64, 128, 256 with aligned rows and
@@ -338,7 +372,6 @@ struct ApplyArgs {
     const int32_t* class_tables;  // tables of the launched class (device)
     int class_count;
     int cls;
-    int cslot;  // the class's slot in the per-class chunk lists
 };
 
 // Streams the backward class kernels are spread over: each class kernel
@@ -347,11 +380,11 @@ struct ApplyArgs {
 constexpr int kApplyStreams = 4;
 
 // One launch per backward class present: class_tables lists the tables of
-// every class (device, grouped by class); class_begin/class_count index it
-// and class_slot gives each class's per-class chunk list.  With more than one
-// class, the launches fork from s onto the given streams and s waits for all.
+// every class (device, grouped by class); class_begin/class_count index it.
+// With more than one class, the launches fork from s onto the given streams
+// and s waits for all.
 cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, const int* class_slot, cudaStream_t s,
+                         const int* class_begin, const int* class_count, cudaStream_t s,
                          const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join);
 
 }  // namespace tbe
