@@ -99,7 +99,7 @@ int next_pow2(int x) {
 int part_stride(const tbe_handle* h) { return (h->max_dim + 3) / 4 * 4; }
 
 struct Layout {
-    size_t counters, hist, status, rle_status, run_status, tile_bag, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
+    size_t counters, hist, tile_bag, tcount, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
         chunk_info, chunk_done, cstart, ustart, partial, total;
     size_t zero_bytes;  // counters..tile_bag are zeroed per call
     int64_t max_chunks;
@@ -119,11 +119,9 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     };
     L.counters = take(sizeof(uint32_t) * CTR_COUNT);
     L.hist = take(sizeof(uint32_t) * kMaxPasses * kMaxRadix);
-    L.status = take(sizeof(uint32_t) * (size_t)h->passes * std::max(L.tiles, 1) * ((size_t)1 << h->digit_bits));
-    L.rle_status = take(sizeof(uint32_t) * std::max(L.tiles, 1));
-    L.run_status = take(sizeof(uint32_t) * std::max(L.tiles, 1));
     L.tile_bag = take(sizeof(uint32_t) * std::max(L.tiles, 1));
     L.zero_bytes = o;
+    L.tcount = take(sizeof(uint32_t) * std::max(L.tiles, 1) * ((size_t)1 << h->digit_bits));
     L.keys0 = take(sizeof(uint32_t) * n);
     L.keys1 = take(sizeof(uint32_t) * n);
     L.vals0 = take(sizeof(uint32_t) * n);
@@ -150,8 +148,7 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     Workspace w{};
     w.counters = reinterpret_cast<uint32_t*>(p + L.counters);
     w.hist = reinterpret_cast<uint32_t*>(p + L.hist);
-    w.status = reinterpret_cast<uint32_t*>(p + L.status);
-    w.rle_status = reinterpret_cast<uint32_t*>(p + L.rle_status);
+    w.tcount = reinterpret_cast<uint32_t*>(p + L.tcount);
     w.tile_bag = reinterpret_cast<uint32_t*>(p + L.tile_bag);
     w.keys[0] = reinterpret_cast<uint32_t*>(p + L.keys0);
     w.keys[1] = reinterpret_cast<uint32_t*>(p + L.keys1);
@@ -164,7 +161,6 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.chunk_info = reinterpret_cast<uint2*>(p + L.chunk_info);
     w.chunk_done = reinterpret_cast<uint32_t*>(p + L.chunk_done);
     w.cstart = reinterpret_cast<uint32_t*>(p + L.cstart);
-    w.run_status = reinterpret_cast<uint32_t*>(p + L.run_status);
     w.ustart = reinterpret_cast<uint32_t*>(p + L.ustart);
     w.partial = reinterpret_cast<float*>(p + L.partial);
     w.max_chunks = L.max_chunks;

@@ -8,18 +8,18 @@
 //     weights or mean pooling apply, and the digit histograms of every radix
 //     pass.  Positions are tiled evenly (the first bag of each tile is marked
 //     by a pass over the bags), so bag lengths do not unbalance the work.
-//  2. onesweep_kernel, once per 8-bit digit: a stable LSD radix pass.  Each
-//     CTA claims the next tile, ranks its keys by digit (warp match + per-warp
-//     counters, in input order), learns the counts of all earlier tiles by a
-//     bounded decoupled look-back, and scatters through shared memory so each
-//     digit's run is written contiguously.  The first pass generates the
-//     values (positions) instead of reading them.
-//  3. rle_kernel: head flags of the sorted keys, a tile scan with look-back,
-//     the distinct keys with their first sorted slot (runstart[U] = N) and
-//     the first distinct key of each table.
-//  4. chunk_scan_kernel: numbers the 256-lookup chunks of every run of at
-//     least kLongRun lookups in key order (a scan over the distinct keys), so
-//     each table's chunks form one consecutive range for the apply step.
+//  2. a stable LSD radix sort of (key, position), 8- or 9-bit digits,
+//     reduce-then-scan per pass: per-tile digit counts (the keys kernel gives
+//     the first pass's), a scan per digit over the tiles, and a scatter that
+//     ranks each tile's keys by digit (ballot match + per-warp counters, in
+//     input order) and writes each digit's run contiguously.
+//  3. run-length encoding, reduce-then-scan: runs per tile
+//     (rle_count_kernel), a scan over the tiles, then rle_kernel writes the
+//     distinct keys with their first sorted slot (runstart[U] = N) and the
+//     first distinct key of each table.
+//  4. chunk_count/chunk_write: number the 256-lookup chunks of every run of
+//     at least kLongRun lookups in key order (a scan over the distinct keys),
+//     so each table's chunks form one consecutive range for the apply step.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -54,6 +54,20 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_
     __syncthreads();  // s_warp may be reused by the caller
     *total = tot;
     return warp_excl + x - v;
+}
+
+// Lanes of the warp whose BITS-bit label equals this lane's, from one ballot
+// per label bit (labels of BITS bits; all lanes must call it).
+template <int BITS>
+__device__ __forceinline__ uint32_t match_label(uint32_t label) {
+    uint32_t peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < BITS; ++b) {
+        const bool bit = (label >> b) & 1u;
+        const uint32_t v = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? v : ~v;
+    }
+    return peers;
 }
 
 // ------------------------------------------------------------------ keys
@@ -121,46 +135,25 @@ __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws
     if (err) atomicOr(&a.blk->error, err);
 }
 
-// Asynchronous global -> shared copy of one element (4 or 8 bytes), and the
-// wait for all of a thread's copies.
-template <int BYTES>
-__device__ __forceinline__ void cp_async(void* smem, const void* gmem) {
-    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sa), "l"(gmem), "n"(BYTES) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Dynamic shared memory of keys_kernel: the tile's indices and weights
-// (copied asynchronously while the bag map is built), the staged offsets and
-// the bag marks.
+// One key per position, tile by tile.  The tile's bags [bf, bl] come from
+// the marks (the last tile finds its last bag with a block-wide search);
+// their offsets are staged in shared memory and every position learns its bag
+// from the bag starts: each non-empty bag marks its first position in the
+// tile, and a position's bag is the last mark at or before it (per 32
+// positions a ballot of the marks, the highest marked lane at or below each
+// lane, and a carry from the previous 32).  Warp w takes positions
+// w*512 + k*32 + lane (k < 16), so loads and stores are coalesced.  The first
+// radix pass's digit counts are kept per tile (for the sort's scan), and the
+// digit histograms of all passes per block, added to the global histograms
+// at the end; equal top digits of a warp (few distinct values) are added
+// once (lanes with equal digits found by ballots).
 template <typename IDX>
-constexpr size_t keys_smem_bytes(bool weights) {
-    return sizeof(IDX) * kSortTile + (weights ? sizeof(float) * kSortTile : 0) + sizeof(int32_t) * (kKeysWindow + 3) +
-           sizeof(int16_t) * kSortTile;
-}
-
-// One key per position, tile by tile.  The tile's indices and weights are
-// copied to shared memory asynchronously first, so their DRAM latency
-// overlaps the rest of the set-up.  The tile's bags [bf, bl] come from the
-// marks (the last tile finds its last bag with a block-wide search); their
-// offsets are staged in shared memory and every position learns its bag from
-// a position -> bag map: each non-empty bag marks its first position in the
-// tile, and an inclusive max-scan over the tile's positions carries each
-// mark forward to the bag's last position.  Warp w takes positions
-// w*512 + k*32 + lane (k < 16), so global stores are coalesced and the scan
-// runs in registers with shuffles.  The digit histograms of all radix passes
-// are counted per block (equal digits of a warp added once, by warp match)
-// and added to the global histograms at the end.
-template <typename IDX>
-__global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
-    extern __shared__ __align__(16) unsigned char keys_smem[];
-    IDX* s_x = reinterpret_cast<IDX*>(keys_smem);
-    float* s_w = reinterpret_cast<float*>(keys_smem + sizeof(IDX) * kSortTile);
-    int32_t* s_off = reinterpret_cast<int32_t*>(keys_smem + sizeof(IDX) * kSortTile +
-                                                (a.weights ? sizeof(float) * kSortTile : 0));
-    int16_t* s_mark = reinterpret_cast<int16_t*>(s_off + kKeysWindow + 3);  // window index of the bag starting here
+__global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) {
+    __shared__ int32_t s_off[kKeysWindow + 3];  // offsets bf .. bl+1 (N < 2^30)
+    __shared__ int16_t s_mark[kSortTile];       // window index of the bag starting at each position
     __shared__ uint32_t s_hist[kMaxPasses][kMaxRadix];
-    __shared__ int32_t s_wmax[kSortThreads / 32];
+    __shared__ uint32_t s_tc[kMaxRadix];  // first-pass digit counts of the current tile
+    __shared__ int32_t s_wlast[kSortThreads / 32];
     __shared__ int64_t s_last;
     const IDX* off = reinterpret_cast<const IDX*>(a.offsets);
     const IDX* ind = reinterpret_cast<const IDX*>(a.indices);
@@ -173,6 +166,7 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
     uint32_t err = 0;
 
     for (int i = threadIdx.x; i < kMaxPasses * kMaxRadix; i += blockDim.x) (&s_hist[0][0])[i] = 0;
+    for (int i = threadIdx.x; i < kMaxRadix; i += blockDim.x) s_tc[i] = 0;
 
     const int64_t tiles = (a.N + kSortTile - 1) / kSortTile;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -180,10 +174,6 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
         const int64_t p1 = min(p0 + (int64_t)kSortTile, a.N);
         const int n = (int)(p1 - p0);
         __syncthreads();  // the previous tile is done with the shared arrays
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            cp_async<sizeof(IDX)>(s_x + i, ind + p0 + i);
-            if (a.weights) cp_async<4>(s_w + i, a.weights + p0 + i);
-        }
         const int64_t bf = tmin<int64_t>((int64_t)__ldg(ws.tile_bag + tile), nbags - 1);
         int64_t bl;
         if (tile + 1 < tiles) {
@@ -196,7 +186,22 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
         }
         const int64_t nwin = bl - bf + 2;  // offsets bf .. bl+1
         const bool staged = nwin <= kKeysWindow;
-        int bj[kSortItems];  // window index of each item's bag (staged tiles)
+        // the tile's indices and weights, loaded before the bag map is built
+        IDX xv[kSortItems];
+        float wv[kSortItems];
+#pragma unroll
+        for (int k = 0; k < kSortItems; ++k) {
+            const int li = warp * (32 * kSortItems) + k * 32 + lane;
+            xv[k] = li < n ? ind[p0 + li] : (IDX)0;
+            wv[k] = (a.weights && li < n) ? __ldg(a.weights + p0 + li) : 1.f;
+        }
+        // window index of each item's bag (staged tiles), two per register
+        uint32_t bj2[kSortItems / 2];
+        auto bj_get = [&](int q) -> int { return (int)((bj2[q >> 1] >> (16 * (q & 1))) & 0xffffu); };
+        auto bj_set = [&](int q, int v) {
+            const uint32_t h = (uint32_t)v & 0xffffu;
+            bj2[q >> 1] = (q & 1) ? ((bj2[q >> 1] & 0x0000ffffu) | (h << 16)) : ((bj2[q >> 1] & 0xffff0000u) | h);
+        };
         if (staged) {
             for (int64_t k = threadIdx.x; k < nwin; k += blockDim.x)
                 s_off[k] = (int32_t)tmin<int64_t>(tmax<int64_t>(ld_index(off, bf + k), 0), Nc);
@@ -210,79 +215,112 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
                 if (st < s_off[j + 1] && st >= p0 && st < p1) s_mark[st - p0] = (int16_t)j;
             }
             __syncthreads();
-            // inclusive max-scan: per warp over its 512 positions, then across warps
+            // last mark at or before each position, per warp over its 512
             int carry = -1;
 #pragma unroll
             for (int k = 0; k < kSortItems; ++k) {
-                int v = s_mark[warp * (32 * kSortItems) + k * 32 + lane];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v = max(v, y);
-                }
-                v = max(v, carry);
-                carry = __shfl_sync(0xffffffffu, v, 31);
-                bj[k] = v;
+                const int m = s_mark[warp * (32 * kSortItems) + k * 32 + lane];
+                const uint32_t marked = __ballot_sync(0xffffffffu, m >= 0);
+                const uint32_t upto = marked & (0xffffffffu >> (31 - lane));
+                const int v = __shfl_sync(0xffffffffu, m, upto ? 31 - __clz(upto) : 0);
+                bj_set(k, upto ? v : carry);  // -1 (no mark yet) is kept as 0xffff
+                const int top = __shfl_sync(0xffffffffu, m, marked ? 31 - __clz(marked) : 0);
+                carry = marked ? top : carry;
             }
-            if (lane == 0) s_wmax[warp] = carry;
-        }
-        cp_async_wait_all();
-        __syncthreads();  // marks, warp maxima and every thread's copies are visible
-        if (staged) {
+            if (lane == 0) s_wlast[warp] = carry;
+            __syncthreads();
             int pre = 0;  // positions before the first mark belong to bag bf (index 0)
-            for (int w = 0; w < warp; ++w) pre = max(pre, s_wmax[w]);
+            for (int w = warp - 1; w >= 0; --w)
+                if (s_wlast[w] >= 0) {
+                    pre = s_wlast[w];
+                    break;
+                }
 #pragma unroll
-            for (int k = 0; k < kSortItems; ++k) bj[k] = tmin<int>(max(bj[k], pre), (int)nwin - 2);
+            for (int k = 0; k < kSortItems; ++k) {
+                const int b = bj_get(k);
+                bj_set(k, tmin<int>(b == 0xffff ? pre : b, (int)nwin - 2));
+            }
         }
-        uint32_t keyv[kSortItems];
+        // table of each bag: the window starts in table tf (whose descriptor
+        // is read once per tile); a bag past it walks forward (rare).  Sizes
+        // fit 32 bits: N < 2^30, T*B < 2^31, sum of rows < 2^32.
+        const uint32_t B32 = (uint32_t)a.B;
+        const uint32_t bf32 = (uint32_t)bf;
+        const int tf = (int)(bf32 / B32);
+        const uint32_t tf_end = (uint32_t)(tf + 1) * B32;  // first bag of the next table
+        const uint32_t rows_f = (uint32_t)a.tabs[tf].rows;
+        const uint32_t rowbase_f = (uint32_t)a.tabs[tf].rowbase;
+        const uint32_t p032 = (uint32_t)p0;
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k) {
             const int li = warp * (32 * kSortItems) + k * 32 + lane;
-            const int64_t p = p0 + li;
-            keyv[k] = 0xffffffffu;
-            if (li < n) {
-                int64_t bag, bstart, bend;
+            const bool valid = li < n;
+            uint32_t keyk = 0xffffffffu;
+            if (valid) {
+                const uint32_t p = p032 + (uint32_t)li;
+                uint32_t bag;
+                int32_t L;
                 if (staged) {
-                    const int j = bj[k];
-                    bag = bf + j;
-                    bstart = s_off[j];
-                    bend = s_off[j + 1];
+                    const int j = bj_get(k);
+                    bag = bf32 + (uint32_t)j;
+                    L = s_off[j + 1] - s_off[j];
                 } else {
-                    bag = upper_bound_global(off, bf, min(bl + 2, nbags + 1), p) - 1;
-                    bag = tmax<int64_t>(tmin<int64_t>(bag, nbags - 1), 0);
-                    bstart = ld_index(off, bag);
-                    bend = ld_index(off, bag + 1);
+                    int64_t b = upper_bound_global(off, bf, min(bl + 2, nbags + 1), (int64_t)p) - 1;
+                    b = tmax<int64_t>(tmin<int64_t>(b, nbags - 1), 0);
+                    bag = (uint32_t)b;
+                    L = (int32_t)(ld_index(off, b + 1) - ld_index(off, b));
                 }
-                const int t = (int)((uint32_t)bag / (uint32_t)a.B);  // T*B < 2^31
-                const int64_t rows = a.tabs[t].rows;
-                const int64_t x = (int64_t)s_x[li];
+                uint32_t rows = rows_f, rowbase = rowbase_f;
+                if (bag >= tf_end) {
+                    int t = tf + 1;
+                    for (uint32_t tb = tf_end + B32; bag >= tb && t < a.T - 1; tb += B32) ++t;
+                    rows = (uint32_t)a.tabs[t].rows;
+                    rowbase = (uint32_t)a.tabs[t].rowbase;
+                }
+                // an index outside [0, rows) (negative ones included) is skipped
                 uint32_t key = a.total_rows;
-                if (x >= 0 && x < rows)
-                    key = (uint32_t)(a.tabs[t].rowbase + x);
+                if ((uint64_t)(int64_t)xv[k] < (uint64_t)rows)
+                    key = rowbase + (uint32_t)xv[k];
                 else
                     err |= ERR_OOB;
-                keyv[k] = key;
+                keyk = key;
                 ws.keys[0][p] = key;
-                ws.bag[p] = (uint32_t)bag;
+                ws.bag[p] = bag;
                 if (ws.scale) {
-                    float sc = a.weights ? s_w[li] : 1.f;
-                    const int64_t L = bend - bstart;
+                    float sc = wv[k];
                     if (a.mean && L > 0) sc = __fdiv_rn(sc, (float)L);
                     ws.scale[p] = sc;
                 }
             }
-        }
-        // digit counts: per pass, the lowest lane of each group of equal
-        // digits adds the group's size (the high digits take few values, so
-        // lane-by-lane atomics would serialize on one counter)
-#pragma unroll
-        for (int k = 0; k < kSortItems; ++k) {
-            const bool valid = warp * (32 * kSortItems) + k * 32 + lane < n;
+            // digit counts; the top pass's digits take few values within a
+            // warp, so equal ones are added once
             for (int q = 0; q < passes; ++q) {
-                const uint32_t d = valid ? (keyv[k] >> (q * dbits)) & dmask : 0xffffffffu;
-                const uint32_t peers = __match_any_sync(0xffffffffu, d);
-                if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&s_hist[q][d], (uint32_t)__popc(peers));
+                const uint32_t d = (keyk >> (q * dbits)) & dmask;
+                uint32_t* c = q == 0 ? &s_tc[d] : &s_hist[q][d];
+                if (q == passes - 1) {
+                    const uint32_t lab = valid ? d : (uint32_t)kMaxRadix;
+                    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                    const uint32_t d_first = __shfl_sync(0xffffffffu, lab, vmask ? __ffs(vmask) - 1 : 0);
+                    if (__all_sync(0xffffffffu, !valid || lab == d_first)) {
+                        // one digit for the whole warp (a table narrower than the digit)
+                        if (vmask && lane == __ffs(vmask) - 1) atomicAdd(c, (uint32_t)__popc(vmask));
+                    } else {
+                        const uint32_t peers = match_label<kMaxRadixBits + 1>(lab);
+                        if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(c, (uint32_t)__popc(peers));
+                    }
+                } else if (valid) {
+                    atomicAdd(c, 1u);
+                }
             }
+        }
+        // the tile's first-pass digit counts: to the sort's count table and
+        // the block's first-pass histogram
+        __syncthreads();
+        for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x) {
+            const uint32_t c = s_tc[d];
+            ws.tcount[(size_t)d * tiles + tile] = c;
+            s_hist[0][d] += c;
+            s_tc[d] = 0;
         }
     }
     __syncthreads();
@@ -293,35 +331,115 @@ __global__ void __launch_bounds__(256) keys_kernel(PrepArgs a, Workspace ws) {
     if (err) atomicOr(&a.blk->error, err);
 }
 
-// One wave of keys_kernel CTAs (as many as fit per SM with this shared memory).
-template <typename IDX>
-static cudaError_t launch_keys(const PrepArgs& a, Workspace& ws, int64_t tiles, int sms, cudaStream_t s) {
-    const bool w = a.weights != nullptr;
-    const size_t smem = keys_smem_bytes<IDX>(w);
-    static int per_sm[2] = {0, 0};  // resident CTAs per SM, without / with weights
-    if (per_sm[w] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(keys_kernel<IDX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)keys_smem_bytes<IDX>(true));
-        int n = 0;
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, keys_kernel<IDX>, 256, smem);
-        if (e != cudaSuccess) return e;
-        per_sm[w] = n > 0 ? n : 1;
+// --------------------------------------------------------- one radix pass
+//
+// Reduce-then-scan: the digit counts of every tile (tcount[d][tile], digit
+// major) come from the keys kernel for the first pass and from
+// upsweep_kernel for later ones; scan_kernel turns each digit's row into the
+// global start of that digit's keys from each tile; downsweep_kernel ranks
+// each tile's keys by digit and scatters them.  Nothing waits on another
+// tile, so the time per tile does not grow with the number of tiles in
+// flight.
+
+// Digit counts of one tile of keys (one CTA per tile).
+template <int RB>
+__global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* __restrict__ keys, uint32_t N,
+                                                               int shift, uint32_t* __restrict__ tcount,
+                                                               uint32_t tiles) {
+    constexpr int RADIX = 1 << RB;
+    __shared__ uint32_t s_c[RADIX];
+    const int tid = threadIdx.x;
+    for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = 0;
+    __syncthreads();
+    const uint32_t base = blockIdx.x * kSortTile;
+    uint32_t key[kSortItems];
+#pragma unroll
+    for (int k = 0; k < kSortItems; ++k) {
+        const uint32_t idx = base + k * kSortThreads + tid;
+        key[k] = idx < N ? __ldg(keys + idx) : 0u;
     }
-    const unsigned grid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * per_sm[w]);
-    keys_kernel<IDX><<<grid, 256, smem, s>>>(a, ws);
-    return cudaGetLastError();
+#pragma unroll
+    for (int k = 0; k < kSortItems; ++k)
+        if (base + k * kSortThreads + tid < N) atomicAdd(&s_c[(key[k] >> shift) & (RADIX - 1)], 1u);
+    __syncthreads();
+    for (int d = tid; d < RADIX; d += kSortThreads) tcount[(size_t)d * tiles + blockIdx.x] = s_c[d];
 }
 
-// --------------------------------------------------------- one radix pass
+// Exclusive scan of n counts in place by one 1024-thread block, each thread
+// taking a contiguous chunk (one block-wide scan in all), plus `start`;
+// returns the total on every thread.
+__device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
+                                                        uint32_t* s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t chunk = (n + 1023) / 1024;
+    const uint32_t i0 = tid * chunk, i1 = tmin<uint32_t>(i0 + chunk, n);
+    uint32_t sum = 0;
+    for (uint32_t i = i0; i < i1; ++i) sum += row[i];
+    uint32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    for (int w = 0; w < 32; ++w) {
+        const uint32_t c = s_warp[w];
+        if (w < warp) before += c;
+        total += c;
+    }
+    uint32_t run = start + before + x - sum;
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint32_t c = row[i];
+        row[i] = run;
+        run += c;
+    }
+    return start + total;
+}
 
+// Exclusive scan of one digit's row of tile counts (one CTA per digit),
+// offset by the number of keys with a smaller digit: the global start of the
+// digit's keys from each tile, in place.
+template <int RB>
+__global__ void __launch_bounds__(1024) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
+                                                    uint32_t tiles) {
+    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_start;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = blockIdx.x;
+    // keys with a smaller digit
+    {
+        uint32_t v = 0;
+        for (int e = tid; e < d; e += 1024) v += __ldg(hist + e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_warp[warp] = v;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t t = 0;
+            for (int w = 0; w < 32; ++w) t += s_warp[w];
+            s_start = t;
+        }
+        __syncthreads();
+    }
+    const uint32_t start = s_start;
+    __syncthreads();  // s_warp is reused below
+    block_scan_row_1024(tcount + (size_t)d * tiles, tiles, start, s_warp);
+}
+
+// Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
+// input order (ballot match + per-warp counters), places them by digit in
+// shared memory and writes each digit's run to its global start from the
+// scan.  The first pass generates the values (positions) instead of
+// reading them.
 template <bool FIRST, int RB>
-__global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(const uint32_t* __restrict__ keys_in,
-                                                                   const uint32_t* __restrict__ vals_in,
-                                                                   uint32_t* __restrict__ keys_out,
-                                                                   uint32_t* __restrict__ vals_out,
-                                                                   const uint32_t* __restrict__ hist,
-                                                                   uint32_t* status, uint32_t* tile_ctr,
-                                                                   uint32_t N, int shift, uint32_t* err) {
+__global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32_t* __restrict__ keys_in,
+                                                                    const uint32_t* __restrict__ vals_in,
+                                                                    uint32_t* __restrict__ keys_out,
+                                                                    uint32_t* __restrict__ vals_out,
+                                                                    const uint32_t* __restrict__ tstart_g,
+                                                                    uint32_t tiles, uint32_t N, int shift) {
     constexpr int RADIX = 1 << RB;
     constexpr int DPT = RADIX / kSortThreads;  // digits per thread (consecutive)
     static_assert(DPT >= 1 && DPT * kSortThreads == RADIX, "digits must split evenly over the threads");
@@ -332,37 +450,20 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(const uint32_
     __shared__ uint32_t s_tile_start[RADIX];
     __shared__ uint32_t s_global[RADIX];
     __shared__ uint32_t s_scan[8];
-    __shared__ uint32_t s_tile;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d0 = tid * DPT;  // this thread's digits
-    if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+    const uint32_t tile = blockIdx.x;
+    const uint32_t base = tile * kSortTile;
     for (int i = tid; i < (kSortThreads / 32) * RADIX; i += kSortThreads) (&s_whist[0][0])[i] = 0;
-    // global start of each digit bin
-    uint32_t bin_start[DPT];
-    {
-        uint32_t hsum = 0;
+    // global start of this thread's digits from this tile (used after ranking)
+    uint32_t gstart[DPT];
 #pragma unroll
-        for (int i = 0; i < DPT; ++i) {
-            bin_start[i] = hist[d0 + i];
-            hsum += bin_start[i];
-        }
-        uint32_t tot;
-        uint32_t ex = block_exclusive_scan_256(hsum, s_scan, &tot);
-#pragma unroll
-        for (int i = 0; i < DPT; ++i) {
-            const uint32_t c = bin_start[i];
-            bin_start[i] = ex;
-            ex += c;
-        }
-    }
+    for (int i = 0; i < DPT; ++i) gstart[i] = __ldg(tstart_g + (size_t)(d0 + i) * tiles + tile);
     __syncthreads();
-    const int tile = (int)s_tile;
-    const uint32_t base = (uint32_t)tile * kSortTile;
 
-    // keys in registers; values stay in memory until the final write, which
-    // gathers them from this tile's input through the item's source index
-    uint32_t key[kSortItems], rank[kSortItems];
+    // ranks inside the warp are below 512: two per register
+    uint32_t key[kSortItems], rank2[kSortItems / 2];
     const uint32_t wbase = base + warp * (32 * kSortItems) + lane;
 #pragma unroll
     for (int k = 0; k < kSortItems; ++k) {
@@ -378,17 +479,22 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(const uint32_
 #pragma unroll
     for (int k = 0; k < kSortItems; ++k) {
         const int d = digit_of(k);
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const uint32_t peers = match_label<RB + 1>((uint32_t)d);  // RADIX (past the end) is a label too
         uint32_t cnt = 0;
         if (d < RADIX) cnt = s_whist[warp][d];
-        rank[k] = cnt + __popc(peers & lt_mask);
+        const uint32_t r = cnt + __popc(peers & lt_mask);
+        if (k & 1)
+            rank2[k >> 1] |= r << 16;
+        else
+            rank2[k >> 1] = r;
         __syncwarp();
         if (d < RADIX && (peers & lt_mask) == 0) s_whist[warp][d] = (uint16_t)(cnt + __popc(peers));
         __syncwarp();
     }
     __syncthreads();
-    // per digit: warp-exclusive offsets, tile total, look-back, tile-local start
+    // per digit: warp-exclusive offsets, tile total, tile-local start
     uint32_t total[DPT];
+    uint32_t tsum = 0;
 #pragma unroll
     for (int i = 0; i < DPT; ++i) {
         total[i] = 0;
@@ -398,20 +504,16 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(const uint32_
             s_whist[w][d0 + i] = (uint16_t)total[i];
             total[i] += c;
         }
+        tsum += total[i];
     }
-    uint32_t prefix[DPT];
-    lookback<DPT>(status, tile, RADIX, d0, total, prefix, err);
     {
-        uint32_t tsum = 0;
-#pragma unroll
-        for (int i = 0; i < DPT; ++i) tsum += total[i];
         uint32_t tile_total;
-        uint32_t tstart = block_exclusive_scan_256(tsum, s_scan, &tile_total);
+        uint32_t ts = block_exclusive_scan_256(tsum, s_scan, &tile_total);
 #pragma unroll
         for (int i = 0; i < DPT; ++i) {
-            s_tile_start[d0 + i] = tstart;
-            s_global[d0 + i] = bin_start[i] + prefix[i] - tstart;
-            tstart += total[i];
+            s_tile_start[d0 + i] = ts;
+            s_global[d0 + i] = gstart[i] - ts;
+            ts += total[i];
         }
     }
     __syncthreads();
@@ -419,25 +521,31 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(const uint32_
     for (int k = 0; k < kSortItems; ++k) {
         const int d = digit_of(k);
         if (d < RADIX) {
-            const uint32_t lp = s_tile_start[d] + s_whist[warp][d] + rank[k];
+            const uint32_t lp = s_tile_start[d] + s_whist[warp][d] + ((rank2[k >> 1] >> (16 * (k & 1))) & 0xffffu);
             s_keys[lp] = key[k];
             s_src[lp] = wbase + k * 32 - base;
         }
     }
     __syncthreads();
-    // write out in sorted order; the value gathers of all items are issued
-    // together (fully unrolled) so their latencies overlap
+    // write out in sorted order (each digit's run is contiguous); the value
+    // gathers of all the thread's items are issued before any store
     const uint32_t nvalid = min((uint32_t)kSortTile, N - base);
+    uint32_t vv[kSortItems];
+#pragma unroll
+    for (int k = 0; k < kSortItems; ++k) {
+        const uint32_t i = (uint32_t)(k * kSortThreads + tid);
+        const uint32_t src = i < nvalid ? base + s_src[i] : 0u;
+        vv[k] = FIRST ? src : (i < nvalid ? __ldg(vals_in + src) : 0u);
+    }
 #pragma unroll
     for (int k = 0; k < kSortItems; ++k) {
         const uint32_t i = (uint32_t)(k * kSortThreads + tid);
         if (i < nvalid) {
             const uint32_t kk = s_keys[i];
-            const uint32_t src = base + s_src[i];
             const uint32_t g = s_global[(kk >> shift) & (RADIX - 1)] + i;
             if (g < N) {
                 keys_out[g] = kk;
-                vals_out[g] = FIRST ? src : __ldg(vals_in + src);
+                vals_out[g] = vv[k];
             }
         }
     }
@@ -464,17 +572,10 @@ __device__ __forceinline__ int key_table(const PrepArgs& a, uint32_t key) {
 // look-back for the running count of distinct keys: uniq/runstart and
 // ustart[t], the first distinct-key index of every table (keys are sorted and
 // each table owns a consecutive key range), ustart[T] the end.
-__global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace ws, const uint32_t* __restrict__ skeys) {
-    __shared__ uint32_t s_scan[8];
-    __shared__ uint32_t s_tile, s_prefix;
-    const uint32_t N = (uint32_t)a.N;
-    uint32_t* err = &a.blk->error;
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0) s_tile = atomicAdd(&ws.counters[CTR_RLE_TILE], 1u);
-    __syncthreads();
-    const uint32_t tile = s_tile;
-    const uint32_t p0 = tile * kSortTile + tid * kSortItems;
-    uint32_t k[kSortItems];
+// A thread's kSortItems consecutive sorted keys (from p0) and their head
+// flags (bit q: position p0+q starts a run).
+__device__ __forceinline__ uint32_t rle_load_heads(const uint32_t* __restrict__ skeys, uint32_t N, uint32_t p0,
+                                                   uint32_t (&k)[kSortItems], uint32_t& prev) {
     if (p0 + kSortItems <= N) {
         const uint4* src = reinterpret_cast<const uint4*>(skeys + p0);
 #pragma unroll
@@ -489,7 +590,7 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
 #pragma unroll
         for (int q = 0; q < kSortItems; ++q) k[q] = p0 + q < N ? skeys[p0 + q] : 0u;
     }
-    const uint32_t prev = (p0 > 0 && p0 - 1 < N) ? skeys[p0 - 1] : 0u;
+    prev = (p0 > 0 && p0 - 1 < N) ? skeys[p0 - 1] : 0u;
     uint32_t heads = 0;
 #pragma unroll
     for (int q = 0; q < kSortItems; ++q) {
@@ -498,20 +599,50 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
         const bool h = p < N && (p == 0 || k[q] != before);
         heads |= (uint32_t)h << q;
     }
+    return heads;
+}
+
+// Number of runs starting in each tile of sorted keys (one CTA per tile).
+__global__ void __launch_bounds__(kSortThreads) rle_count_kernel(const uint32_t* __restrict__ skeys, uint32_t N,
+                                                                 uint32_t* __restrict__ tcount) {
+    __shared__ uint32_t s_scan[8];
+    uint32_t k[kSortItems], prev;
+    const uint32_t heads = rle_load_heads(skeys, N, blockIdx.x * kSortTile + threadIdx.x * kSortItems, k, prev);
+    uint32_t total;
+    block_exclusive_scan_256(__popc(heads), s_scan, &total);
+    if (threadIdx.x == 0) tcount[blockIdx.x] = total;
+}
+
+// Exclusive scan of n counts in place by one CTA of 1024 threads; the total
+// goes to *total_out.
+__global__ void __launch_bounds__(1024) tile_scan_kernel(uint32_t* __restrict__ cnt, uint32_t n,
+                                                         uint32_t* __restrict__ total_out) {
+    __shared__ uint32_t s_warp[32];
+    const uint32_t total = block_scan_row_1024(cnt, n, 0u, s_warp);
+    if (threadIdx.x == 0) *total_out = total;
+}
+
+// Run-length encoding of the sorted keys, one CTA per tile, the tile's first
+// distinct-key index from the scanned run counts: uniq/runstart (runstart[U]
+// = N) and ustart[t], the first distinct-key index of every table (keys are
+// sorted and each table owns a consecutive key range), ustart[T] the end.
+__global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace ws, const uint32_t* __restrict__ skeys) {
+    __shared__ uint32_t s_scan[8];
+    const uint32_t N = (uint32_t)a.N;
+    const int tid = threadIdx.x;
+    const uint32_t tile = blockIdx.x;
+    const uint32_t p0 = tile * kSortTile + tid * kSortItems;
+    uint32_t k[kSortItems], prev;
+    const uint32_t heads = rle_load_heads(skeys, N, p0, k, prev);
     uint32_t tile_total;
     const uint32_t excl = block_exclusive_scan_256(__popc(heads), s_scan, &tile_total);
-    if (tid < 32) {
-        const uint32_t pre = lookback_warp(ws.rle_status, (int)tile, tile_total, err, lane);
-        if (tid == 0) s_prefix = pre;
-    }
-    __syncthreads();
-    const uint32_t U = tmin<uint32_t>(s_prefix + tile_total, N);
-    uint32_t u = s_prefix + excl;
+    const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], N);
+    uint32_t u = ws.tcount[tile] + excl;
 #pragma unroll
     for (int q = 0; q < kSortItems; ++q) {
         if (!(heads & (1u << q))) continue;
         const uint32_t p = p0 + q, key = k[q];
-        if (u < N) {  // holds unless a look-back ran out (then ERR_TIMEOUT is set)
+        if (u < N) {
             ws.uniq[u] = key;
             ws.runstart[u] = p;
             // tables whose key range starts after the previous key and at or
@@ -526,73 +657,87 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
     if (N > 0 && p0 <= N - 1 && N - 1 < p0 + kSortItems) {
         const int tlast = key_table(a, skeys[N - 1]);
         for (int t2 = tlast + 1; t2 <= a.T; ++t2) ws.ustart[t2] = U;
-    }
-    if (tid == 0 && (uint64_t)(tile + 1) * kSortTile >= N) {
-        ws.counters[CTR_U] = U;
         ws.runstart[U] = N;
     }
 }
 
-// Chunks of the long runs, in key order, after the run-length kernel: a scan
-// over the distinct keys (tiles of kSortTile keys claimed in order, a
-// warp-parallel look-back) gives every run of at least kLongRun lookups its
-// first chunk g0, the number of chunks of all earlier runs.  The run's
-// ceil(len / kLongRun) chunks g0 .. get (u, g0) and the run's finished-chunk
-// count (kept at g0) is cleared.  cstart[t] is the first chunk of table t
-// (the chunk base at its first distinct key) and cstart[T] the total, so the
-// chunks of each table are one consecutive range in key order.  Persistent
-// CTAs claim tiles until the distinct keys are covered.
-__global__ void __launch_bounds__(kSortThreads) chunk_scan_kernel(PrepArgs a, Workspace ws) {
-    __shared__ uint32_t s_scan[8];
-    __shared__ uint32_t s_base[kSortTile];  // exclusive chunk base of each distinct key of the tile
-    __shared__ uint32_t s_tile, s_prefix;
+// Chunks of the long runs, numbered in key order after the run-length
+// encoding (count, scan, write over tiles of kSortTile distinct keys): every
+// run of at least kLongRun lookups gets its first chunk g0, the number of
+// chunks of all earlier runs; the run's ceil(len / kLongRun) chunks g0 ..
+// get (u, g0) and the run's finished-chunk count (kept at g0) is cleared.
+// cstart[t] is the first chunk of table t (the chunk base at its first
+// distinct key) and cstart[T] the total, so the chunks of each table are one
+// consecutive range in key order.
+
+// Chunk counts of the runs of a thread's kSortItems distinct keys from u0.
+__device__ __forceinline__ void run_chunks(const PrepArgs& a, const Workspace& ws, uint32_t U, uint32_t u0,
+                                           uint32_t (&nc)[kSortItems]) {
     const uint32_t N = (uint32_t)a.N;
-    const uint32_t U = tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_U], N);
-    const uint32_t utiles = (U + kSortTile - 1) / kSortTile;
-    uint32_t* err = &a.blk->error;
-    const int tid = threadIdx.x, lane = tid & 31;
-    for (;;) {
-        __syncthreads();  // the previous tile is done with the shared state
-        if (tid == 0) s_tile = atomicAdd(&ws.counters[CTR_RUN_TILE], 1u);
-        __syncthreads();
-        const uint32_t tile = s_tile;
-        if (tile >= utiles) break;
-        const uint32_t t0 = tile * kSortTile;
-        const uint32_t u0 = t0 + tid * kSortItems;
-        // run starts u0 .. u0 + kSortItems (runstart[U] = N)
-        uint32_t rs[kSortItems + 1];
-        if (u0 + kSortItems <= U) {
-            const uint4* src = reinterpret_cast<const uint4*>(ws.runstart + u0);
+    uint32_t rs[kSortItems + 1];
+    if (u0 + kSortItems <= U) {
+        const uint4* src = reinterpret_cast<const uint4*>(ws.runstart + u0);
 #pragma unroll
-            for (int q = 0; q < kSortItems / 4; ++q) {
-                const uint4 v = src[q];
-                rs[4 * q] = v.x;
-                rs[4 * q + 1] = v.y;
-                rs[4 * q + 2] = v.z;
-                rs[4 * q + 3] = v.w;
-            }
-            rs[kSortItems] = u0 + kSortItems < U ? ws.runstart[u0 + kSortItems] : N;
-        } else {
+        for (int q = 0; q < kSortItems / 4; ++q) {
+            const uint4 v = src[q];
+            rs[4 * q] = v.x;
+            rs[4 * q + 1] = v.y;
+            rs[4 * q + 2] = v.z;
+            rs[4 * q + 3] = v.w;
+        }
+        rs[kSortItems] = u0 + kSortItems < U ? ws.runstart[u0 + kSortItems] : N;
+    } else {
 #pragma unroll
-            for (int q = 0; q <= kSortItems; ++q) rs[q] = u0 + q < U ? ws.runstart[u0 + q] : N;
+        for (int q = 0; q <= kSortItems; ++q) rs[q] = u0 + q < U ? ws.runstart[u0 + q] : N;
+    }
+#pragma unroll
+    for (int q = 0; q < kSortItems; ++q) {
+        nc[q] = 0;
+        const uint32_t r0 = tmin<uint32_t>(rs[q], N), r1 = tmin<uint32_t>(rs[q + 1], N);
+        if (u0 + q < U && r1 > r0 && r1 - r0 >= (uint32_t)kLongRun && ws.uniq[u0 + q] < a.total_rows)
+            nc[q] = (r1 - r0 + kLongRun - 1) / kLongRun;
+    }
+}
+
+// Chunks per tile of distinct keys (tiles past the distinct keys count 0).
+__global__ void __launch_bounds__(kSortThreads) chunk_count_kernel(PrepArgs a, Workspace ws, uint32_t tiles) {
+    __shared__ uint32_t s_scan[8];
+    const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], (uint32_t)a.N);
+    for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        if (tile * kSortTile >= U) {
+            if (threadIdx.x == 0) ws.tcount[tile] = 0;
+            continue;
         }
         uint32_t nc[kSortItems], sum = 0;
+        run_chunks(a, ws, U, tile * kSortTile + threadIdx.x * kSortItems, nc);
 #pragma unroll
-        for (int q = 0; q < kSortItems; ++q) {
-            nc[q] = 0;
-            const uint32_t r0 = tmin<uint32_t>(rs[q], N), r1 = tmin<uint32_t>(rs[q + 1], N);
-            if (u0 + q < U && r1 > r0 && r1 - r0 >= (uint32_t)kLongRun && ws.uniq[u0 + q] < a.total_rows)
-                nc[q] = (r1 - r0 + kLongRun - 1) / kLongRun;
-            sum += nc[q];
-        }
+        for (int q = 0; q < kSortItems; ++q) sum += nc[q];
+        uint32_t total;
+        block_exclusive_scan_256(sum, s_scan, &total);
+        if (threadIdx.x == 0) ws.tcount[tile] = total;
+    }
+}
+
+// The chunk records and cstart, from the scanned chunk counts.
+__global__ void __launch_bounds__(kSortThreads) chunk_write_kernel(PrepArgs a, Workspace ws, uint32_t tiles) {
+    __shared__ uint32_t s_scan[8];
+    __shared__ uint32_t s_base[kSortTile];  // exclusive chunk base of each distinct key of the tile
+    const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], (uint32_t)a.N);
+    const uint32_t total = tmin<uint32_t>(ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
+    const int tid = threadIdx.x;
+    if (blockIdx.x == 0)  // tables that start at or after the last distinct key
+        for (int t = tid; t <= a.T; t += blockDim.x)
+            if (tmin<uint32_t>(ws.ustart[t], U) == U) ws.cstart[t] = total;
+    for (uint32_t tile = blockIdx.x; tile < tiles && tile * kSortTile < U; tile += gridDim.x) {
+        const uint32_t t0 = tile * kSortTile;
+        const uint32_t u0 = t0 + tid * kSortItems;
+        uint32_t nc[kSortItems], sum = 0;
+        run_chunks(a, ws, U, u0, nc);
+#pragma unroll
+        for (int q = 0; q < kSortItems; ++q) sum += nc[q];
         uint32_t tile_total;
         const uint32_t excl = block_exclusive_scan_256(sum, s_scan, &tile_total);
-        if (tid < 32) {
-            const uint32_t pre = lookback_warp(ws.run_status, (int)tile, tile_total, err, lane);
-            if (tid == 0) s_prefix = pre;
-        }
-        __syncthreads();
-        uint32_t base = s_prefix + excl;
+        uint32_t base = ws.tcount[tile] + excl;
 #pragma unroll
         for (int q = 0; q < kSortItems; ++q) {
             s_base[tid * kSortItems + q] = base;
@@ -604,16 +749,20 @@ __global__ void __launch_bounds__(kSortThreads) chunk_scan_kernel(PrepArgs a, Wo
         }
         __syncthreads();
         // first chunk of every table whose first distinct key is in this tile
-        const uint32_t total = s_prefix + tile_total;
         for (int t = tid; t <= a.T; t += blockDim.x) {
             const uint32_t us = tmin<uint32_t>(ws.ustart[t], U);
-            if (us >= t0 && us < tmin<uint32_t>(t0 + kSortTile, U))
-                ws.cstart[t] = s_base[us - t0];
-            else if (us == U && tile == utiles - 1)
-                ws.cstart[t] = total;
+            if (us >= t0 && us < tmin<uint32_t>(t0 + kSortTile, U)) ws.cstart[t] = s_base[us - t0];
         }
-        if (tid == 0 && tile == utiles - 1) ws.counters[CTR_NCHUNK] = total;
+        __syncthreads();  // s_base is reused by the next tile
     }
+}
+
+// One wave of keys_kernel CTAs (three per SM).
+template <typename IDX>
+static cudaError_t launch_keys(const PrepArgs& a, Workspace& ws, int64_t tiles, int sms, cudaStream_t s) {
+    const unsigned grid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 3);
+    keys_kernel<IDX><<<grid, 256, 0, s>>>(a, ws);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ launch
@@ -641,39 +790,42 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     int cur = 0;
     const int radix = 1 << ws.digit_bits;
     for (int p = 0; p < ws.passes; ++p) {
-        uint32_t* st = ws.status + (size_t)p * tiles * radix;
-        uint32_t* ctr = ws.counters + CTR_PASS_TILE + p;
         const uint32_t* kin = ws.keys[cur];
         const uint32_t* vin = p == 0 ? nullptr : ws.vals[cur];
         uint32_t* kout = ws.keys[cur ^ 1];
         uint32_t* vout = ws.vals[cur ^ 1];
         const uint32_t* hp = ws.hist + p * kMaxRadix;
         const int shift = p * ws.digit_bits;
+        const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
+            if (p > 0) upsweep_kernel<9><<<tiles, kSortThreads, 0, s>>>(kin, n, shift, ws.tcount, nt);
+            scan_kernel<9><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
             if (p == 0)
-                onesweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, hp, st, ctr,
-                                                                        (uint32_t)a.N, shift, &a.blk->error);
+                downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
             else
-                onesweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, hp, st, ctr,
-                                                                         (uint32_t)a.N, shift, &a.blk->error);
+                downsweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
         } else {
+            if (p > 0) upsweep_kernel<8><<<tiles, kSortThreads, 0, s>>>(kin, n, shift, ws.tcount, nt);
+            scan_kernel<8><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
             if (p == 0)
-                onesweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, hp, st, ctr,
-                                                                        (uint32_t)a.N, shift, &a.blk->error);
+                downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
             else
-                onesweep_kernel<false, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, hp, st, ctr,
-                                                                         (uint32_t)a.N, shift, &a.blk->error);
+                downsweep_kernel<false, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cur ^= 1;
     }
     ws.sorted_buf = cur;
+    rle_count_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, ws.tcount);
+    tile_scan_kernel<<<1, 1024, 0, s>>>(ws.tcount, (uint32_t)tiles, ws.counters + CTR_U);
     rle_kernel<<<tiles, kSortThreads, 0, s>>>(a, ws, ws.keys[cur]);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const unsigned cgrid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 2);
-    chunk_scan_kernel<<<cgrid, kSortThreads, 0, s>>>(a, ws);
+    const unsigned cgrid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 4);
+    chunk_count_kernel<<<cgrid, kSortThreads, 0, s>>>(a, ws, (uint32_t)tiles);
+    tile_scan_kernel<<<1, 1024, 0, s>>>(ws.tcount, (uint32_t)tiles, ws.counters + CTR_NCHUNK);
+    chunk_write_kernel<<<cgrid, kSortThreads, 0, s>>>(a, ws, (uint32_t)tiles);
     return cudaGetLastError();
 }
 

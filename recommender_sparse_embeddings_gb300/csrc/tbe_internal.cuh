@@ -35,11 +35,7 @@ constexpr int kRadix = 1 << kRadixBits;
 constexpr int kMaxRadixBits = 9;
 constexpr int kMaxRadix = 1 << kMaxRadixBits;
 constexpr int kMaxPasses = 4;
-// Decoupled look-back status words: 2 flag bits + 30 count bits.
-constexpr uint32_t kFlagAgg = 1u << 30;
-constexpr uint32_t kFlagPrefix = 2u << 30;
-constexpr uint32_t kCountMask = (1u << 30) - 1u;
-// Iteration limit of every spin wait (each iteration sleeps ~100 ns).
+// Iteration limit of every spin wait (each iteration sleeps ~64 ns).
 constexpr int kSpinLimit = 1 << 20;
 
 struct TableDesc {
@@ -133,134 +129,6 @@ __device__ __forceinline__ int64_t ld_index(const IDX* p, int64_t k) {
     return (int64_t)__ldg(p + k);
 }
 
-__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_volatile_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Decoupled look-back for D running counts of one thread (counts d0 ..
-// d0+D-1 of a tile's status row): publishes this tile's aggregates, walks
-// back over earlier tiles until one with an inclusive prefix, then publishes
-// this tile's inclusive prefixes; excl receives the exclusive prefixes.
-// Eight status words (8/D predecessors per count) are read per round trip.  Every earlier tile
-// was claimed (atomic tile counter) by a CTA that is already resident and
-// publishes its aggregates without waiting, so each wait ends; the spin is
-// still bounded and raises ERR_TIMEOUT if it runs out.
-constexpr int kLookbackWidth = 8;
-
-template <int D>
-__device__ __forceinline__ void lookback(uint32_t* status, int tile, uint32_t stride, int d0,
-                                         const uint32_t (&aggregate)[D], uint32_t (&excl)[D], uint32_t* err) {
-    uint32_t* row = status + (size_t)tile * stride + d0;
-#pragma unroll
-    for (int i = 0; i < D; ++i) excl[i] = 0;
-    if (tile == 0) {
-#pragma unroll
-        for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagPrefix | aggregate[i]);
-        return;
-    }
-#pragma unroll
-    for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagAgg | aggregate[i]);
-    int j[D];
-    bool done[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) {
-        j[i] = tile - 1;
-        done[i] = false;
-    }
-    constexpr int W = kLookbackWidth / D;  // predecessors per count per round trip
-    int spins = 0;
-    for (;;) {
-        uint32_t sv[D][W];
-#pragma unroll
-        for (int i = 0; i < D; ++i)
-#pragma unroll
-            for (int k = 0; k < W; ++k)
-                sv[i][k] = (!done[i] && j[i] - k >= 0)
-                               ? ld_volatile_u32(status + (size_t)(j[i] - k) * stride + d0 + i)
-                               : 0u;
-        bool all_done = true, any_stall = false;
-#pragma unroll
-        for (int i = 0; i < D; ++i) {
-            if (done[i]) continue;
-            int used = 0;
-            bool stall = false;
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-                if (done[i] || stall) continue;
-                const uint32_t f = sv[i][k] & ~kCountMask;
-                if (f == 0) {
-                    stall = true;
-                    continue;
-                }
-                excl[i] += sv[i][k] & kCountMask;
-                ++used;
-                if (f == kFlagPrefix) done[i] = true;
-            }
-            j[i] -= used;
-            all_done = all_done && done[i];
-            any_stall = any_stall || (stall && !done[i]);
-        }
-        if (all_done) break;
-        if (any_stall) {
-            if (++spins > kSpinLimit) {
-                atomicOr(err, ERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(100);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < D; ++i) st_volatile_u32(row + i, kFlagPrefix | ((excl[i] + aggregate[i]) & kCountMask));
-}
-
-// The same for one count per tile (stride 1), done by a whole warp: the
-// lanes read 32 predecessors at once, so a chain of t tiles takes t/32 round
-// trips.  All lanes of the warp must call it; all get the exclusive prefix.
-__device__ __forceinline__ uint32_t lookback_warp(uint32_t* status, int tile, uint32_t aggregate,
-                                                  uint32_t* err, int lane) {
-    if (tile == 0) {
-        if (lane == 0) st_volatile_u32(status, kFlagPrefix | aggregate);
-        return 0;
-    }
-    if (lane == 0) st_volatile_u32(status + tile, kFlagAgg | aggregate);
-    uint32_t excl = 0;
-    int top = tile - 1;  // nearest predecessor not yet counted
-    int spins = 0;
-    while (top >= 0) {
-        const int idx = top - lane;
-        // below tile 0 reads as an empty prefix (never reached past tile 0,
-        // which always holds one)
-        const uint32_t sv = idx >= 0 ? ld_volatile_u32(status + idx) : kFlagPrefix;
-        const uint32_t f = sv & ~kCountMask;
-        const unsigned pre = __ballot_sync(0xffffffffu, f == kFlagPrefix);
-        const unsigned inval = __ballot_sync(0xffffffffu, f == 0);
-        const int first_pre = pre ? __ffs(pre) - 1 : 32;
-        const unsigned need = first_pre == 32 ? 0xffffffffu : (0xffffffffu >> (31 - first_pre));
-        if (inval & need) {  // a tile before the nearest prefix is not ready yet
-            if (++spins > kSpinLimit) {
-                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
-                break;
-            }
-            __nanosleep(100);
-            continue;
-        }
-        uint32_t c = ((need >> lane) & 1u) ? (sv & kCountMask) : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        excl += c;
-        if (first_pre < 32) break;
-        top -= 32;
-    }
-    if (lane == 0) st_volatile_u32(status + tile, kFlagPrefix | ((excl + aggregate) & kCountMask));
-    return excl;
-}
-
 // ------------------------------------------------------------ launch API
 // (host functions defined in the kernel files, called by the ABI layer)
 
@@ -293,8 +161,7 @@ cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_
 struct Workspace {
     uint32_t* counters;   // [64]
     uint32_t* hist;       // [kMaxPasses][kMaxRadix]
-    uint32_t* status;     // [passes][tiles][1 << digit_bits]
-    uint32_t* rle_status; // [tiles]
+    uint32_t* tcount;     // [1 << digit_bits][tiles]: digit counts of each tile, then digit starts
     uint32_t* tile_bag;   // [tiles]: first bag of each key tile (zeroed per call)
     uint32_t* keys[2];    // [N] ping-pong
     uint32_t* vals[2];    // [N] ping-pong
@@ -305,7 +172,6 @@ struct Workspace {
     uint2* chunk_info;    // [max_chunks]: (distinct-key index u of the run, first chunk of the run)
     uint32_t* chunk_done; // [max_chunks]: chunks of the run finished, kept at the run's first chunk
     uint32_t* cstart;     // [T+1]: first chunk of each table's long runs (cstart[T]: total)
-    uint32_t* run_status; // [tiles]: look-back status of the chunk scan (zeroed per call)
     uint32_t* ustart;     // [T+1]: first distinct-key index of each table (ustart[T]: end)
     float* partial;       // [max_chunks][part_stride]
     int64_t max_chunks;
@@ -318,10 +184,7 @@ struct Workspace {
 // Counter slots inside Workspace::counters.
 enum : int {
     CTR_U = 0,          // number of distinct keys
-    CTR_RUN_TILE = 1,   // tile claim counter of the chunk scan
     CTR_NCHUNK = 2,     // number of chunks of long runs
-    CTR_RLE_TILE = 3,   // tile claim counter of the run-length kernel
-    CTR_PASS_TILE = 4,  // tile claim counters of the sort passes [4]
     CTR_WORK = 8,       // apply work-item counters, one per backward class [15]
     CTR_EXIT = 24,      // apply finished-warp counters, one per backward class [15]
     CTR_HAS_SCALE = 63, // nonzero when prepare wrote the per-lookup scale array
