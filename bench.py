@@ -373,9 +373,16 @@ def run_ours(args):
         brk["prepare"] += e[1].elapsed_time(e[2]) / nb_steps
         brk["apply"] += e[2].elapsed_time(e[3]) / nb_steps
 
-    # U (distinct keys) for the byte count: read once after the run
+    # U (distinct keys) for the byte count: read once after the run; the
+    # histogram tables' lookups are not sorted, so their distinct rows are
+    # counted here
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
+    offs = off.to(torch.int64).cpu()
+    for t, p in enumerate(tbe.tbe_table_paths(h)):
+        if p == "histogram":
+            lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
+            U += int(torch.unique(ind[lo:hi]).numel())
     # radix passes of the sort: 8-bit digits, or 9-bit ones when they save a pass
     key_bits = max(1, h.total_rows.bit_length())
     passes = min((key_bits + 7) // 8, (key_bits + 8) // 9)
@@ -389,13 +396,18 @@ def run_ours(args):
     dominant = max(seg_ms, key=seg_ms.get)
     achieved = nbytes[dominant] / (seg_ms[dominant] / 1e3) / 1e9
     # our kernels per step: forward (gather pool if any gather table, long
-    # bags, one histogram launch per dtype with histogram tables), prepare
-    # (bag marks, keys, one per radix pass, run-length, long runs), apply
-    # (one per backward class)
+    # bags, one histogram launch per dtype with histogram tables); prepare
+    # (bag marks, [compaction], keys, per radix pass [upsweep] + scan +
+    # downsweep, run-length count/scan/write, chunk count/scan/write); apply
+    # (one per backward class of the sorted-path tables, dense sums + update)
     paths = tbe.tbe_table_paths(h)
     hist_dtypes = {s.dtype for s, p in zip(specs, paths) if p == "histogram"}
+    dense = bool(hist_dtypes)  # histogram tables take the dense backward
     fwd_launches = (1 if any(p != "histogram" for p in paths) else 0) + 1 + len(hist_dtypes)
-    launches_per_step = fwd_launches + (2 + passes + 2) + backward_classes(specs)
+    prep_launches = 2 + (1 if dense else 0) + 2 * passes + (passes if dense else passes - 1) + 6
+    sorted_specs = [s for s, p in zip(specs, paths) if p != "histogram"]
+    apply_launches = backward_classes(sorted_specs) + (2 if dense else 0)
+    launches_per_step = fwd_launches + prep_launches + apply_launches
 
     # end-to-end through the public API: inputs from pinned host memory every
     # step, pooled output read back every step

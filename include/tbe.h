@@ -84,6 +84,12 @@ typedef enum { TBE_OPT_SGD = 1, TBE_OPT_ROWWISE_ADAGRAD = 2 } tbe_optimizer_kind
 /* tbe_create flags */
 #define TBE_FLAG_NO_HISTOGRAM 0x1u    /* never use the small-table tensor-core path */
 #define TBE_FLAG_FORCE_HISTOGRAM 0x2u /* use it for every eligible table */
+#define TBE_FLAG_DENSE_BACKWARD 0x4u  /* histogram tables take the dense backward (below) */
+/* Dense backward of a histogram table: its lookups are not sorted; each
+ * row's gradient is summed in fp32 in shared memory straight from the
+ * lookups (the table has at most 1024 rows; each row summed by one warp in
+ * lookup order, so results are reproducible), then every touched row gets
+ * one optimizer step.  Without the flag every table takes the sorted path. */
 
 /* One embedding table.  data: device, row-major rows x dim of dtype,
  * caller-owned, read by forward and updated in place by backward.  The
@@ -114,10 +120,13 @@ typedef struct tbe_handle tbe_handle;
 
 /* Byte offsets, inside a backward workspace, of the arrays the preparation
  * step (transpose, sort, run-length encoding) leaves there.  All arrays are
- * uint32.  sorted_keys/sorted_pos: N entries (key = rowbase_t + row, or
+ * uint32.  sorted_keys/sorted_pos: Ns entries (key = rowbase_t + row, or
  * sum-of-rows for a skipped lookup; pos = the lookup's position in indices),
- * stably sorted by key.  uniq: the distinct keys ascending; runstart: the
- * first sorted slot of each (runstart[U] = N); num_unique: one entry, U. */
+ * stably sorted by key, where Ns = N, or, when the handle has dense-backward
+ * tables (histogram tables with TBE_FLAG_DENSE_BACKWARD), the number of
+ * lookups of the other tables: a dense table's lookups are not sorted.
+ * uniq: the distinct keys ascending; runstart: the first sorted slot of each
+ * (runstart[U] = Ns); num_unique: one entry, U. */
 typedef struct {
     uint64_t sorted_keys;
     uint64_t sorted_pos;
@@ -245,6 +254,10 @@ int tbe_get_error(tbe_handle* h, void* stream);
 
 /* Static description of a status code. */
 const char* tbe_strerror(int code);
+
+/* The cudaError_t of the last CUDA call that failed in a tbe_* call of this
+ * host thread (0 if none), for diagnosing TBE_ERR_CUDA. */
+int tbe_last_cuda_error(void);
 
 /* Per-table schedule chosen at create time, for tests and tuning:
  * out_path[t] = 0 gather path (vector), 1 gather path (element-wise),

@@ -37,6 +37,7 @@ TBE_POOL_SUM, TBE_POOL_MEAN = 0, 1
 TBE_OPT_SGD, TBE_OPT_ROWWISE_ADAGRAD = 1, 2
 TBE_FLAG_NO_HISTOGRAM = 0x1
 TBE_FLAG_FORCE_HISTOGRAM = 0x2
+TBE_FLAG_DENSE_BACKWARD = 0x4
 
 PATH_NAMES = {0: "gather", 1: "gather_elementwise", 2: "histogram"}
 
@@ -99,6 +100,7 @@ def load_library():
         "tbe_backward_sgd_noalloc": ([P, P, P, i32, i64, i32, P, P, f32, P], ctypes.c_int),
         "tbe_get_error": ([P, P], ctypes.c_int),
         "tbe_strerror": ([ctypes.c_int], ctypes.c_char_p),
+        "tbe_last_cuda_error": ([], ctypes.c_int),
         "tbe_table_paths": ([P, ctypes.POINTER(i32)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -119,6 +121,8 @@ def declared_functions() -> List[str]:
 
 def _check(rc: int, where: str):
     if rc != TBE_OK:
+        if rc == TBE_ERR_CUDA:
+            where = f"{where} (cudaError_t {load_library().tbe_last_cuda_error()})"
         raise TBEError(rc, where)
 
 

@@ -29,6 +29,14 @@ struct tbe_handle {
     int32_t* dhist_tables = nullptr;  // histogram-path tables: f16 ones, then bf16 ones
     int n_hist_f16 = 0, n_hist_bf16 = 0;
     size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
+    // dense-backward tables (the histogram tables with TBE_FLAG_DENSE_BACKWARD)
+    int n_dense = 0;
+    int32_t* ddense_tables = nullptr;   // device [n_dense]
+    int64_t* ddense_goff = nullptr;     // device [n_dense+1]: first gradient float of each
+    int64_t* ddense_roff = nullptr;     // device [n_dense+1]: first row count of each
+    int64_t dense_floats = 0, dense_rows = 0;
+    int dense_max_rows = 0, dense_max_dim = 0;
+    int dense_splits = 1;               // most parts per table's lookups (gradient slices)
     int class_begin[kNumClasses] = {};
     int class_count[kNumClasses] = {};
     int total_d = 0;
@@ -55,6 +63,9 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t tabs_offset() { return align_up(sizeof(DevBlock)); }
 size_t class_list_offset(int T) { return align_up(tabs_offset() + sizeof(TableDesc) * T); }
 size_t hist_list_offset(int T) { return align_up(class_list_offset(T) + sizeof(int32_t) * T); }
+size_t dense_list_offset(int T) { return align_up(hist_list_offset(T) + sizeof(int32_t) * T); }
+size_t dense_off_offset(int T) { return align_up(dense_list_offset(T) + sizeof(int32_t) * T); }
+size_t dev_block_bytes(int T) { return dense_off_offset(T) + 2 * sizeof(int64_t) * (T + 1); }
 
 // Small tables the tensor-core histogram path can take: 16-bit rows whose
 // dim is a multiple of 16 in [16, 256] (the MMA's N), 16-byte aligned data,
@@ -94,13 +105,22 @@ int next_pow2(int x) {
     return p;
 }
 
+// Parts each dense table's lookups are split into for a batch of N lookups
+// (one gradient slice each): enough CTAs for the GPU, but at least about
+// 32K lookups per part, so small batches keep a small workspace.
+int dense_parts(const tbe_handle* h, int64_t N) {
+    if (h->n_dense == 0) return 1;
+    const int64_t by_size = N / ((int64_t)h->n_dense * 32768);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(h->dense_splits, by_size));
+}
+
 // Floats per partial-sum row: the widest dim rounded up to 16 bytes, so the
 // vector classes read partial rows with 16-byte loads.
 int part_stride(const tbe_handle* h) { return (h->max_dim + 3) / 4 * 4; }
 
 struct Layout {
     size_t counters, hist, tile_bag, tcount, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
-        chunk_info, chunk_done, cstart, ustart, partial, total;
+        chunk_info, chunk_done, cstart, ustart, tpos, cbase, hrow, dgrad, dcount, partial, total;
     size_t zero_bytes;  // counters..tile_bag are zeroed per call
     int64_t max_chunks;
     int tiles;
@@ -134,6 +154,13 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     L.chunk_done = take(sizeof(uint32_t) * L.max_chunks);
     L.cstart = take(sizeof(uint32_t) * (h->T + 1));
     L.ustart = take(sizeof(uint32_t) * (h->T + 1));
+    L.tpos = take(sizeof(uint32_t) * (h->T + 1));
+    L.cbase = take(sizeof(uint32_t) * (h->T + 1));
+    if (h->n_dense > 0) {
+        L.hrow = take(sizeof(uint16_t) * n);
+        L.dgrad = take(sizeof(float) * (size_t)h->dense_floats * dense_parts(h, N));
+        L.dcount = take(sizeof(uint32_t) * (size_t)h->dense_rows);
+    }
     L.partial = take(sizeof(float) * (size_t)L.max_chunks * part_stride(h));
     L.total = o;
     return L;
@@ -162,6 +189,14 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.chunk_done = reinterpret_cast<uint32_t*>(p + L.chunk_done);
     w.cstart = reinterpret_cast<uint32_t*>(p + L.cstart);
     w.ustart = reinterpret_cast<uint32_t*>(p + L.ustart);
+    w.tpos = reinterpret_cast<uint32_t*>(p + L.tpos);
+    w.cbase = reinterpret_cast<uint32_t*>(p + L.cbase);
+    w.compact = h->n_dense > 0;
+    if (w.compact) {
+        w.hrow = reinterpret_cast<uint16_t*>(p + L.hrow);
+        w.dgrad = reinterpret_cast<float*>(p + L.dgrad);
+        w.dcount = reinterpret_cast<uint32_t*>(p + L.dcount);
+    }
     w.partial = reinterpret_cast<float*>(p + L.partial);
     w.max_chunks = L.max_chunks;
     w.tiles = L.tiles;
@@ -190,12 +225,20 @@ int check_batch(const tbe_handle* h, const void* indices, const void* offsets, i
     return TBE_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? TBE_OK : TBE_ERR_CUDA; }
+// The last failing CUDA call of this host thread, for tbe_last_cuda_error.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = e;
+    return TBE_ERR_CUDA;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? TBE_OK : cuda_fail(e); }
 
 int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
     if (B == h->last_B) return TBE_OK;
     cudaError_t e = launch_forward_schedule(h->dtabs, h->T, B, s);
-    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     h->last_B = B;
     return TBE_OK;
 }
@@ -211,7 +254,8 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
     if (num_tables > kMaxTables) return TBE_ERR_UNSUPPORTED;
     if (pooling != TBE_POOL_SUM && pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
-    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM)) return TBE_ERR_INVALID_ARG;
+    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM | TBE_FLAG_DENSE_BACKWARD))
+        return TBE_ERR_INVALID_ARG;
     tbe_handle* h = new (std::nothrow) tbe_handle();
     if (!h) return TBE_ERR_NO_MEMORY;
     h->T = num_tables;
@@ -280,7 +324,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
     if (e != cudaSuccess) {
         delete h;
-        return TBE_ERR_CUDA;
+        return cuda_fail(e);
     }
     std::vector<int32_t> hist_f16, hist_bf16;
     if (!(flags & TBE_FLAG_NO_HISTOGRAM)) {
@@ -305,12 +349,40 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     }
     h->n_hist_f16 = (int)hist_f16.size();
     h->n_hist_bf16 = (int)hist_bf16.size();
+    // dense backward: the histogram tables, when asked for
+    std::vector<int32_t> dense;
+    std::vector<int64_t> dense_off;  // goff[0..n], then roff[0..n]
+    {
+        std::vector<int64_t> goff{0}, roff{0};
+        for (int t = 0; t < num_tables; ++t) {
+            TableDesc& d = h->tabs[t];
+            d.dslot = -1;
+            if (d.path != PATH_HIST || !(flags & TBE_FLAG_DENSE_BACKWARD)) continue;
+            d.dslot = (int32_t)dense.size();
+            dense.push_back(t);
+            goff.push_back(goff.back() + d.rows * d.dim);
+            roff.push_back(roff.back() + d.rows);
+            h->dense_max_rows = std::max(h->dense_max_rows, (int)d.rows);
+            h->dense_max_dim = std::max(h->dense_max_dim, (int)d.dim);
+        }
+        h->n_dense = (int)dense.size();
+        h->dense_floats = goff.back();
+        h->dense_rows = roff.back();
+        if (h->n_dense > 0) {
+            // about three CTAs per SM, at most 8 gradient slices
+            const int width = h->dense_max_rows <= 512 ? 64 : 32;
+            const int slices = (h->dense_max_dim + width - 1) / width;
+            h->dense_splits = std::max(1, std::min(8, 3 * h->num_sms / (h->n_dense * slices)));
+        }
+        dense_off = goff;
+        dense_off.insert(dense_off.end(), roff.begin(), roff.end());
+    }
     std::vector<int32_t> order;
     {
         std::vector<std::vector<int32_t>> by_class(kNumClasses);
         for (int t = 0; t < num_tables; ++t) {
             h->tabs[t].cls = backward_class(h->tabs[t], h->total_d);
-            by_class[h->tabs[t].cls].push_back(t);
+            if (h->tabs[t].dslot < 0) by_class[h->tabs[t].cls].push_back(t);
         }
         for (int c = 0; c < kNumClasses; ++c) {
             h->class_begin[c] = (int)order.size();
@@ -318,30 +390,37 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
             order.insert(order.end(), by_class[c].begin(), by_class[c].end());
         }
     }
-    const size_t bytes = hist_list_offset(num_tables) + sizeof(int32_t) * num_tables;
+    const size_t bytes = dev_block_bytes(num_tables);
     e = cudaMalloc(&h->dev, bytes);
     if (e != cudaSuccess) {
         delete h;
-        return e == cudaErrorMemoryAllocation ? TBE_ERR_NO_MEMORY : TBE_ERR_CUDA;
+        return e == cudaErrorMemoryAllocation ? TBE_ERR_NO_MEMORY : cuda_fail(e);
     }
     h->blk = static_cast<DevBlock*>(h->dev);
     h->dtabs = reinterpret_cast<TableDesc*>(static_cast<char*>(h->dev) + tabs_offset());
     h->dclass_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + class_list_offset(num_tables));
     h->dhist_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + hist_list_offset(num_tables));
+    h->ddense_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + dense_list_offset(num_tables));
+    h->ddense_goff = reinterpret_cast<int64_t*>(static_cast<char*>(h->dev) + dense_off_offset(num_tables));
+    h->ddense_roff = h->ddense_goff + (h->n_dense + 1);
     e = cudaMemset(h->dev, 0, tabs_offset());
     if (e == cudaSuccess)
         e = cudaMemcpy(h->dtabs, h->tabs.data(), sizeof(TableDesc) * num_tables, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-        e = cudaMemcpy(h->dclass_tables, order.data(), sizeof(int32_t) * num_tables, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !order.empty())  // dense tables are in no class list
+        e = cudaMemcpy(h->dclass_tables, order.data(), sizeof(int32_t) * order.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !hist_f16.empty())
         e = cudaMemcpy(h->dhist_tables, hist_f16.data(), sizeof(int32_t) * hist_f16.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !hist_bf16.empty())
         e = cudaMemcpy(h->dhist_tables + hist_f16.size(), hist_bf16.data(), sizeof(int32_t) * hist_bf16.size(),
                        cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !dense.empty())
+        e = cudaMemcpy(h->ddense_tables, dense.data(), sizeof(int32_t) * dense.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->ddense_goff, dense_off.data(), sizeof(int64_t) * dense_off.size(), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(h->dev);
         delete h;
-        return TBE_ERR_CUDA;
+        return cuda_fail(e);
     }
     {
         int least = 0, greatest = 0;
@@ -356,7 +435,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         }
         if (e != cudaSuccess) {
             tbe_destroy(h);
-            return TBE_ERR_CUDA;
+            return cuda_fail(e);
         }
     }
     *out = h;
@@ -454,10 +533,10 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     Workspace w = bind(h, L, workspace, scale);
     cudaError_t e = cudaMemsetAsync(workspace, 0, L.zero_bytes, s);
     if (e == cudaSuccess && num_indices == 0) e = cudaMemsetAsync(w.runstart, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     // remember, in the workspace's counter block, whether a scale array was written
     if (scale) e = cudaMemsetAsync(w.counters + CTR_HAS_SCALE, 0xff, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     PrepArgs a{};
     a.tabs = h->dtabs;
     a.blk = h->blk;
@@ -472,6 +551,7 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     a.total_rows = (uint32_t)h->total_rows;
     a.key_bits = h->key_bits;
     a.digit_bits = h->digit_bits;
+    a.compact = h->n_dense > 0;
     return cuda_status(launch_prepare(a, w, s));
 }
 
@@ -484,8 +564,9 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
     if (workspace_bytes < make_layout(h, num_indices, kLayoutWithScale).total) return TBE_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // fork: the side stream starts after everything already queued on s
-    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return TBE_ERR_CUDA;
-    if (cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess) return TBE_ERR_CUDA;
+    cudaError_t fe = cudaEventRecord(h->ev_fork, s);
+    if (fe == cudaSuccess) fe = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+    if (fe != cudaSuccess) return cuda_fail(fe);
     rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size, per_sample_weights,
                               workspace, workspace_bytes, h->side);
     // the forward pass runs on s meanwhile
@@ -528,7 +609,27 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.eps = opt->eps;
     a.state = opt->state;
     a.num_sms = h->num_sms;
+    DenseArgs d{};
+    d.tabs = h->dtabs;
+    d.B = batch_size;
+    d.grad = grad_out;
+    d.total_d = h->total_d;
+    d.opt = opt->kind;
+    d.lr = opt->lr;
+    d.eps = opt->eps;
+    d.state = opt->state;
+    d.tables = h->ddense_tables;
+    d.goff = h->ddense_goff;
+    d.roff = h->ddense_roff;
+    d.n = h->n_dense;
+    d.max_rows = h->dense_max_rows;
+    d.max_dim = h->dense_max_dim;
+    d.num_sms = h->num_sms;
+    d.total_rows = h->dense_rows;
+    d.total_floats = h->dense_floats;
+    d.splits = dense_parts(h, num_indices);
     return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count,
+                                    h->n_dense > 0 ? &d : nullptr,
                                     static_cast<cudaStream_t>(stream), h->apply_streams, h->ev_apply_fork,
                                     h->ev_apply_join));
 }
@@ -565,12 +666,14 @@ int tbe_get_error(tbe_handle* h, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&h->blk->error, 0, sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return TBE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     if (bits & ERR_TIMEOUT) return TBE_ERR_TIMEOUT;
     if (bits & ERR_OFFSETS) return TBE_ERR_BAD_OFFSETS;
     if (bits & ERR_OOB) return TBE_ERR_INDEX_OOB;
     return TBE_OK;
 }
+
+int tbe_last_cuda_error(void) { return (int)g_last_cuda_error; }
 
 const char* tbe_strerror(int code) {
     switch (code) {

@@ -777,14 +777,15 @@ static cudaError_t launch_dtype(const ApplyArgs& a, const Workspace& ws, const u
 }
 
 cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, cudaStream_t s,
-                         const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join) {
+                         const int* class_begin, const int* class_count, const DenseArgs* dense,
+                         cudaStream_t s, const cudaStream_t* streams, cudaEvent_t ev_fork,
+                         const cudaEvent_t* ev_join) {
     if (a_in.N == 0) return cudaSuccess;
     const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
     const unsigned grid = (unsigned)(a_in.num_sms * kApplyCtasPerSm);
-    int present = 0;
+    int present = dense ? 1 : 0;  // the dense tables' work counts as one more launch group
     for (int cls = 0; cls < kNumClasses; ++cls) present += class_count[cls] > 0;
-    // more than one class: fork onto the side streams, which start after
+    // more than one group: fork onto the side streams, which start after
     // everything already queued on s
     const bool fork = present > 1;
     if (fork) {
@@ -793,6 +794,11 @@ cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32
         if (e != cudaSuccess) return e;
     }
     int k = 0;
+    if (dense) {
+        const cudaError_t e = launch_dense(*dense, ws, fork ? streams[k % kApplyStreams] : s);
+        ++k;
+        if (e != cudaSuccess) return e;
+    }
     for (int cls = 0; cls < kNumClasses; ++cls) {
         if (class_count[cls] == 0) continue;
         ApplyArgs a = a_in;

@@ -56,6 +56,39 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_
     return warp_excl + x - v;
 }
 
+// Exclusive scan of n counts in place by one 1024-thread block, each thread
+// taking a contiguous chunk (one block-wide scan in all), plus `start`;
+// returns the total on every thread.
+__device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
+                                                        uint32_t* s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t chunk = (n + 1023) / 1024;
+    const uint32_t i0 = tid * chunk, i1 = tmin<uint32_t>(i0 + chunk, n);
+    uint32_t sum = 0;
+    for (uint32_t i = i0; i < i1; ++i) sum += row[i];
+    uint32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+    for (int w = 0; w < 32; ++w) {
+        const uint32_t c = s_warp[w];
+        if (w < warp) before += c;
+        total += c;
+    }
+    uint32_t run = start + before + x - sum;
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint32_t c = row[i];
+        row[i] = run;
+        run += c;
+    }
+    return start + total;
+}
+
 // Lanes of the warp whose BITS-bit label equals this lane's, from one ballot
 // per label bit (labels of BITS bits; all lanes must call it).
 template <int BITS>
@@ -108,10 +141,10 @@ __device__ __forceinline__ int64_t upper_bound_global(const IDX* off, int64_t lo
     return lo;
 }
 
-// Offsets check and the first bag of every key tile: a grid-stride pass over
-// the bags; a bag [o, o1) marks every tile whose first position it holds, so
-// with valid offsets each tile start is marked exactly once (by the bag that
-// contains it).  Malformed offsets leave some marks stale or zero; the keys
+// Offsets check, the first position of every table (tpos) and the first bag
+// of every key tile: a grid-stride pass over the bags; a bag [o, o1) marks
+// every tile whose first position it holds, so with valid offsets each tile
+// start is marked exactly once (by the bag that contains it).  Malformed offsets leave some marks stale or zero; the keys
 // kernel only uses marks to narrow its search and stays in range regardless.
 template <typename IDX>
 __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws) {
@@ -124,6 +157,7 @@ __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws
         if (o < 0 || o > a.N) err |= ERR_OFFSETS;
         if (g == 0 && o != 0) err |= ERR_OFFSETS;
         if (g == nbags && o != a.N) err |= ERR_OFFSETS;
+        if (g % a.B == 0) ws.tpos[g / a.B] = (uint32_t)tmin<int64_t>(tmax<int64_t>(o, 0), a.N);  // table starts
         if (g < nbags) {
             const int64_t o1 = ld_index(off, g + 1);
             if (o1 < o) err |= ERR_OFFSETS;
@@ -133,6 +167,33 @@ __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws
         }
     }
     if (err) atomicOr(&a.blk->error, err);
+}
+
+// Where each sorted-path table's keys go when dense tables are present (their
+// lookups are not sorted): cbase[t] = the lookups of the sorted-path tables
+// before t, cbase[T] and counters[CTR_NS] = all of them (one CTA).
+__global__ void __launch_bounds__(1024) compact_kernel(PrepArgs a, Workspace ws) {
+    __shared__ uint32_t s_warp[32];
+    for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+        uint32_t c = 0;
+        if (a.tabs[t].dslot < 0) {
+            const uint32_t lo = ws.tpos[t];
+            c = tmax<uint32_t>(ws.tpos[t + 1], lo) - lo;
+        }
+        ws.cbase[t] = c;
+    }
+    __syncthreads();
+    const uint32_t total = tmin<uint32_t>(block_scan_row_1024(ws.cbase, (uint32_t)a.T, 0u, s_warp), (uint32_t)a.N);
+    if (threadIdx.x == 0) {
+        ws.cbase[a.T] = total;
+        ws.counters[CTR_NS] = total;
+    }
+}
+
+// Keys to sort: all lookups, or those of the sorted-path tables when dense
+// tables are present.
+__device__ __forceinline__ uint32_t sorted_count(const PrepArgs& a, const Workspace& ws) {
+    return ws.compact ? tmin<uint32_t>(ws.counters[CTR_NS], (uint32_t)a.N) : (uint32_t)a.N;
 }
 
 // One key per position, tile by tile.  The tile's bags [bf, bl] come from
@@ -163,6 +224,7 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
     const int passes = (a.key_bits + dbits - 1) / dbits;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t Nc = a.N;  // offsets are clamped to [0, N] when staged
+    const uint32_t ns = tmax<uint32_t>(sorted_count(a, ws), 1u);
     uint32_t err = 0;
 
     for (int i = threadIdx.x; i < kMaxPasses * kMaxRadix; i += blockDim.x) (&s_hist[0][0])[i] = 0;
@@ -188,12 +250,10 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
         const bool staged = nwin <= kKeysWindow;
         // the tile's indices and weights, loaded before the bag map is built
         IDX xv[kSortItems];
-        float wv[kSortItems];
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k) {
             const int li = warp * (32 * kSortItems) + k * 32 + lane;
             xv[k] = li < n ? ind[p0 + li] : (IDX)0;
-            wv[k] = (a.weights && li < n) ? __ldg(a.weights + p0 + li) : 1.f;
         }
         // window index of each item's bag (staged tiles), two per register
         uint32_t bj2[kSortItems / 2];
@@ -250,6 +310,9 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
         const uint32_t tf_end = (uint32_t)(tf + 1) * B32;  // first bag of the next table
         const uint32_t rows_f = (uint32_t)a.tabs[tf].rows;
         const uint32_t rowbase_f = (uint32_t)a.tabs[tf].rowbase;
+        const bool dense_f = a.tabs[tf].dslot >= 0;
+        // compacted slot of a sorted-path lookup: cbase[t] + (p - tpos[t])
+        const uint32_t shift_f = ws.compact ? ws.cbase[tf] - ws.tpos[tf] : 0u;
         const uint32_t p032 = (uint32_t)p0;
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k) {
@@ -270,55 +333,66 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
                     bag = (uint32_t)b;
                     L = (int32_t)(ld_index(off, b + 1) - ld_index(off, b));
                 }
-                uint32_t rows = rows_f, rowbase = rowbase_f;
+                uint32_t rows = rows_f, rowbase = rowbase_f, shift = shift_f;
+                bool dense = dense_f;
                 if (bag >= tf_end) {
                     int t = tf + 1;
                     for (uint32_t tb = tf_end + B32; bag >= tb && t < a.T - 1; tb += B32) ++t;
                     rows = (uint32_t)a.tabs[t].rows;
                     rowbase = (uint32_t)a.tabs[t].rowbase;
+                    dense = a.tabs[t].dslot >= 0;
+                    shift = ws.compact ? ws.cbase[t] - ws.tpos[t] : 0u;
                 }
                 // an index outside [0, rows) (negative ones included) is skipped
-                uint32_t key = a.total_rows;
-                if ((uint64_t)(int64_t)xv[k] < (uint64_t)rows)
-                    key = rowbase + (uint32_t)xv[k];
-                else
-                    err |= ERR_OOB;
-                keyk = key;
-                ws.keys[0][p] = key;
+                const bool in_range = (uint64_t)(int64_t)xv[k] < (uint64_t)rows;
+                if (!in_range) err |= ERR_OOB;
+                if (dense) {
+                    // dense tables: the row for the shared-memory backward, no key
+                    ws.hrow[p] = in_range ? (uint16_t)xv[k] : (uint16_t)0xffffu;
+                } else {
+                    const uint32_t key = in_range ? rowbase + (uint32_t)xv[k] : a.total_rows;
+                    keyk = key;
+                    // malformed offsets could send a slot out of range: clamp
+                    const uint32_t c = ws.compact ? tmin<uint32_t>(p + shift, ns - 1u) : p;
+                    ws.keys[0][c] = key;
+                    if (ws.compact) ws.vals[0][c] = p;
+                }
                 ws.bag[p] = bag;
                 if (ws.scale) {
-                    float sc = wv[k];
+                    float sc = a.weights ? __ldg(a.weights + p) : 1.f;
                     if (a.mean && L > 0) sc = __fdiv_rn(sc, (float)L);
                     ws.scale[p] = sc;
                 }
             }
-            // digit counts; the top pass's digits take few values within a
-            // warp, so equal ones are added once
+            // digit counts of the sorted keys; the top pass's digits take few
+            // values within a warp, so equal ones are added once
+            const bool counted = keyk != 0xffffffffu;
             for (int q = 0; q < passes; ++q) {
                 const uint32_t d = (keyk >> (q * dbits)) & dmask;
                 uint32_t* c = q == 0 ? &s_tc[d] : &s_hist[q][d];
                 if (q == passes - 1) {
-                    const uint32_t lab = valid ? d : (uint32_t)kMaxRadix;
-                    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+                    const uint32_t lab = counted ? d : (uint32_t)kMaxRadix;
+                    const uint32_t vmask = __ballot_sync(0xffffffffu, counted);
                     const uint32_t d_first = __shfl_sync(0xffffffffu, lab, vmask ? __ffs(vmask) - 1 : 0);
-                    if (__all_sync(0xffffffffu, !valid || lab == d_first)) {
+                    if (__all_sync(0xffffffffu, !counted || lab == d_first)) {
                         // one digit for the whole warp (a table narrower than the digit)
                         if (vmask && lane == __ffs(vmask) - 1) atomicAdd(c, (uint32_t)__popc(vmask));
                     } else {
                         const uint32_t peers = match_label<kMaxRadixBits + 1>(lab);
-                        if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(c, (uint32_t)__popc(peers));
+                        if (counted && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(c, (uint32_t)__popc(peers));
                     }
-                } else if (valid) {
+                } else if (counted) {
                     atomicAdd(c, 1u);
                 }
             }
         }
         // the tile's first-pass digit counts: to the sort's count table and
         // the block's first-pass histogram
+        // (compacted keys do not follow these tiles: the sort counts its own)
         __syncthreads();
         for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x) {
             const uint32_t c = s_tc[d];
-            ws.tcount[(size_t)d * tiles + tile] = c;
+            if (!ws.compact) ws.tcount[(size_t)d * tiles + tile] = c;
             s_hist[0][d] += c;
             s_tc[d] = 0;
         }
@@ -344,11 +418,12 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
 // Digit counts of one tile of keys (one CTA per tile).
 template <int RB>
 __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* __restrict__ keys, uint32_t N,
-                                                               int shift, uint32_t* __restrict__ tcount,
-                                                               uint32_t tiles) {
+                                                               const uint32_t* __restrict__ nsp, int shift,
+                                                               uint32_t* __restrict__ tcount, uint32_t tiles) {
     constexpr int RADIX = 1 << RB;
     __shared__ uint32_t s_c[RADIX];
     const int tid = threadIdx.x;
+    if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
     for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = 0;
     __syncthreads();
     const uint32_t base = blockIdx.x * kSortTile;
@@ -363,39 +438,6 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
         if (base + k * kSortThreads + tid < N) atomicAdd(&s_c[(key[k] >> shift) & (RADIX - 1)], 1u);
     __syncthreads();
     for (int d = tid; d < RADIX; d += kSortThreads) tcount[(size_t)d * tiles + blockIdx.x] = s_c[d];
-}
-
-// Exclusive scan of n counts in place by one 1024-thread block, each thread
-// taking a contiguous chunk (one block-wide scan in all), plus `start`;
-// returns the total on every thread.
-__device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
-                                                        uint32_t* s_warp) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t chunk = (n + 1023) / 1024;
-    const uint32_t i0 = tid * chunk, i1 = tmin<uint32_t>(i0 + chunk, n);
-    uint32_t sum = 0;
-    for (uint32_t i = i0; i < i1; ++i) sum += row[i];
-    uint32_t x = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-    for (int w = 0; w < 32; ++w) {
-        const uint32_t c = s_warp[w];
-        if (w < warp) before += c;
-        total += c;
-    }
-    uint32_t run = start + before + x - sum;
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint32_t c = row[i];
-        row[i] = run;
-        run += c;
-    }
-    return start + total;
 }
 
 // Exclusive scan of one digit's row of tile counts (one CTA per digit),
@@ -439,7 +481,8 @@ __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32
                                                                     uint32_t* __restrict__ keys_out,
                                                                     uint32_t* __restrict__ vals_out,
                                                                     const uint32_t* __restrict__ tstart_g,
-                                                                    uint32_t tiles, uint32_t N, int shift) {
+                                                                    uint32_t tiles, uint32_t N,
+                                                                    const uint32_t* __restrict__ nsp, int shift) {
     constexpr int RADIX = 1 << RB;
     constexpr int DPT = RADIX / kSortThreads;  // digits per thread (consecutive)
     static_assert(DPT >= 1 && DPT * kSortThreads == RADIX, "digits must split evenly over the threads");
@@ -455,6 +498,8 @@ __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32
     const int d0 = tid * DPT;  // this thread's digits
     const uint32_t tile = blockIdx.x;
     const uint32_t base = tile * kSortTile;
+    if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
+    if (base >= N) return;                 // whole CTA: a tile past the sorted keys
     for (int i = tid; i < (kSortThreads / 32) * RADIX; i += kSortThreads) (&s_whist[0][0])[i] = 0;
     // global start of this thread's digits from this tile (used after ranking)
     uint32_t gstart[DPT];
@@ -604,8 +649,10 @@ __device__ __forceinline__ uint32_t rle_load_heads(const uint32_t* __restrict__ 
 
 // Number of runs starting in each tile of sorted keys (one CTA per tile).
 __global__ void __launch_bounds__(kSortThreads) rle_count_kernel(const uint32_t* __restrict__ skeys, uint32_t N,
+                                                                 const uint32_t* __restrict__ nsp,
                                                                  uint32_t* __restrict__ tcount) {
     __shared__ uint32_t s_scan[8];
+    if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
     uint32_t k[kSortItems], prev;
     const uint32_t heads = rle_load_heads(skeys, N, blockIdx.x * kSortTile + threadIdx.x * kSortItems, k, prev);
     uint32_t total;
@@ -628,9 +675,16 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(uint32_t* __restrict__ 
 // sorted and each table owns a consecutive key range), ustart[T] the end.
 __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace ws, const uint32_t* __restrict__ skeys) {
     __shared__ uint32_t s_scan[8];
-    const uint32_t N = (uint32_t)a.N;
+    const uint32_t N = sorted_count(a, ws);
     const int tid = threadIdx.x;
     const uint32_t tile = blockIdx.x;
+    if (N == 0) {  // every lookup belongs to a dense table: no runs
+        if (tile == 0) {
+            for (int t = tid; t <= a.T; t += blockDim.x) ws.ustart[t] = 0;
+            if (tid == 0) ws.runstart[0] = 0;
+        }
+        return;
+    }
     const uint32_t p0 = tile * kSortTile + tid * kSortItems;
     uint32_t k[kSortItems], prev;
     const uint32_t heads = rle_load_heads(skeys, N, p0, k, prev);
@@ -673,7 +727,7 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
 // Chunk counts of the runs of a thread's kSortItems distinct keys from u0.
 __device__ __forceinline__ void run_chunks(const PrepArgs& a, const Workspace& ws, uint32_t U, uint32_t u0,
                                            uint32_t (&nc)[kSortItems]) {
-    const uint32_t N = (uint32_t)a.N;
+    const uint32_t N = sorted_count(a, ws);
     uint32_t rs[kSortItems + 1];
     if (u0 + kSortItems <= U) {
         const uint4* src = reinterpret_cast<const uint4*>(ws.runstart + u0);
@@ -779,45 +833,53 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     const int64_t nbags = (int64_t)a.T * a.B;
     const unsigned mgrid = (unsigned)tmax<int64_t>(1, tmin<int64_t>((nbags + 256) / 256, (int64_t)sms * 8));
     cudaError_t e;
-    if (a.idx64) {
+    if (a.idx64)
         bag_marks_kernel<int64_t><<<mgrid, 256, 0, s>>>(a, ws);
-        e = launch_keys<int64_t>(a, ws, tiles, sms, s);
-    } else {
+    else
         bag_marks_kernel<int32_t><<<mgrid, 256, 0, s>>>(a, ws);
-        e = launch_keys<int32_t>(a, ws, tiles, sms, s);
-    }
+    // dense tables present: only the other tables' keys are sorted, compacted
+    if (a.compact) compact_kernel<<<1, 1024, 0, s>>>(a, ws);
+    e = a.idx64 ? launch_keys<int64_t>(a, ws, tiles, sms, s) : launch_keys<int32_t>(a, ws, tiles, sms, s);
     if (e != cudaSuccess) return e;
+    const uint32_t* nsp = a.compact ? ws.counters + CTR_NS : nullptr;  // sorted keys (device count)
     int cur = 0;
     const int radix = 1 << ws.digit_bits;
     for (int p = 0; p < ws.passes; ++p) {
+        // the first pass numbers the positions itself unless the keys kernel
+        // wrote them (compacted keys) and counted its tiles' digits otherwise
+        const bool gen = p == 0 && !a.compact;
         const uint32_t* kin = ws.keys[cur];
-        const uint32_t* vin = p == 0 ? nullptr : ws.vals[cur];
+        const uint32_t* vin = gen ? nullptr : ws.vals[cur];
         uint32_t* kout = ws.keys[cur ^ 1];
         uint32_t* vout = ws.vals[cur ^ 1];
         const uint32_t* hp = ws.hist + p * kMaxRadix;
         const int shift = p * ws.digit_bits;
         const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
-            if (p > 0) upsweep_kernel<9><<<tiles, kSortThreads, 0, s>>>(kin, n, shift, ws.tcount, nt);
+            if (!gen) upsweep_kernel<9><<<tiles, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt);
             scan_kernel<9><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
-            if (p == 0)
-                downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
+            if (gen)
+                downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
+                                                                         shift);
             else
-                downsweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
+                downsweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
+                                                                          shift);
         } else {
-            if (p > 0) upsweep_kernel<8><<<tiles, kSortThreads, 0, s>>>(kin, n, shift, ws.tcount, nt);
+            if (!gen) upsweep_kernel<8><<<tiles, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt);
             scan_kernel<8><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
-            if (p == 0)
-                downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
+            if (gen)
+                downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
+                                                                         shift);
             else
-                downsweep_kernel<false, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, shift);
+                downsweep_kernel<false, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
+                                                                          shift);
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cur ^= 1;
     }
     ws.sorted_buf = cur;
-    rle_count_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, ws.tcount);
+    rle_count_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, nsp, ws.tcount);
     tile_scan_kernel<<<1, 1024, 0, s>>>(ws.tcount, (uint32_t)tiles, ws.counters + CTR_U);
     rle_kernel<<<tiles, kSortThreads, 0, s>>>(a, ws, ws.keys[cur]);
     e = cudaGetLastError();

@@ -51,7 +51,7 @@ struct TableDesc {
     int32_t vecs;       // column blocks of 32 vectors per row (vector path, 1..4)
     int32_t warp_begin; // first warp of this table in the forward warp map
     int32_t cls;        // backward class: dtype * NUM_SHAPES + row shape code
-    int32_t pad_;
+    int32_t dslot;      // index among the dense-backward tables, -1 for the sorted path
 };
 
 // Device-resident descriptor block owned by a handle.
@@ -173,6 +173,12 @@ struct Workspace {
     uint32_t* chunk_done; // [max_chunks]: chunks of the run finished, kept at the run's first chunk
     uint32_t* cstart;     // [T+1]: first chunk of each table's long runs (cstart[T]: total)
     uint32_t* ustart;     // [T+1]: first distinct-key index of each table (ustart[T]: end)
+    uint32_t* tpos;       // [T+1]: position of each table's first lookup (tpos[T] = N)
+    uint32_t* cbase;      // [T+1]: first sorted slot of each sorted-path table's keys (compacted)
+    uint16_t* hrow;       // [N]: row of each dense-table lookup (0xffff: skipped)
+    float* dgrad;         // [splits][dense floats]: dense tables' partial gradients, row-major per table
+    uint32_t* dcount;     // dense tables' lookups per row
+    int compact;          // dense tables present: their lookups stay out of the sort
     float* partial;       // [max_chunks][part_stride]
     int64_t max_chunks;
     int tiles;
@@ -184,6 +190,7 @@ struct Workspace {
 // Counter slots inside Workspace::counters.
 enum : int {
     CTR_U = 0,          // number of distinct keys
+    CTR_NS = 1,         // number of sorted keys (lookups of sorted-path tables)
     CTR_NCHUNK = 2,     // number of chunks of long runs
     CTR_WORK = 8,       // apply work-item counters, one per backward class [15]
     CTR_EXIT = 24,      // apply finished-warp counters, one per backward class [15]
@@ -205,6 +212,7 @@ struct PrepArgs {
     uint32_t total_rows;  // sentinel key for skipped lookups
     int key_bits;
     int digit_bits;  // radix digit width (8 or 9)
+    int compact;     // dense tables present (their lookups are not sorted)
 };
 
 // Backward row-shape codes: dim 32, 64, 128, 256 with aligned rows and
@@ -237,6 +245,31 @@ struct ApplyArgs {
     int cls;
 };
 
+// Dense backward of the histogram tables (dense.cu): per table, the row
+// gradients are summed in shared memory straight from the lookups (no sort),
+// then every row some lookup touched gets one optimizer step.
+struct DenseArgs {
+    const TableDesc* tabs;
+    int B;
+    const float* grad;
+    int total_d;
+    int opt;
+    float lr;
+    float eps;
+    float* state;
+    const int32_t* tables;   // dense tables (device)
+    const int64_t* goff;     // [n+1] first gradient float of each dense table in dgrad (device)
+    const int64_t* roff;     // [n+1] first row count of each dense table in dcount (device)
+    int n;
+    int max_rows;
+    int max_dim;
+    int num_sms;
+    int64_t total_rows;      // sum of the dense tables' rows (rows to update)
+    int64_t total_floats;    // sum of the dense tables' rows x dims
+    int splits;              // parts each table's lookups are split into (one gradient slice each)
+};
+cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s);
+
 // Streams the backward class kernels are spread over: each class kernel
 // takes its work from its own counter, so they may run side by side and one
 // class's tail overlaps the next class's work.
@@ -246,8 +279,10 @@ constexpr int kApplyStreams = 4;
 // every class (device, grouped by class); class_begin/class_count index it.
 // With more than one class, the launches fork from s onto the given streams
 // and s waits for all.
+// dense (nullable) runs side by side with the class kernels.
 cudaError_t launch_apply(const ApplyArgs& a, const Workspace& ws, const int32_t* class_tables,
-                         const int* class_begin, const int* class_count, cudaStream_t s,
-                         const cudaStream_t* streams, cudaEvent_t ev_fork, const cudaEvent_t* ev_join);
+                         const int* class_begin, const int* class_count, const DenseArgs* dense,
+                         cudaStream_t s, const cudaStream_t* streams, cudaEvent_t ev_fork,
+                         const cudaEvent_t* ev_join);
 
 }  // namespace tbe

@@ -57,22 +57,26 @@ def test_full_size(cid):
     out = tbe.tbe_forward_prepare(h, batch.indices, batch.offsets, B, ws, batch.weights)
     assert tbe.tbe_get_error(h) == tbe.TBE_OK
 
-    # ---- sort / run-length: whole arrays, bit-exact
+    # ---- sort / run-length: whole arrays, bit-exact (default flags: every
+    # table's keys are sorted)
     keys, bag_of = oracle.make_keys(rows, ind, off, B)
-    perm = np.argsort(keys, kind="stable")
-    skeys = keys[perm]
+    dense = np.zeros(T, dtype=bool)
+    keep = np.flatnonzero(~dense[bag_of // B])
+    Ns = len(keep)
+    perm = np.argsort(keys[keep], kind="stable")
+    skeys = keys[keep][perm]
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
 
     def u32(offset, n):
         return ws[offset:offset + 4 * n].view(torch.int32).cpu().numpy().view(np.uint32).astype(np.int64)
 
-    np.testing.assert_array_equal(u32(lay.sorted_keys, N), skeys)
-    np.testing.assert_array_equal(u32(lay.sorted_pos, N), perm)
+    np.testing.assert_array_equal(u32(lay.sorted_keys, Ns), skeys)
+    np.testing.assert_array_equal(u32(lay.sorted_pos, Ns), keep[perm])
     U = int(u32(lay.num_unique, 1)[0])
     head = np.flatnonzero(np.r_[True, skeys[1:] != skeys[:-1]])
     assert U == len(head)
     np.testing.assert_array_equal(u32(lay.uniq, U), skeys[head])
-    np.testing.assert_array_equal(u32(lay.runstart, U + 1), np.r_[head, N])
+    np.testing.assert_array_equal(u32(lay.runstart, U + 1), np.r_[head, Ns])
 
     # ---- forward: sampled bags
     bsample = np.sort(rng.choice(B, size=48, replace=False))

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import recommender_sparse_embeddings_gb300 as tbe
 import workloads
 from helpers import FP32_TOL, assert_close, oracle_forward
@@ -106,3 +107,132 @@ def test_histogram_workload_small_tables():
     assert_close(got[:, :64 * 64], ref[:, :64 * 64], what="hist tables", **HIST_TOL)
     assert_close(got[:, 64 * 64:], ref[:, 64 * 64:], what="gather table", **FP32_TOL)
     h.close()
+
+
+# ------------------------------------------------------ dense backward
+
+def _multi_table_batch(specs, B, max_len, seed, oob_table=None):
+    """CSR batch over several tables (table-major)."""
+    ind, off = [], [torch.zeros(1, dtype=torch.int64)]
+    for t, (rows, _, _) in enumerate(specs):
+        i, o = batch_for(rows, B, max_len, seed=seed + t, oob=(t == oob_table))
+        ind.append(i)
+        off.append(o[1:] + off[-1][-1])
+    return torch.cat(ind), torch.cat(off)
+
+
+def _dense_case(specs, B, pooling, weighted, optimizer, flags=tbe.TBE_FLAG_DENSE_BACKWARD, seed=0, oob_table=None,
+                applies=1):
+    from helpers import DT_NAME, table_bits, touched_rows, assert_tables_match
+    g = torch.Generator().manual_seed(seed)
+    tables = [(torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV) for r, d, dt in specs]
+    ind, off = _multi_table_batch(specs, B, 70, seed=seed + 11, oob_table=oob_table)
+    w = torch.rand(ind.numel(), generator=g) if weighted else None
+    grad = torch.randn((B, sum(d for _, d, _ in specs)), generator=g)
+    before = [table_bits(t) for t in tables]
+    cpu_tables = [t.cpu() for t in tables]
+    h = tbe.tbe_create(tables, pooling, flags)
+    ws = tbe.make_workspace(h, ind.numel(), B)
+    total_rows = sum(r for r, _, _ in specs)
+    state = torch.zeros(total_rows, dtype=torch.float32, device=DEV) if optimizer == "adagrad" else None
+    tbe.tbe_backward_prepare(h, ind.to(DEV), off.to(DEV), B, ws, None if w is None else w.to(DEV))
+    for _ in range(applies):
+        tbe.tbe_backward_apply(h, ind.numel(), B, grad.to(DEV), ws, optimizer, 0.05, 1e-8, state)
+    rc = tbe.tbe_get_error(h)
+    assert rc == (tbe.TBE_ERR_INDEX_OOB if oob_table is not None else tbe.TBE_OK)
+    ref_tabs = [table_bits(t) for t in cpu_tables]
+    ref_state = None if state is None else np.zeros(total_rows, np.float32)
+    for _ in range(applies):
+        oracle.backward(ref_tabs, [DT_NAME[t.dtype] for t in cpu_tables], ind.numpy(), off.numpy(), B,
+                        grad.numpy(), optimizer, 0.05, eps=1e-8, weights=None if w is None else w.numpy(),
+                        pooling=pooling, state=ref_state)
+    touched = touched_rows(cpu_tables, ind, off, B)
+    assert_tables_match(tables, ref_tabs, before, touched, what=f"dense {specs} {pooling} w={weighted} {optimizer}")
+    if state is not None:
+        assert_close(state.cpu().numpy(), ref_state, what="dense state", **FP32_TOL)
+        st = state.cpu().numpy()
+        tm = np.concatenate(touched)
+        assert (st[tm] > 0).all() and not st[~tm].any()
+    h.close()
+    return tables
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("rows,dim", [(512, 64), (100, 16), (33, 48), (300, 128), (512, 256)])
+@pytest.mark.parametrize("pooling,weighted", [("sum", False), ("sum", True), ("mean", True)])
+def test_dense_backward_sgd_matches_oracle(dtype, rows, dim, pooling, weighted):
+    """A histogram table next to a gather-path table: the first takes the
+    dense backward, the second the sorted one (compacted keys)."""
+    specs = [(rows, dim, dtype), (3000, 32, torch.float32)]
+    _dense_case(specs, 333, pooling, weighted, "sgd", seed=rows + dim)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("rows,dim", [(512, 64), (33, 48), (200, 256)])
+def test_dense_backward_rowwise_adagrad_matches_oracle(dtype, rows, dim):
+    specs = [(700, 64, torch.bfloat16), (rows, dim, dtype), (rows, dim, torch.float16)]
+    _dense_case(specs, 257, "mean", True, "adagrad", seed=rows * 3 + dim)
+
+
+def test_dense_backward_only_dense_tables():
+    """Every lookup belongs to a dense table: nothing is sorted."""
+    specs = [(512, 64, torch.float16), (128, 32, torch.bfloat16)]
+    _dense_case(specs, 300, "sum", True, "adagrad", seed=7)
+
+
+def test_dense_backward_out_of_range_is_skipped():
+    specs = [(64, 32, torch.float16), (5000, 32, torch.float32)]
+    _dense_case(specs, 130, "sum", False, "sgd", seed=9, oob_table=0)
+
+
+def test_dense_backward_applies_twice():
+    """prepare once, apply twice: the shared-memory sums start from zero each
+    time (the accumulators are cleared per apply).  Each apply is checked as
+    one oracle step from the tables it started from (16-bit storage rounds
+    after every step, so two oracle steps from the start would compound
+    one-ulp differences)."""
+    from helpers import DT_NAME, table_bits, touched_rows, assert_tables_match
+    specs = [(512, 64, torch.float16), (2000, 64, torch.float32)]
+    g = torch.Generator().manual_seed(13)
+    tables = [(torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV) for r, d, dt in specs]
+    B = 200
+    ind, off = _multi_table_batch(specs, B, 70, seed=24)
+    w = torch.rand(ind.numel(), generator=g)
+    grad = torch.randn((B, 128), generator=g)
+    h = tbe.tbe_create(tables, "sum", tbe.TBE_FLAG_DENSE_BACKWARD)
+    ws = tbe.make_workspace(h, ind.numel(), B)
+    tbe.tbe_backward_prepare(h, ind.to(DEV), off.to(DEV), B, ws, w.to(DEV))
+    touched = touched_rows([t.cpu() for t in tables], ind, off, B)
+    for step in range(2):
+        start = [t.cpu() for t in tables]
+        tbe.tbe_backward_apply(h, ind.numel(), B, grad.to(DEV), ws, "sgd", 0.05)
+        assert tbe.tbe_get_error(h) == tbe.TBE_OK
+        ref = [table_bits(t) for t in start]
+        oracle.backward(ref, [DT_NAME[t.dtype] for t in start], ind.numpy(), off.numpy(), B, grad.numpy(), "sgd",
+                        0.05, weights=w.numpy())
+        assert_tables_match(tables, ref, [table_bits(t) for t in start], touched, what=f"apply {step}")
+    h.close()
+
+
+def test_dense_and_sorted_backward_agree_on_the_histogram_workload():
+    """The 65-table workload shrunk: default (sorted) and TBE_FLAG_DENSE_BACKWARD
+    (dense) backward both match the oracle."""
+    cfg = workloads.get_config(5).scaled(B=300, rows_div=1000, rows_min=512)
+    specs = workloads.realize_tables(cfg)
+    from helpers import oracle_backward, table_bits, touched_rows, assert_tables_match
+    batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
+    grad = workloads.make_grad(cfg, "cpu", specs)
+    base = workloads.make_tables(cfg, "cpu", specs)
+    ref_tabs, _ = oracle_backward(base, batch.indices, batch.offsets, cfg.B, grad, "sgd", cfg.lr,
+                                  weights=batch.weights, pooling=cfg.pooling)
+    touched = touched_rows(base, batch.indices, batch.offsets, cfg.B)
+    before = [table_bits(t) for t in base]
+    for flags in (0, tbe.TBE_FLAG_DENSE_BACKWARD):
+        tables = [t.to(DEV) for t in base]
+        h = tbe.tbe_create(tables, cfg.pooling, flags)
+        ws = tbe.make_workspace(h, batch.N, cfg.B)
+        tbe.tbe_backward_sgd(h, batch.indices.to(DEV), batch.offsets.to(DEV), cfg.B, grad.to(DEV), cfg.lr, ws,
+                             batch.weights.to(DEV))
+        assert tbe.tbe_get_error(h) == tbe.TBE_OK
+        assert_tables_match(tables, ref_tabs, before, touched, what=f"workload 5 flags={flags}")
+        h.close()

@@ -55,10 +55,10 @@ def test_forward_matches_oracle(cid, index_dtype):
     assert_close(out.cpu().numpy(), ref, what=f"cfg{cid} forward", **FP32_TOL)
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
-def test_prepare_sort_and_rle_bit_exact(cid):
+@pytest.mark.parametrize("cid,flags", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (5, tbe.TBE_FLAG_DENSE_BACKWARD)])
+def test_prepare_sort_and_rle_bit_exact(cid, flags):
     cfg, tables, batch, _ = make_problem(cid)
-    h = tbe.tbe_create(tables, cfg.pooling)
+    h = tbe.tbe_create(tables, cfg.pooling, flags)
     ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
     w = None if batch.weights is None else batch.weights.to(DEV)
     ws = tbe.make_workspace(h, batch.N, cfg.B)
@@ -71,24 +71,31 @@ def test_prepare_sort_and_rle_bit_exact(cid):
         return ws[offset:offset + 4 * n].view(torch.int32).cpu().numpy().view(np.uint32).astype(np.int64)
 
     U = int(view(lay.num_unique, 1)[0])
-    keys, _ = oracle.make_keys([t.shape[0] for t in tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
-    ref = oracle.sort_rle(keys)
-    np.testing.assert_array_equal(view(lay.sorted_keys, N), ref["sorted_keys"])
-    np.testing.assert_array_equal(view(lay.sorted_pos, N), ref["sorted_pos"])
+    keys, bag = oracle.make_keys([t.shape[0] for t in tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
+    # with TBE_FLAG_DENSE_BACKWARD the histogram tables' lookups are not
+    # sorted: only the other tables' keys (their positions in ascending order)
+    dense = np.array([p == "histogram" and bool(flags & tbe.TBE_FLAG_DENSE_BACKWARD)
+                      for p in tbe.tbe_table_paths(h)])
+    keep = np.flatnonzero(~dense[bag // cfg.B])
+    ref = oracle.sort_rle(keys[keep])
+    Ns = len(keep)
+    np.testing.assert_array_equal(view(lay.sorted_keys, Ns), ref["sorted_keys"])
+    np.testing.assert_array_equal(view(lay.sorted_pos, Ns), keep[ref["sorted_pos"]])
     assert U == len(ref["uniq"])
     np.testing.assert_array_equal(view(lay.uniq, U), ref["uniq"])
     rs = view(lay.runstart, U + 1)
     np.testing.assert_array_equal(rs[:U], ref["runstart"])
-    assert rs[U] == N
+    assert rs[U] == Ns
     np.testing.assert_array_equal(np.diff(rs), ref["runlen"])
 
 
-@pytest.mark.parametrize("index_dtype", [torch.int64, torch.int32])
+@pytest.mark.parametrize("index_dtype,flags", [(torch.int64, 0), (torch.int32, 0),
+                                               (torch.int64, tbe.TBE_FLAG_DENSE_BACKWARD)])
 @pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
-def test_backward_matches_oracle(cid, index_dtype):
+def test_backward_matches_oracle(cid, index_dtype, flags):
     cfg, tables, batch, grad = make_problem(cid, index_dtype)
     before = [table_bits(t) for t in tables]
-    h = tbe.tbe_create(tables, cfg.pooling)
+    h = tbe.tbe_create(tables, cfg.pooling, flags)
     ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
     w = None if batch.weights is None else batch.weights.to(DEV)
     ws = tbe.make_workspace(h, batch.N, cfg.B)
