@@ -65,6 +65,8 @@ def _load():
         lib.oracle_backward.argtypes = [i32, P, P, P, P, i32, i32, P, P, i64, P, i32, P, i32,
                                         f32, f32, P, P, P, P]
         lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_weight_grad.argtypes = [i32, P, P, P, P, i32, i32, P, P, i64, i32, P, P]
+        lib.oracle_weight_grad.restype = ctypes.c_int
         lib.oracle_round.argtypes = [i32, P, i64, P]
         lib.oracle_round.restype = None
         lib.oracle_decode.argtypes = [i32, P, i64, P]
@@ -131,6 +133,28 @@ def forward(tables: Sequence[np.ndarray], dtypes: Sequence[str], indices, offset
     if rc:
         raise OracleError(f"oracle_forward failed: {rc}")
     return out, int(skipped.value)
+
+
+def weight_grad(tables: Sequence[np.ndarray], dtypes: Sequence[str], indices, offsets, B: int, grad_out,
+                pooling: str = "sum"):
+    """dL/dw_i for every lookup (0 for skipped ones), given G = dL/dout."""
+    lib = _load()
+    tabs = [_table_bits(w, d) for w, d in zip(tables, dtypes)]
+    rows, dims, codes = _table_meta(tabs, dtypes)
+    indices, offsets, is64 = _index_arrays(indices, offsets)
+    T = len(tabs)
+    if offsets.shape[0] != T * B + 1:
+        raise ValueError("offsets must have T*B+1 entries")
+    g = np.ascontiguousarray(grad_out, dtype=np.float32)
+    if g.shape != (B, int(dims.sum())):
+        raise ValueError("grad_out must be [B, sum of dims]")
+    ptrs = (ctypes.c_void_p * T)(*[w.ctypes.data for w in tabs])
+    out = np.zeros(indices.shape[0], dtype=np.float32)
+    rc = lib.oracle_weight_grad(T, _ptr(rows), _ptr(dims), _ptr(codes), ptrs, B, is64, _ptr(indices),
+                                _ptr(offsets), indices.shape[0], int(pooling == "mean"), _ptr(g), _ptr(out))
+    if rc:
+        raise OracleError(f"oracle_weight_grad failed: {rc}")
+    return out
 
 
 def make_keys(rows: Sequence[int], indices, offsets, B: int):

@@ -38,6 +38,10 @@
  *  - sort key of lookup i is rowbase_t + idx_i (rowbase_t = sum of rows of
  *    the tables before t); a skipped lookup gets the key sum_t rows_t.  The
  *    sort is stable (equal keys keep ascending position).
+ *  - the per-sample weights are trainable inputs: their gradient is the dot
+ *    product of the looked-up row (as stored, before this step's update)
+ *    with the bag's slice of the upstream gradient, times 1/L for mean
+ *    pooling; a skipped lookup's weight gets gradient 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -196,6 +200,48 @@ int oracle_forward(int32_t T, const int64_t* rows, const int32_t* dims, const in
     }
     free(acc);
     if (n_skipped) *n_skipped = skipped;
+    return OR_OK;
+}
+
+/* Gradient of the loss with respect to each lookup's per-sample weight
+ * (kimbodo "What Happened": per-sample weights), given the upstream gradient
+ * G = dL/dout:  out[b, Doff_t + j] = sum_i s_i W_t[idx_i, j] with
+ * s_i = w_i (times 1/L for mean pooling), so
+ * dL/dw_i = sum_j G[b, Doff_t + j] W_t[idx_i, j]   (times 1/L for mean).
+ * A skipped lookup (index out of range) gets 0.  Sums in double, one
+ * rounding to float. */
+int oracle_weight_grad(int32_t T, const int64_t* rows, const int32_t* dims, const int32_t* dtypes,
+                       const void* const* tables, int32_t B, int32_t index_is64,
+                       const void* indices, const void* offsets, int64_t N, int32_t mean_pooling,
+                       const float* grad_out, float* wgrad) {
+    if (T <= 0 || B < 0 || N < 0) return OR_BAD_ARG;
+    int rc = check_offsets(offsets, index_is64, (int64_t)T * B, N);
+    if (rc) return rc;
+    int64_t total_d = 0;
+    for (int t = 0; t < T; ++t) total_d += dims[t];
+    int64_t doff = 0;
+    for (int t = 0; t < T; ++t) {
+        const int D = dims[t];
+        for (int b = 0; b < B; ++b) {
+            const int64_t bag = (int64_t)t * B + b;
+            const int64_t start = load_index(offsets, index_is64, bag);
+            const int64_t end = load_index(offsets, index_is64, bag + 1);
+            const int64_t L = end - start;
+            const float* g = grad_out + (int64_t)b * total_d + doff;
+            for (int64_t i = start; i < end; ++i) {
+                const int64_t r = load_index(indices, index_is64, i);
+                if (r < 0 || r >= rows[t]) {
+                    wgrad[i] = 0.0f;
+                    continue;
+                }
+                double dot = 0.0;
+                for (int j = 0; j < D; ++j) dot += (double)g[j] * load_elem(tables[t], dtypes[t], r * D + j);
+                if (mean_pooling && L > 0) dot /= (double)L;
+                wgrad[i] = (float)dot;
+            }
+        }
+        doff += D;
+    }
     return OR_OK;
 }
 

@@ -420,3 +420,70 @@ def test_backward_low_precision_rows_round_once():
         if dts[t] == "f16":
             np.testing.assert_array_equal(after[t], exact.astype(np.float16).view(np.uint16))
         np.testing.assert_array_equal(after[t], expect)
+
+
+# ------------------------------------------------- per-sample weight gradient
+
+def torch_weight_grad(tabs, ind, off, B, w, pooling, G):
+    """per_sample_weights.grad of sum(out * G) through torch CPU embedding_bag in
+    float64; out-of-range lookups are routed to an appended zero row."""
+    leaf = torch.from_numpy(w.astype(np.float64)).requires_grad_(True)
+    outs = []
+    for t, wt in enumerate(tabs):
+        R = wt.shape[0]
+        w64 = torch.cat([wt.to(torch.float64), torch.zeros(1, wt.shape[1], dtype=torch.float64)])
+        o = off[t * B:(t + 1) * B + 1].astype(np.int64)
+        ii = ind[o[0]:o[-1]].astype(np.int64)
+        ii = np.where((ii < 0) | (ii >= R), R, ii)
+        psw = leaf[o[0]:o[-1]]
+        if pooling == "mean":
+            lens = np.diff(o)
+            psw = psw / torch.from_numpy(np.repeat(lens, lens).astype(np.float64))
+        outs.append(F.embedding_bag(torch.from_numpy(ii), w64, torch.from_numpy(o - o[0]), mode="sum",
+                                    per_sample_weights=psw, include_last_offset=True))
+    (torch.cat(outs, 1) * torch.from_numpy(G.astype(np.float64))).sum().backward()
+    return leaf.grad.numpy()
+
+
+@pytest.mark.parametrize("pooling", ["sum", "mean"])
+@pytest.mark.parametrize("oob", [False, True])
+def test_weight_grad_matches_torch_autograd(pooling, oob):
+    for seed in range(3):
+        tabs, dts, ind, off, w, _ = random_problem(40 + seed, weights=True, max_len=8, oob=oob)
+        B = 7
+        G = np.random.default_rng(seed).standard_normal((B, 24)).astype(np.float32)
+        got = oracle.weight_grad(np_tables(tabs), dts, ind, off, B, G, pooling=pooling)
+        ref = torch_weight_grad(tabs, ind, off, B, w, pooling, G)
+        np.testing.assert_allclose(got, ref.astype(np.float32), rtol=1e-6, atol=1e-7)
+        if oob:
+            rows = [t.shape[0] for t in tabs]
+            for t in range(3):
+                lo, hi = off[t * B], off[(t + 1) * B]
+                bad = (ind[lo:hi] < 0) | (ind[lo:hi] >= rows[t])
+                assert not got[lo:hi][bad].any()
+
+
+def test_weight_grad_euler_identity():
+    """out is linear in the weights, so sum_i w_i dL/dw_i = sum(out * G)."""
+    tabs, dts, ind, off, w, _ = random_problem(51, weights=True, max_len=9)
+    B = 7
+    G = np.random.default_rng(4).standard_normal((B, 24)).astype(np.float32)
+    for pooling in ("sum", "mean"):
+        out, _ = oracle.forward(np_tables(tabs), dts, ind, off, B, weights=w, pooling=pooling)
+        gw = oracle.weight_grad(np_tables(tabs), dts, ind, off, B, G, pooling=pooling)
+        lhs = float(np.dot(w.astype(np.float64), gw.astype(np.float64)))
+        rhs = float((out.astype(np.float64) * G.astype(np.float64)).sum())
+        assert lhs == pytest.approx(rhs, rel=1e-5, abs=1e-6)
+
+
+def test_weight_grad_hand_case():
+    """One table of two rows, D = 2; bag 0 = rows (1, 0, 1), bag 1 empty."""
+    W = np.array([[1.0, 2.0], [3.0, -1.0]], np.float32)
+    ind = np.array([1, 0, 1], np.int64)
+    off = np.array([0, 3, 3], np.int64)
+    G = np.array([[0.5, 2.0], [7.0, 7.0]], np.float32)
+    got = oracle.weight_grad([W], ["f32"], ind, off, 2, G)
+    # row 1 . G[0] = 1.5 - 2 = -0.5; row 0 . G[0] = 0.5 + 4 = 4.5
+    np.testing.assert_array_equal(got, np.array([-0.5, 4.5, -0.5], np.float32))
+    got = oracle.weight_grad([W], ["f32"], ind, off, 2, G, pooling="mean")
+    np.testing.assert_allclose(got, np.array([-0.5, 4.5, -0.5], np.float32) / 3, rtol=1e-7)
