@@ -104,6 +104,16 @@ def algorithmic_bytes(specs, batch_lengths, N, B, T, idx_bytes, weights, optimiz
     return dict(forward=fwd, prepare=prep, apply=apply, step=fwd + prep + apply)
 
 
+def wgrad_bytes(specs, batch_lengths, N, B, T, idx_bytes):
+    """Algorithmic bytes of the per-sample weight gradient: the looked-up rows,
+    indices and offsets (as the forward pass), the upstream gradient read once
+    and one fp32 result per lookup."""
+    per_table_lookups = batch_lengths.view(T, B).sum(1).tolist()
+    gathered = sum(n * s.dim * ELEM[s.dtype] for n, s in zip(per_table_lookups, specs))
+    total_d = sum(s.dim for s in specs)
+    return gathered + N * idx_bytes + (T * B + 1) * idx_bytes + B * total_d * 4 + N * 4
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -300,7 +310,9 @@ def run_ours(args):
     batch = workloads.make_batch(cfg, dev, idx_dtype, specs)
     grad = workloads.make_grad(cfg, dev, specs)
     T, B, N = len(specs), cfg.B, batch.N
-    h = tbe.tbe_create(tables, cfg.pooling, tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0)
+    flags = (tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0) | (
+        tbe.TBE_FLAG_SORTED_BACKWARD if args.sorted_backward else 0)
+    h = tbe.tbe_create(tables, cfg.pooling, flags)
     ws = tbe.make_workspace(h, N, B, dev)
     out = torch.empty((B, h.total_dim), dtype=torch.float32, device=dev)
     state = (torch.zeros(h.total_rows, dtype=torch.float32, device=dev)
@@ -373,6 +385,23 @@ def run_ours(args):
         brk["prepare"] += e[1].elapsed_time(e[2]) / nb_steps
         brk["apply"] += e[2].elapsed_time(e[3]) / nb_steps
 
+    # per-sample weight gradient (weighted batches): timed alone, after a flush
+    wg_ms = None
+    if w is not None:
+        gw_out = torch.empty(N, dtype=torch.float32, device=dev)
+        evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nb_steps)]
+        for k in range(nb_steps):
+            flush.zero_()
+            evw[k][0].record(stream)
+            tbe.tbe_per_sample_weight_grad(h, ind, off, B, grad, gw_out)
+            evw[k][1].record(stream)
+        torch.cuda.synchronize()
+        wg_ms = sum(a.elapsed_time(b) for a, b in evw) / nb_steps
+        rc = tbe.tbe_get_error(h)
+        if rc != tbe.TBE_OK:
+            raise RuntimeError(f"device error in the weight gradient: {tbe.tbe_strerror(rc)}")
+
     # U (distinct keys) for the byte count: read once after the run; the
     # histogram tables' lookups are not sorted, so their distinct rows are
     # counted here
@@ -380,7 +409,7 @@ def run_ours(args):
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
     offs = off.to(torch.int64).cpu()
     for t, p in enumerate(tbe.tbe_table_paths(h)):
-        if p == "histogram":
+        if p == "histogram" and not args.sorted_backward:
             lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
             U += int(torch.unique(ind[lo:hi]).numel())
     # radix passes of the sort: 8-bit digits, or 9-bit ones when they save a pass
@@ -402,10 +431,10 @@ def run_ours(args):
     # (one per backward class of the sorted-path tables, dense sums + update)
     paths = tbe.tbe_table_paths(h)
     hist_dtypes = {s.dtype for s, p in zip(specs, paths) if p == "histogram"}
-    dense = bool(hist_dtypes)  # histogram tables take the dense backward
+    dense = bool(hist_dtypes) and not args.sorted_backward  # histogram tables' dense backward
     fwd_launches = (1 if any(p != "histogram" for p in paths) else 0) + 1 + len(hist_dtypes)
     prep_launches = 2 + (1 if dense else 0) + 2 * passes + (passes if dense else passes - 1) + 6
-    sorted_specs = [s for s, p in zip(specs, paths) if p != "histogram"]
+    sorted_specs = [s for s, p in zip(specs, paths) if not (dense and p == "histogram")]
     apply_launches = backward_classes(sorted_specs) + (2 if dense else 0)
     launches_per_step = fwd_launches + prep_launches + apply_launches
 
@@ -485,6 +514,11 @@ def run_ours(args):
                     "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
                     "frac": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9 / peak,
                     "ms": brk["forward"]},
+            "wgrad": None if wg_ms is None else {
+                "ms": wg_ms, "bytes": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize),
+                "gbs": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9,
+                "frac": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9 / peak,
+                "note": "per-sample weight gradient, timed alone outside the step"},
             "step_gbs": nbytes["step"] / (ms_step / 1e3) / 1e9,
             "segments_ms": seg_ms,
             "breakdown_ms_sequential": brk,
@@ -557,6 +591,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-histogram", action="store_true",
                    help="keep small tables on the gather path (no tensor-core histogram path)")
+    p.add_argument("--sorted-backward", action="store_true",
+                   help="histogram tables take the sorted backward instead of the dense (tensor-core) one")
     p.add_argument("--tables", type=int, default=0,
                    help="use only the first K tables of the workload (profiling cases)")
     args = p.parse_args(argv)

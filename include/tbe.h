@@ -84,12 +84,12 @@ typedef enum { TBE_OPT_SGD = 1, TBE_OPT_ROWWISE_ADAGRAD = 2 } tbe_optimizer_kind
 /* tbe_create flags */
 #define TBE_FLAG_NO_HISTOGRAM 0x1u    /* never use the small-table tensor-core path */
 #define TBE_FLAG_FORCE_HISTOGRAM 0x2u /* use it for every eligible table */
-#define TBE_FLAG_DENSE_BACKWARD 0x4u  /* histogram tables take the dense backward (below) */
-/* Dense backward of a histogram table: its lookups are not sorted; each
- * row's gradient is summed in fp32 in shared memory straight from the
- * lookups (the table has at most 1024 rows; each row summed by one warp in
- * lookup order, so results are reproducible), then every touched row gets
- * one optimizer step.  Without the flag every table takes the sorted path. */
+#define TBE_FLAG_SORTED_BACKWARD 0x4u /* histogram tables too take the sorted backward */
+/* Backward of a histogram table (default): its lookups are not sorted; the
+ * table's whole gradient H^T . G is one tensor-core product (bf16 operands
+ * split three ways for fp32 accuracy, fp32 accumulation; reproducible), then
+ * every touched row gets one optimizer step.  TBE_FLAG_SORTED_BACKWARD sends
+ * these tables through the sort and segment reduction like the others. */
 
 /* One embedding table.  data: device, row-major rows x dim of dtype,
  * caller-owned, read by forward and updated in place by backward.  The
@@ -123,7 +123,7 @@ typedef struct tbe_handle tbe_handle;
  * uint32.  sorted_keys/sorted_pos: Ns entries (key = rowbase_t + row, or
  * sum-of-rows for a skipped lookup; pos = the lookup's position in indices),
  * stably sorted by key, where Ns = N, or, when the handle has dense-backward
- * tables (histogram tables with TBE_FLAG_DENSE_BACKWARD), the number of
+ * tables (histogram tables, unless TBE_FLAG_SORTED_BACKWARD), the number of
  * lookups of the other tables: a dense table's lookups are not sorted.
  * uniq: the distinct keys ascending; runstart: the first sorted slot of each
  * (runstart[U] = Ns); num_unique: one entry, U. */
@@ -244,6 +244,30 @@ int tbe_backward_sgd_noalloc(tbe_handle* h, const void* indices, const void* off
                              int32_t index_dtype, int64_t num_indices, int32_t batch_size,
                              const float* per_sample_weights, const float* grad_out, float lr,
                              void* stream);
+
+/* ----------------------------------------------- per-sample weight gradient */
+
+/* Gradient of the loss with respect to each per-sample weight, for callers
+ * that train the weights (kimbodo "What Happened": per-sample weights on the
+ * generic path; the pages give no formula, this is the derivative of the
+ * forward pass's definition):
+ *   grad_weights[i] = (1/L if mean) * sum_j grad_out[b, Doff_t + j] * W_t[idx_i, j]
+ * for lookup i of bag (t, b) of length L; 0 for a lookup whose index is out
+ * of range (the forward pass skips it; reported as TBE_ERR_INDEX_OOB by
+ * tbe_get_error).  fp32 products and sums for every table dtype.
+ *  indices, offsets, index_dtype, num_indices, batch_size: the batch, as
+ *    for tbe_forward (device, CSR, T*B+1 offsets);
+ *  grad_out: device fp32 [batch_size, sum of dims], read only;
+ *  grad_weights: device fp32 [num_indices], caller-owned, fully written
+ *    when the offsets are well formed (a malformed bag is reported as
+ *    TBE_ERR_BAD_OFFSETS by tbe_get_error and its entries are not written).
+ * It reads the table rows as they are when it runs on `stream`: call it
+ * before tbe_backward_apply (or the fused backward calls) updates them.
+ * Errors: INVALID_ARG (null pointers, bad enums or sizes), UNSUPPORTED
+ * (more than 2^26 bags), CUDA. */
+int tbe_per_sample_weight_grad(tbe_handle* h, const void* indices, const void* offsets,
+                               int32_t index_dtype, int64_t num_indices, int32_t batch_size,
+                               const float* grad_out, float* grad_weights, void* stream);
 
 /* ------------------------------------------------------------- diagnostics */
 

@@ -37,7 +37,7 @@ TBE_POOL_SUM, TBE_POOL_MEAN = 0, 1
 TBE_OPT_SGD, TBE_OPT_ROWWISE_ADAGRAD = 1, 2
 TBE_FLAG_NO_HISTOGRAM = 0x1
 TBE_FLAG_FORCE_HISTOGRAM = 0x2
-TBE_FLAG_DENSE_BACKWARD = 0x4
+TBE_FLAG_SORTED_BACKWARD = 0x4
 
 PATH_NAMES = {0: "gather", 1: "gather_elementwise", 2: "histogram"}
 
@@ -98,6 +98,7 @@ def load_library():
         "tbe_backward_rowwise_adagrad": ([P, P, P, i32, i64, i32, P, P, P, f32, f32, P,
                                           ctypes.c_size_t, P], ctypes.c_int),
         "tbe_backward_sgd_noalloc": ([P, P, P, i32, i64, i32, P, P, f32, P], ctypes.c_int),
+        "tbe_per_sample_weight_grad": ([P, P, P, i32, i64, i32, P, P, P], ctypes.c_int),
         "tbe_get_error": ([P, P], ctypes.c_int),
         "tbe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tbe_last_cuda_error": ([], ctypes.c_int),
@@ -220,6 +221,20 @@ def tbe_forward(h: Handle, indices: torch.Tensor, offsets: torch.Tensor, batch_s
                          _stream(stream))
     _check(rc, "tbe_forward")
     return out
+
+
+def tbe_per_sample_weight_grad(h: Handle, indices: torch.Tensor, offsets: torch.Tensor, batch_size: int,
+                               grad_out: torch.Tensor, grad_weights: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """dL/dw_i for every lookup; call before the backward pass updates the rows."""
+    lib = load_library()
+    if grad_weights is None:
+        grad_weights = torch.empty(indices.numel(), dtype=torch.float32, device=offsets.device)
+    rc = lib.tbe_per_sample_weight_grad(h.ptr, _ptr(indices), _ptr(offsets), _index_dtype(indices, offsets),
+                                        indices.numel(), batch_size, _ptr(grad_out), _ptr(grad_weights),
+                                        _stream(stream))
+    _check(rc, "tbe_per_sample_weight_grad")
+    return grad_weights
 
 
 def tbe_backward_workspace_bytes(h: Handle, num_indices: int, batch_size: int) -> int:

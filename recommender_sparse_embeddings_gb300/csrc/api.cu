@@ -29,14 +29,14 @@ struct tbe_handle {
     int32_t* dhist_tables = nullptr;  // histogram-path tables: f16 ones, then bf16 ones
     int n_hist_f16 = 0, n_hist_bf16 = 0;
     size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
-    // dense-backward tables (the histogram tables with TBE_FLAG_DENSE_BACKWARD)
+    // dense-backward tables (the histogram tables unless TBE_FLAG_SORTED_BACKWARD)
     int n_dense = 0;
     int32_t* ddense_tables = nullptr;   // device [n_dense]
     int64_t* ddense_goff = nullptr;     // device [n_dense+1]: first gradient float of each
     int64_t* ddense_roff = nullptr;     // device [n_dense+1]: first row count of each
     int64_t dense_floats = 0, dense_rows = 0;
     int dense_max_rows = 0, dense_max_dim = 0;
-    int dense_splits = 1;               // most parts per table's lookups (gradient slices)
+    int dense_groups = 1;               // CTAs per table for its rows (128-row tiles per CTA)
     int class_begin[kNumClasses] = {};
     int class_count[kNumClasses] = {};
     int total_d = 0;
@@ -105,13 +105,23 @@ int next_pow2(int x) {
     return p;
 }
 
-// Parts each dense table's lookups are split into for a batch of N lookups
-// (one gradient slice each): enough CTAs for the GPU, but at least about
-// 32K lookups per part, so small batches keep a small workspace.
-int dense_parts(const tbe_handle* h, int64_t N) {
+// Parts each dense table's bags are split into for a batch of B bags (one
+// CTA and one gradient slice each; one CTA per SM): the count of at most 8
+// that best fills whole waves, with at least 64 bags per part.
+int dense_parts(const tbe_handle* h, int64_t B) {
     if (h->n_dense == 0) return 1;
-    const int64_t by_size = N / ((int64_t)h->n_dense * 32768);
-    return (int)std::max<int64_t>(1, std::min<int64_t>(h->dense_splits, by_size));
+    const int64_t ctas = (int64_t)h->n_dense * h->dense_groups;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 8 && (s == 1 || B / s >= 64); ++s) {
+        const double waves = (double)((ctas * s + h->num_sms - 1) / h->num_sms);
+        const double cost = waves / s;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 // Floats per partial-sum row: the widest dim rounded up to 16 bytes, so the
@@ -120,13 +130,13 @@ int part_stride(const tbe_handle* h) { return (h->max_dim + 3) / 4 * 4; }
 
 struct Layout {
     size_t counters, hist, tile_bag, tcount, keys0, keys1, vals0, vals1, bag, scale, uniq, runstart,
-        chunk_info, chunk_done, cstart, ustart, tpos, cbase, hrow, dgrad, dcount, partial, total;
+        chunk_info, chunk_done, cstart, ustart, tpos, cbase, hrow, dboff, dgrad, dcount, partial, total;
     size_t zero_bytes;  // counters..tile_bag are zeroed per call
     int64_t max_chunks;
     int tiles;
 };
 
-Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
+Layout make_layout(const tbe_handle* h, int64_t N, int64_t B, bool scale) {
     Layout L{};
     const int64_t n = std::max<int64_t>(N, 1);
     L.tiles = (int)((N + kSortTile - 1) / kSortTile);
@@ -158,7 +168,8 @@ Layout make_layout(const tbe_handle* h, int64_t N, bool scale) {
     L.cbase = take(sizeof(uint32_t) * (h->T + 1));
     if (h->n_dense > 0) {
         L.hrow = take(sizeof(uint16_t) * n);
-        L.dgrad = take(sizeof(float) * (size_t)h->dense_floats * dense_parts(h, N));
+        L.dboff = take(sizeof(uint32_t) * (size_t)h->n_dense * (size_t)(std::max<int64_t>(B, 0) + 1));
+        L.dgrad = take(sizeof(float) * (size_t)h->dense_floats * dense_parts(h, B));
         L.dcount = take(sizeof(uint32_t) * (size_t)h->dense_rows);
     }
     L.partial = take(sizeof(float) * (size_t)L.max_chunks * part_stride(h));
@@ -194,6 +205,7 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
     w.compact = h->n_dense > 0;
     if (w.compact) {
         w.hrow = reinterpret_cast<uint16_t*>(p + L.hrow);
+        w.dboff = reinterpret_cast<uint32_t*>(p + L.dboff);
         w.dgrad = reinterpret_cast<float*>(p + L.dgrad);
         w.dcount = reinterpret_cast<uint32_t*>(p + L.dcount);
     }
@@ -254,7 +266,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
     if (num_tables > kMaxTables) return TBE_ERR_UNSUPPORTED;
     if (pooling != TBE_POOL_SUM && pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
-    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM | TBE_FLAG_DENSE_BACKWARD))
+    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM | TBE_FLAG_SORTED_BACKWARD))
         return TBE_ERR_INVALID_ARG;
     tbe_handle* h = new (std::nothrow) tbe_handle();
     if (!h) return TBE_ERR_NO_MEMORY;
@@ -349,7 +361,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     }
     h->n_hist_f16 = (int)hist_f16.size();
     h->n_hist_bf16 = (int)hist_bf16.size();
-    // dense backward: the histogram tables, when asked for
+    // dense backward: the histogram tables, unless the sorted path is asked for
     std::vector<int32_t> dense;
     std::vector<int64_t> dense_off;  // goff[0..n], then roff[0..n]
     {
@@ -357,7 +369,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         for (int t = 0; t < num_tables; ++t) {
             TableDesc& d = h->tabs[t];
             d.dslot = -1;
-            if (d.path != PATH_HIST || !(flags & TBE_FLAG_DENSE_BACKWARD)) continue;
+            if (d.path != PATH_HIST || (flags & TBE_FLAG_SORTED_BACKWARD)) continue;
             d.dslot = (int32_t)dense.size();
             dense.push_back(t);
             goff.push_back(goff.back() + d.rows * d.dim);
@@ -369,10 +381,10 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         h->dense_floats = goff.back();
         h->dense_rows = roff.back();
         if (h->n_dense > 0) {
-            // about three CTAs per SM, at most 8 gradient slices
-            const int width = h->dense_max_rows <= 512 ? 64 : 32;
-            const int slices = (h->dense_max_dim + width - 1) / width;
-            h->dense_splits = std::max(1, std::min(8, 3 * h->num_sms / (h->n_dense * slices)));
+            // rows per CTA: 128-row tiles whose accumulators (dim columns
+            // each) fit the 512 tensor-memory columns, at most four
+            const int mt = std::min(4, 512 / h->dense_max_dim);
+            h->dense_groups = (h->dense_max_rows + mt * 128 - 1) / (mt * 128);
         }
         dense_off = goff;
         dense_off.insert(dense_off.end(), roff.begin(), roff.end());
@@ -499,17 +511,42 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
     return rc;
 }
 
+int tbe_per_sample_weight_grad(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                               int64_t num_indices, int32_t batch_size, const float* grad_out,
+                               float* grad_weights, void* stream) {
+    int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
+    if (rc) return rc;
+    if (batch_size == 0 || num_indices == 0) return TBE_OK;
+    if (!grad_out || !grad_weights) return TBE_ERR_INVALID_ARG;
+    if ((int64_t)h->T * batch_size >= (int64_t(1) << 31) / 32) return TBE_ERR_UNSUPPORTED;
+    WgradArgs a{};
+    a.tabs = h->dtabs;
+    a.blk = h->blk;
+    a.T = h->T;
+    a.B = batch_size;
+    a.N = num_indices;
+    a.indices = indices;
+    a.offsets = offsets;
+    a.idx64 = index_dtype == TBE_I64;
+    a.grad = grad_out;
+    a.total_d = h->total_d;
+    a.grad_vec = h->total_d % 4 == 0 && ((uintptr_t)grad_out % 16) == 0;
+    a.mean = h->pooling == TBE_POOL_MEAN;
+    a.out = grad_weights;
+    return cuda_status(launch_wgrad(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t tbe_backward_workspace_bytes(const tbe_handle* h, int64_t num_indices, int32_t batch_size) {
     (void)batch_size;
     if (!h || num_indices < 0) return 0;
-    return make_layout(h, num_indices, kLayoutWithScale).total;
+    return make_layout(h, num_indices, batch_size, kLayoutWithScale).total;
 }
 
 int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int32_t batch_size,
                                   tbe_ws_layout* out) {
     (void)batch_size;
     if (!h || !out || num_indices < 0) return TBE_ERR_INVALID_ARG;
-    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    const Layout L = make_layout(h, num_indices, batch_size, kLayoutWithScale);
     const bool odd = h->passes % 2 == 1;
     out->sorted_keys = odd ? L.keys1 : L.keys0;
     out->sorted_pos = odd ? L.vals1 : L.vals0;
@@ -526,7 +563,7 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (!workspace) return TBE_ERR_INVALID_ARG;
-    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    const Layout L = make_layout(h, num_indices, batch_size, kLayoutWithScale);
     if (workspace_bytes < L.total) return TBE_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool scale = needs_scale(h, per_sample_weights);
@@ -561,7 +598,7 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (!workspace || (batch_size > 0 && !out)) return TBE_ERR_INVALID_ARG;
-    if (workspace_bytes < make_layout(h, num_indices, kLayoutWithScale).total) return TBE_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < make_layout(h, num_indices, batch_size, kLayoutWithScale).total) return TBE_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // fork: the side stream starts after everything already queued on s
     cudaError_t fe = cudaEventRecord(h->ev_fork, s);
@@ -588,7 +625,7 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     if (opt->kind != TBE_OPT_SGD && opt->kind != TBE_OPT_ROWWISE_ADAGRAD) return TBE_ERR_INVALID_ARG;
     if (opt->kind == TBE_OPT_ROWWISE_ADAGRAD && !opt->state) return TBE_ERR_INVALID_ARG;
     if (num_indices > 0 && !grad_out) return TBE_ERR_INVALID_ARG;
-    const Layout L = make_layout(h, num_indices, kLayoutWithScale);
+    const Layout L = make_layout(h, num_indices, batch_size, kLayoutWithScale);
     if (workspace_bytes < L.total) return TBE_ERR_WORKSPACE_TOO_SMALL;
     if (num_indices == 0 || batch_size == 0) return TBE_OK;
     Workspace w = bind(h, L, workspace, true);
@@ -611,6 +648,7 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.num_sms = h->num_sms;
     DenseArgs d{};
     d.tabs = h->dtabs;
+    d.blk = h->blk;
     d.B = batch_size;
     d.grad = grad_out;
     d.total_d = h->total_d;
@@ -627,7 +665,8 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     d.num_sms = h->num_sms;
     d.total_rows = h->dense_rows;
     d.total_floats = h->dense_floats;
-    d.splits = dense_parts(h, num_indices);
+    d.splits = dense_parts(h, batch_size);
+    d.grad_vec = ((uintptr_t)grad_out % 16) == 0 && h->total_d % 4 == 0;
     return cuda_status(launch_apply(a, w, h->dclass_tables, h->class_begin, h->class_count,
                                     h->n_dense > 0 ? &d : nullptr,
                                     static_cast<cudaStream_t>(stream), h->apply_streams, h->ev_apply_fork,

@@ -89,20 +89,6 @@ __device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ r
     return start + total;
 }
 
-// Lanes of the warp whose BITS-bit label equals this lane's, from one ballot
-// per label bit (labels of BITS bits; all lanes must call it).
-template <int BITS>
-__device__ __forceinline__ uint32_t match_label(uint32_t label) {
-    uint32_t peers = 0xffffffffu;
-#pragma unroll
-    for (int b = 0; b < BITS; ++b) {
-        const bool bit = (label >> b) & 1u;
-        const uint32_t v = __ballot_sync(0xffffffffu, bit);
-        peers &= bit ? v : ~v;
-    }
-    return peers;
-}
-
 // ------------------------------------------------------------------ keys
 
 constexpr int kKeysWindow = kSortTile + 1;  // offsets staged per tile
@@ -157,7 +143,14 @@ __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws
         if (o < 0 || o > a.N) err |= ERR_OFFSETS;
         if (g == 0 && o != 0) err |= ERR_OFFSETS;
         if (g == nbags && o != a.N) err |= ERR_OFFSETS;
-        if (g % a.B == 0) ws.tpos[g / a.B] = (uint32_t)tmin<int64_t>(tmax<int64_t>(o, 0), a.N);  // table starts
+        const uint32_t oc = (uint32_t)tmin<int64_t>(tmax<int64_t>(o, 0), a.N);
+        const int tg = (int)(g / a.B), bl = (int)(g % a.B);
+        if (bl == 0) ws.tpos[tg] = oc;  // table starts
+        if (a.compact) {                // bag offsets of the dense tables
+            if (tg < a.T && a.tabs[tg].dslot >= 0) ws.dboff[(int64_t)a.tabs[tg].dslot * (a.B + 1) + bl] = oc;
+            if (bl == 0 && tg > 0 && a.tabs[tg - 1].dslot >= 0)
+                ws.dboff[(int64_t)a.tabs[tg - 1].dslot * (a.B + 1) + a.B] = oc;
+        }
         if (g < nbags) {
             const int64_t o1 = ld_index(off, g + 1);
             if (o1 < o) err |= ERR_OFFSETS;

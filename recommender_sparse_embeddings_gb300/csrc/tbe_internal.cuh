@@ -124,6 +124,20 @@ __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
     }
 }
 
+// Lanes of the warp whose BITS-bit label equals this lane's, from one ballot
+// per label bit (labels of BITS bits; all lanes must call it).
+template <int BITS>
+__device__ __forceinline__ uint32_t match_label(uint32_t label) {
+    uint32_t peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < BITS; ++b) {
+        const bool bit = (label >> b) & 1u;
+        const uint32_t v = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? v : ~v;
+    }
+    return peers;
+}
+
 template <typename IDX>
 __device__ __forceinline__ int64_t ld_index(const IDX* p, int64_t k) {
     return (int64_t)__ldg(p + k);
@@ -153,6 +167,25 @@ struct FwdArgs {
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 
+// Gradient of the per-sample weights (wgrad.cu).
+struct WgradArgs {
+    const TableDesc* tabs;
+    DevBlock* blk;
+    int T;
+    int B;
+    int64_t N;
+    const void* indices;
+    const void* offsets;
+    int idx64;
+    const float* grad;  // [B, total_d]
+    int total_d;
+    int grad_vec;       // grad rows and table column offsets allow 16-byte loads
+    int mean;
+    float* out;         // [N]
+};
+
+cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s);
+
 // Small-table tensor-core path (hist.cu).
 size_t hist_smem_bytes(int64_t rows, int dim);
 cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_f16, size_t smem_f16,
@@ -176,6 +209,7 @@ struct Workspace {
     uint32_t* tpos;       // [T+1]: position of each table's first lookup (tpos[T] = N)
     uint32_t* cbase;      // [T+1]: first sorted slot of each sorted-path table's keys (compacted)
     uint16_t* hrow;       // [N]: row of each dense-table lookup (0xffff: skipped)
+    uint32_t* dboff;      // [dense tables][B+1]: offsets of each dense table's bags
     float* dgrad;         // [splits][dense floats]: dense tables' partial gradients, row-major per table
     uint32_t* dcount;     // dense tables' lookups per row
     int compact;          // dense tables present: their lookups stay out of the sort
@@ -250,6 +284,7 @@ struct ApplyArgs {
 // then every row some lookup touched gets one optimizer step.
 struct DenseArgs {
     const TableDesc* tabs;
+    DevBlock* blk;
     int B;
     const float* grad;
     int total_d;
@@ -266,7 +301,8 @@ struct DenseArgs {
     int num_sms;
     int64_t total_rows;      // sum of the dense tables' rows (rows to update)
     int64_t total_floats;    // sum of the dense tables' rows x dims
-    int splits;              // parts each table's lookups are split into (one gradient slice each)
+    int splits;              // parts each table's bags are split into (one gradient slice each)
+    int grad_vec;            // grad is 16-byte aligned with total_d % 4 == 0 (float4 rows)
 };
 cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s);
 

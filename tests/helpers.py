@@ -35,7 +35,24 @@ def np_index(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
+def accumulation_allowance(terms_abs_sum, n_terms, scale) -> np.ndarray:
+    """Absolute error allowance for an updated row w - scale * g, where g is an
+    fp32 sum of n_terms terms whose magnitudes add up to terms_abs_sum.
+
+    Each fp32 addition rounds to nearest with relative error at most 2^-24 of
+    a partial sum bounded by terms_abs_sum; taking those errors as
+    independent, the error of g has a standard deviation of about
+    sqrt(n) * 2^-24 * terms_abs_sum, and four of those are allowed.  The
+    update multiplies that error by `scale` (lr for SGD, lr / (sqrt(m) + eps)
+    for row-wise Adagrad).  Where w and scale * g nearly cancel, the relative
+    tolerance on the small result is tighter than the fp32 gradient itself
+    can be; this term covers exactly that."""
+    n = np.asarray(n_terms, dtype=np.float64)
+    return 4.0 * np.sqrt(n) * 2.0 ** -24 * np.asarray(terms_abs_sum, np.float64) * np.asarray(scale, np.float64)
+
+
 def assert_close(got, ref, rtol, atol, what=""):
+    """|got - ref| <= atol + rtol * |ref| element-wise (atol may be an array)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
@@ -44,8 +61,9 @@ def assert_close(got, ref, rtol, atol, what=""):
     bad = ~(err <= bound)
     if bad.any():
         k = np.flatnonzero(bad.ravel())[:5]
+        atol_at = np.broadcast_to(np.asarray(atol, np.float64), ref.shape).ravel()[k]
         raise AssertionError(
-            f"{what}: {int(bad.sum())} of {bad.size} outside tol (rtol={rtol}, atol={atol}); "
+            f"{what}: {int(bad.sum())} of {bad.size} outside tol (rtol={rtol}, atol={atol_at.tolist()}); "
             f"first at flat {k.tolist()}: got {got.ravel()[k].tolist()} ref {ref.ravel()[k].tolist()}; "
             f"max abs err {err.max():.3e}")
 

@@ -1,5 +1,6 @@
 """GPU parity at the workloads' full sizes, in the configuration bench.py
-times (default handle flags, int64 indices).
+times (default handle flags, int64 indices: histogram tables take the dense
+backward and stay out of the sort).
 
 Full tables (4 to 20 GB) are too large for the oracle, so the checks are:
   - sort and run-length encoding: the whole sorted key array, sorted
@@ -22,7 +23,7 @@ import torch
 import oracle
 import recommender_sparse_embeddings_gb300 as tbe
 import workloads
-from helpers import DT_NAME, FP32_TOL, LOWP_TOL, assert_close, table_bits
+from helpers import DT_NAME, FP32_TOL, LOWP_TOL, accumulation_allowance, assert_close, table_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -57,10 +58,10 @@ def test_full_size(cid):
     out = tbe.tbe_forward_prepare(h, batch.indices, batch.offsets, B, ws, batch.weights)
     assert tbe.tbe_get_error(h) == tbe.TBE_OK
 
-    # ---- sort / run-length: whole arrays, bit-exact (default flags: every
-    # table's keys are sorted)
+    # ---- sort / run-length: whole arrays, bit-exact (histogram tables take
+    # the dense backward: only the other tables' keys are sorted)
     keys, bag_of = oracle.make_keys(rows, ind, off, B)
-    dense = np.zeros(T, dtype=bool)
+    dense = np.array([p == "histogram" for p in paths])
     keep = np.flatnonzero(~dense[bag_of // B])
     Ns = len(keep)
     perm = np.argsort(keys[keep], kind="stable")
@@ -140,7 +141,13 @@ def test_full_size(cid):
         oracle.backward([c_tab], [name], remap.astype(np.int64), np.arange(len(hit) + 1, dtype=np.int64),
                         len(hit), c_grad, cfg.optimizer, cfg.lr, eps=cfg.eps, weights=s.astype(np.float32),
                         pooling="sum", state=c_state)
-        tol = FP32_TOL if name == "f32" else LOWP_TOL
+        tol = dict(FP32_TOL if name == "f32" else LOWP_TOL)
+        # rounding allowance of the fp32 row sums (rows hit thousands of times)
+        abs_terms = np.zeros((len(touched), c_grad.shape[1]))
+        np.add.at(abs_terms, remap, np.abs(s[:, None] * c_grad.astype(np.float64)))
+        n_terms = np.bincount(remap, minlength=len(touched))[:, None]
+        scale = cfg.lr if state is None else cfg.lr / (np.sqrt(c_state.astype(np.float64)) + cfg.eps)[:, None]
+        tol["atol"] = tol["atol"] + accumulation_allowance(abs_terms, n_terms, scale)
         assert_close(oracle.decode(name, after_tr), oracle.decode(name, c_tab), what=f"cfg{cid} table {t} rows",
                      **tol)
         if state is not None:

@@ -121,7 +121,7 @@ def _multi_table_batch(specs, B, max_len, seed, oob_table=None):
     return torch.cat(ind), torch.cat(off)
 
 
-def _dense_case(specs, B, pooling, weighted, optimizer, flags=tbe.TBE_FLAG_DENSE_BACKWARD, seed=0, oob_table=None,
+def _dense_case(specs, B, pooling, weighted, optimizer, flags=0, seed=0, oob_table=None,
                 applies=1):
     from helpers import DT_NAME, table_bits, touched_rows, assert_tables_match
     g = torch.Generator().manual_seed(seed)
@@ -199,7 +199,7 @@ def test_dense_backward_applies_twice():
     ind, off = _multi_table_batch(specs, B, 70, seed=24)
     w = torch.rand(ind.numel(), generator=g)
     grad = torch.randn((B, 128), generator=g)
-    h = tbe.tbe_create(tables, "sum", tbe.TBE_FLAG_DENSE_BACKWARD)
+    h = tbe.tbe_create(tables, "sum")
     ws = tbe.make_workspace(h, ind.numel(), B)
     tbe.tbe_backward_prepare(h, ind.to(DEV), off.to(DEV), B, ws, w.to(DEV))
     touched = touched_rows([t.cpu() for t in tables], ind, off, B)
@@ -215,8 +215,8 @@ def test_dense_backward_applies_twice():
 
 
 def test_dense_and_sorted_backward_agree_on_the_histogram_workload():
-    """The 65-table workload shrunk: default (sorted) and TBE_FLAG_DENSE_BACKWARD
-    (dense) backward both match the oracle."""
+    """The 65-table workload shrunk: default (dense) and TBE_FLAG_SORTED_BACKWARD
+    (sorted) backward both match the oracle."""
     cfg = workloads.get_config(5).scaled(B=300, rows_div=1000, rows_min=512)
     specs = workloads.realize_tables(cfg)
     from helpers import oracle_backward, table_bits, touched_rows, assert_tables_match
@@ -227,7 +227,7 @@ def test_dense_and_sorted_backward_agree_on_the_histogram_workload():
                                   weights=batch.weights, pooling=cfg.pooling)
     touched = touched_rows(base, batch.indices, batch.offsets, cfg.B)
     before = [table_bits(t) for t in base]
-    for flags in (0, tbe.TBE_FLAG_DENSE_BACKWARD):
+    for flags in (0, tbe.TBE_FLAG_SORTED_BACKWARD):
         tables = [t.to(DEV) for t in base]
         h = tbe.tbe_create(tables, cfg.pooling, flags)
         ws = tbe.make_workspace(h, batch.N, cfg.B)

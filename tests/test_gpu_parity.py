@@ -55,7 +55,7 @@ def test_forward_matches_oracle(cid, index_dtype):
     assert_close(out.cpu().numpy(), ref, what=f"cfg{cid} forward", **FP32_TOL)
 
 
-@pytest.mark.parametrize("cid,flags", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (5, tbe.TBE_FLAG_DENSE_BACKWARD)])
+@pytest.mark.parametrize("cid,flags", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (5, tbe.TBE_FLAG_SORTED_BACKWARD)])
 def test_prepare_sort_and_rle_bit_exact(cid, flags):
     cfg, tables, batch, _ = make_problem(cid)
     h = tbe.tbe_create(tables, cfg.pooling, flags)
@@ -72,9 +72,10 @@ def test_prepare_sort_and_rle_bit_exact(cid, flags):
 
     U = int(view(lay.num_unique, 1)[0])
     keys, bag = oracle.make_keys([t.shape[0] for t in tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
-    # with TBE_FLAG_DENSE_BACKWARD the histogram tables' lookups are not
-    # sorted: only the other tables' keys (their positions in ascending order)
-    dense = np.array([p == "histogram" and bool(flags & tbe.TBE_FLAG_DENSE_BACKWARD)
+    # the histogram tables' lookups take the dense backward unless
+    # TBE_FLAG_SORTED_BACKWARD: only the other tables' keys are sorted (their
+    # positions in ascending order)
+    dense = np.array([p == "histogram" and not (flags & tbe.TBE_FLAG_SORTED_BACKWARD)
                       for p in tbe.tbe_table_paths(h)])
     keep = np.flatnonzero(~dense[bag // cfg.B])
     ref = oracle.sort_rle(keys[keep])
@@ -90,7 +91,7 @@ def test_prepare_sort_and_rle_bit_exact(cid, flags):
 
 
 @pytest.mark.parametrize("index_dtype,flags", [(torch.int64, 0), (torch.int32, 0),
-                                               (torch.int64, tbe.TBE_FLAG_DENSE_BACKWARD)])
+                                               (torch.int64, tbe.TBE_FLAG_SORTED_BACKWARD)])
 @pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
 def test_backward_matches_oracle(cid, index_dtype, flags):
     cfg, tables, batch, grad = make_problem(cid, index_dtype)
