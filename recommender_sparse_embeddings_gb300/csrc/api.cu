@@ -381,9 +381,9 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         h->dense_floats = goff.back();
         h->dense_rows = roff.back();
         if (h->n_dense > 0) {
-            // rows per CTA: 128-row tiles whose accumulators (dim columns
-            // each) fit the 512 tensor-memory columns, at most four
-            const int mt = std::min(4, 512 / h->dense_max_dim);
+            // rows per CTA: 128-row tiles whose two accumulators (dim
+            // columns each) fit the 512 tensor-memory columns, at most four
+            const int mt = dense_mtiles(h->dense_max_dim);
             h->dense_groups = (h->dense_max_rows + mt * 128 - 1) / (mt * 128);
         }
         dense_off = goff;

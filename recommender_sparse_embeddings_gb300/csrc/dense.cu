@@ -8,25 +8,35 @@
 // gradient.  Its lookups need no sort:
 //
 //  dense_mma_kernel: a CTA owns (table, up to four 128-row M tiles, one of S
-//    consecutive bag ranges).  For every 32 bags it builds H^T (rows x bags)
-//    and G_t (columns x bags) in shared memory in the no-swizzle K-major
-//    core-matrix layout and issues tcgen05.mma (kind::f16, bf16 operands,
-//    fp32 accumulator in tensor memory, M = 128, N = dim, K = 16).  For fp32
-//    accuracy both operands are split into three bf16 terms,
-//    x = x0 + x1 + x2 (24 significant bits), and the six products with
-//    i + j <= 2 are accumulated.  H^T is built without races: warp w owns
-//    bags w and w + 16 of the tile and walks their lookups in order,
-//    merging
-//    repeated rows (ballot match) so every entry has one writer; results
-//    do not depend on scheduling.  Every kDenseFlush bag tiles, and after its
-//    last one, the CTA reads the accumulator back (tcgen05.ld) and adds it to
-//    its own slice of the gradient buffer (fp32, fixed order), then restarts
-//    the accumulator; at the end it adds its lookup counts per row (integer
+//    consecutive bag ranges) and walks its bags 32 at a time.  Per tile:
+//     - every thread takes lookups of the tile by position, finds its bag
+//       (a shuffle search over the tile's bag offsets) and adds its scale to
+//       an fp32 histogram in shared memory (shared-memory atomics; a bag's
+//       lookups are spread over the CTA's threads);
+//     - the touched histogram entries are split into three bf16 terms
+//       x = x0 + x1 + x2 (24 significant bits) and written into H^T (rows x
+//       bags, no-swizzle K-major core matrices); G_t (columns x bags) is
+//       split the same way;
+//     - one thread issues tcgen05.mma (kind::f16, bf16 operands, fp32
+//       accumulator in tensor memory, M = 128, N = dim, K = 16) for the six
+//       products x_i y_j with i + j <= 2, and commits to an mbarrier.
+//    While the tensor cores run, the threads clear the histogram entries
+//    they touched and build the next tile's histogram and G_t (G_t is
+//    double-buffered); after the MMAs, only the touched H^T entries are
+//    cleared.  Every kDensePromote tiles the tensor-memory accumulator is
+//    added (fp32, round to nearest) into a second tensor-memory sum and
+//    restarted, so the tensor cores' own accumulation rounds against a small
+//    partial sum.  At the end the CTA stores that sum into its own slice of
+//    the gradient buffer and adds its lookup counts per row (integer
 //    atomics).
 //  dense_update_kernel: one warp per row of every dense table; a row that
 //    some lookup touched adds its S partial sums in order, gets its optimizer
 //    step (the same SGD / row-wise Adagrad arithmetic as the sorted path) and
 //    is stored once.
+//
+// Repeated lookups of one row in one bag meet in a shared-memory fp32
+// atomic; their order (and so the last bit of such an entry when the scales
+// are not integers) may vary from run to run.
 #include "tbe_internal.cuh"
 #include "tcgen05.cuh"
 
@@ -37,11 +47,9 @@ constexpr int kDenseWarps = kDenseThreads / 32;
 constexpr int kDenseKT = 32;      // bags per tile (two MMA K steps)
 constexpr int kDenseSplit = 3;    // bf16 terms per operand
 constexpr int kDenseMaxMp = 512;  // rows per CTA (four 128-row M tiles)
-// Bag tiles summed in tensor memory before the partial sum is added to the
-// CTA's gradient slice in fp32 (round to nearest).  The tensor cores' own
-// accumulation rounds each step against the magnitude of the running sum;
-// restarting it every few tiles keeps that sum, and so the error, small.
-constexpr int kDenseFlush = 32;
+constexpr int kDenseLk = 4;       // lookups per thread per tile remembered for the sparse clears
+constexpr int kDensePromote = 4;  // tiles summed in the tensor-memory accumulator before it is restarted
+constexpr uint32_t kNoEntry = 0xffffffffu;
 
 // bf16 bits of x rounded to nearest even, and the value they stand for.
 __device__ __forceinline__ uint16_t to_bf16(float x, float& back) {
@@ -60,32 +68,45 @@ __device__ __forceinline__ void split3(float x, uint16_t (&t)[kDenseSplit]) {
     t[2] = to_bf16(x, b);
 }
 
-__device__ __forceinline__ float bf16_value(uint16_t bits) { return __uint_as_float((uint32_t)bits << 16); }
-
-// Shared-memory plan of one CTA for Mp rows and dim D (bytes).
+// Shared-memory plan of one CTA for Mp rows and dim D (bytes): H^T terms,
+// two buffers of G_t terms, the fp32 histogram, the row counts.
 __host__ __device__ inline size_t dense_a_bytes(int Mp) { return (size_t)Mp * kDenseKT * 2; }
 __host__ __device__ inline size_t dense_b_bytes(int D) { return (size_t)D * kDenseKT * 2; }
 __host__ __device__ inline size_t dense_smem_bytes(int Mp, int D) {
-    return kDenseSplit * (dense_a_bytes(Mp) + dense_b_bytes(D)) + sizeof(uint32_t) * (size_t)Mp;
-}
-
-// 128-row M tiles per CTA for dim D: the accumulator takes D tensor-memory
-// columns per tile, 512 columns in all.
-__host__ __device__ inline int dense_mtiles(int D) {
-    const int by_tmem = 512 / D;
-    return by_tmem < kDenseMaxMp / 128 ? by_tmem : kDenseMaxMp / 128;
+    return kDenseSplit * dense_a_bytes(Mp) + 2 * kDenseSplit * dense_b_bytes(D) +
+           sizeof(float) * (size_t)Mp * kDenseKT + sizeof(uint32_t) * (size_t)Mp;
 }
 
 __host__ __device__ inline uint32_t dense_tmem_cols(int n) {
     return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
 }
 
+// Histogram entry (m, j): row-major [Mp][32] with the bag index swizzled by
+// the row, so the lanes of a warp (mostly one bag, many rows) hit different
+// banks.
+__device__ __forceinline__ uint32_t hf_index(uint32_t m, uint32_t j) { return m * kDenseKT + (j ^ (m & 31u)); }
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a, Workspace ws, int groups_max) {
     extern __shared__ __align__(1024) unsigned char dsm[];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     constexpr int kMaxMma = (kDenseMaxMp / 128) * (kDenseKT / 16) * 6;
-    __shared__ uint64_t s_adesc[kMaxMma], s_bdesc[kMaxMma];
+    __shared__ uint64_t s_adesc[kMaxMma], s_bdesc[2][kMaxMma];
     __shared__ uint32_t s_dcol[kMaxMma];
     __shared__ bool s_init[kMaxMma];
     const int splits = a.splits;
@@ -105,23 +126,31 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     unsigned char* As = dsm;                                    // [split][Mp x KT] bf16
-    unsigned char* Bs = dsm + kDenseSplit * dense_a_bytes(Mp);  // [split][D x KT] bf16
-    uint32_t* s_cnt = reinterpret_cast<uint32_t*>(Bs + kDenseSplit * dense_b_bytes(D));  // [Mp]
+    unsigned char* Bs = dsm + kDenseSplit * dense_a_bytes(Mp);  // [buffer][split][D x KT] bf16
+    float* Hf = reinterpret_cast<float*>(Bs + 2 * kDenseSplit * dense_b_bytes(D));  // [Mp][KT] fp32
+    uint32_t* s_cnt = reinterpret_cast<uint32_t*>(Hf + (size_t)Mp * kDenseKT);     // [Mp]
     const uint32_t sbo = (uint32_t)(kDenseKT / 8) * 128u;  // bytes per 8 rows (K-major core matrices)
 
     // bag range of this part
     const int bk0 = (int)(((int64_t)a.B * sp) / splits);
     const int bk1 = (int)(((int64_t)a.B * (sp + 1)) / splits);
+    const int ntiles = (bk1 - bk0 + kDenseKT - 1) / kDenseKT;
     const uint32_t* boff = ws.dboff + (int64_t)td.dslot * (a.B + 1);
     const bool has_scale = ws.counters[CTR_HAS_SCALE] != 0;
-    const bool gvec = a.grad_vec && td.doff % 4 == 0;
-    const uint32_t ncols = dense_tmem_cols(mtiles * D);
+    const uint32_t ncols = dense_tmem_cols(2 * mtiles * D);  // short and long accumulators
+    const uint32_t long0 = (uint32_t)(mtiles * D);           // first column of the long one
     if (warp == 0) tmem_alloc(&s_tmem, ncols);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = tid; i < Mp; i += kDenseThreads) s_cnt[i] = 0;
+    {
+        uint4* pa = reinterpret_cast<uint4*>(As);
+        const int n16 = (int)(kDenseSplit * dense_a_bytes(Mp) / 16);
+        for (int i = tid; i < n16; i += kDenseThreads) pa[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < Mp * kDenseKT; i += kDenseThreads) Hf[i] = 0.f;
+        for (int i = tid; i < Mp; i += kDenseThreads) s_cnt[i] = 0;
+    }
     tcgen05_before_sync();
     __syncthreads();
     tcgen05_after_sync();
@@ -136,183 +165,191 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         const int pr = tid % 6, ks = (tid / 6) % (kDenseKT / 16), i = tid / (6 * (kDenseKT / 16));
         const int pa = (0x910 >> (2 * pr)) & 3, pb = (0x184 >> (2 * pr)) & 3;
         const uint32_t ad = abase + (uint32_t)(pa * dense_a_bytes(Mp)) + (uint32_t)(i * 16) * sbo + 256u * ks;
-        const uint32_t bd = bbase + (uint32_t)(pb * dense_b_bytes(D)) + 256u * ks;
         s_adesc[tid] = smem_desc(ad, 128u, sbo);
-        s_bdesc[tid] = smem_desc(bd, 128u, sbo);
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+            const uint32_t bd = bbase + (uint32_t)((bb * kDenseSplit + pb) * dense_b_bytes(D)) + 256u * ks;
+            s_bdesc[bb][tid] = smem_desc(bd, 128u, sbo);
+        }
         s_dcol[tid] = (uint32_t)(i * D);
         s_init[tid] = ks == 0 && pr == 0;  // the first MMA of each M tile starts the sum
     }
     __syncthreads();
+
+    // A tile's inputs, loaded into registers one tile ahead so their latency
+    // hides behind the previous tile's work: the bag offsets (lane l: first
+    // lookup of bag l), the row and scale of this thread's lookups
+    // q0 + tid + 512*kk, and the gradient values of its G_t items (a warp
+    // item covers 8 columns x 8 bags; lane: column c0 + lane%8, bags
+    // 2*(lane/8) and +1, so each split term is one 4-byte store and a warp's
+    // stores fill distinct banks).
+    constexpr int kGItems = 4;  // G_t items per warp held in registers (dim <= 128; dim 256 loads the rest in place)
+    struct TileIn {
+        int b0, nb;
+        uint32_t q0, qend, ol;
+        int r[kDenseLk];
+        float s[kDenseLk];
+        float g[2 * kGItems];
+    };
+    const int bitems = (D / 8) * (kDenseKT / 8);
+    auto g_item = [&](const TileIn& in, int it, float& g0, float& g1) {
+        const int c = (it % (D / 8)) * 8 + (lane & 7);
+        const int j = (it / (D / 8)) * 8 + (lane >> 3) * 2;
+        const float* gp = a.grad + (int64_t)(in.b0 + j) * a.total_d + td.doff + c;
+        g0 = j < in.nb ? __ldg(gp) : 0.f;
+        g1 = j + 1 < in.nb ? __ldg(gp + a.total_d) : 0.f;
+    };
+    auto load_offsets = [&](int b0, TileIn& in) {
+        in.b0 = b0;
+        in.nb = tmin<int>(kDenseKT, bk1 - b0);
+        in.q0 = __ldg(boff + b0);
+        in.qend = __ldg(boff + b0 + in.nb);
+        in.ol = __ldg(boff + b0 + tmin<int>(lane, in.nb));
+    };
+    auto load_inputs = [&](TileIn& in) {  // after load_offsets
+#pragma unroll
+        for (int kk = 0; kk < kDenseLk; ++kk) {
+            const uint32_t q = in.q0 + (uint32_t)(tid + kk * kDenseThreads);
+            in.r[kk] = 0xffff;
+            in.s[kk] = 0.f;
+            if (q < in.qend) {
+                in.r[kk] = __ldg(ws.hrow + q);
+                in.s[kk] = has_scale ? __ldg(ws.scale + q) : 1.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGItems; ++i) {
+            const int it = warp + i * kDenseWarps;
+            in.g[2 * i] = in.g[2 * i + 1] = 0.f;
+            if (it < bitems) g_item(in, it, in.g[2 * i], in.g[2 * i + 1]);
+        }
+    };
+    auto put_b = [&](int it, int bb, float g0, float g1) {
+        uint16_t t0[kDenseSplit], t1[kDenseSplit];
+        split3(g0, t0);
+        split3(g1, t1);
+        const uint32_t off = core_off((it % (D / 8)) * 8 + (lane & 7), (it / (D / 8)) * 8 + (lane >> 3) * 2, sbo);
+#pragma unroll
+        for (int si = 0; si < kDenseSplit; ++si)
+            *reinterpret_cast<uint32_t*>(Bs + (bb * kDenseSplit + si) * dense_b_bytes(D) + off) =
+                (uint32_t)t0[si] | ((uint32_t)t1[si] << 16);
+    };
+    auto build_b = [&](const TileIn& in, int bb) {
+#pragma unroll
+        for (int i = 0; i < kGItems; ++i) {
+            const int it = warp + i * kDenseWarps;
+            if (it < bitems) put_b(it, bb, in.g[2 * i], in.g[2 * i + 1]);
+        }
+        for (int it = warp + kGItems * kDenseWarps; it < bitems; it += kDenseWarps) {
+            float g0, g1;
+            g_item(in, it, g0, g1);
+            put_b(it, bb, g0, g1);
+        }
+    };
+
+    // Histogram of a tile: the lookups of `in` (remembered in ent[kk]); the
+    // rest (tiles of more than 2048 lookups) marks the tile `full`, whose
+    // clears then cover whole arrays.
+    auto accumulate = [&](const TileIn& in, uint32_t(&ent)[kDenseLk], bool& full) {
+        full = in.qend - in.q0 > (uint32_t)(kDenseThreads * kDenseLk);
+        auto one = [&](uint32_t q, int r, float sc) -> uint32_t {
+            // bag of q: the last j < nb with first lookup <= q (whole warp)
+            int j = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const uint32_t v = __shfl_sync(0xffffffffu, in.ol, j + step);
+                if (j + step < in.nb && v <= q) j += step;
+            }
+            const int m = r - row0;
+            if (q < in.qend && r < R && m >= 0 && m < Mp) {
+                atomicAdd(&Hf[hf_index((uint32_t)m, (uint32_t)j)], sc);
+                atomicAdd(&s_cnt[m], 1u);
+                return ((uint32_t)m << 5) | (uint32_t)j;
+            }
+            return kNoEntry;
+        };
+#pragma unroll
+        for (int kk = 0; kk < kDenseLk; ++kk)
+            ent[kk] = one(in.q0 + (uint32_t)(tid + kk * kDenseThreads), in.r[kk], in.s[kk]);
+        if (full) {
+            for (uint32_t base = in.q0 + kDenseThreads * kDenseLk; base < in.qend; base += kDenseThreads) {
+                const uint32_t q = base + (uint32_t)tid;
+                int r = 0xffff;
+                float sc = 0.f;
+                if (q < in.qend) {
+                    r = __ldg(ws.hrow + q);
+                    sc = has_scale ? __ldg(ws.scale + q) : 1.f;
+                }
+                (void)one(q, r, sc);
+            }
+        }
+    };
+
     uint32_t phase = 0;
-    bool first = true, timed_out = false, written = false;
-    int in_acc = 0;  // bag tiles in the accumulator since the last flush
-    float* dg = ws.dgrad + (size_t)sp * a.total_floats + a.goff[k];
+    bool first = true, promoted = false, timed_out = false;
     const int lg = warp & 3;  // warp w reads tensor-memory lanes 32*(w%4) .. +31
-    // accumulator (or zeros, when it holds no tile) -> this part's gradient
-    // slice: stored by the first flush, added by the later ones
-    auto flush = [&]() {
-        for (int i = 0; i < mtiles; ++i) {
-            const int r = row0 + i * 128 + lg * 32 + lane;
+    const uint32_t tlane = tmem + ((uint32_t)(lg * 32) << 16);
+    // short accumulator (+ long sum so far) -> long sum; the short one restarts
+    auto promote = [&]() {
+        for (int i = 0; i < mtiles; ++i)
             for (int c = (warp >> 2) * 16; c < D; c += (kDenseWarps / 4) * 16) {
                 float v[16];
-                if (!first) {
-                    tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(i * D + c), v);  // whole warp
-                } else {
+                tmem_ld16(tlane + (uint32_t)(i * D + c), v);
+                if (promoted) {
+                    float u[16];
+                    tmem_ld16(tlane + long0 + (uint32_t)(i * D + c), u);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                    for (int q = 0; q < 16; ++q) v[q] += u[q];
                 }
-                if (r < R) {
-                    float4* dst = reinterpret_cast<float4*>(dg + (int64_t)r * D + c);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                        if (written) {
-                            const float4 p = dst[q];
-                            o.x = p.x + o.x;
-                            o.y = p.y + o.y;
-                            o.z = p.z + o.z;
-                            o.w = p.w + o.w;
-                        }
-                        dst[q] = o;
-                    }
-                }
+                tmem_st16(tlane + long0 + (uint32_t)(i * D + c), v);
             }
-        }
-        written = true;
-        first = true;  // the next tile's first MMAs overwrite the accumulator
-        in_acc = 0;
+        tmem_st_wait();
+        promoted = true;
+        first = true;
     };
 
-    // Registers holding the next tile's inputs, loaded while the previous
-    // tile's MMAs run: gradient vectors (element e = tid + 512*q of the
-    // tile's KT x D/4 float4 grid) and, per owned bag, its lookup range and
-    // first 32 lookups.
-    constexpr int kBagsPerWarp = kDenseKT / kDenseWarps;
-    constexpr int kGPre = 2;  // prefetched: dim <= 128 (the rest of a dim-256 tile loads in place)
-    float4 gpre[kGPre];
-    uint32_t bp[kBagsPerWarp], bq[kBagsPerWarp];
-    int rpre[kBagsPerWarp];
-    float spre[kBagsPerWarp];
-    auto prefetch = [&](int b0) {
-        const int nb = tmin<int>(kDenseKT, bk1 - b0);
+    uint32_t cur[kDenseLk], nxt[kDenseLk];
+    bool full_cur = false, full_nxt = false;
 #pragma unroll
-        for (int q = 0; q < kGPre; ++q) {
-            const int e = tid + q * kDenseThreads;
-            const int j = e / (D / 4), c4 = (e % (D / 4)) * 4;
-            gpre[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < kDenseKT * (D / 4) && j < nb) {
-                const float* gp = a.grad + (int64_t)(b0 + j) * a.total_d + td.doff + c4;
-                if (gvec) {
-                    gpre[q] = __ldg(reinterpret_cast<const float4*>(gp));
-                } else {
-                    gpre[q].x = __ldg(gp);
-                    gpre[q].y = __ldg(gp + 1);
-                    gpre[q].z = __ldg(gp + 2);
-                    gpre[q].w = __ldg(gp + 3);
-                }
-            }
+    for (int kk = 0; kk < kDenseLk; ++kk) cur[kk] = nxt[kk] = kNoEntry;
+    TileIn pf;  // inputs of the next tile to accumulate
+    if (ntiles > 0) {
+        load_offsets(bk0, pf);
+        load_inputs(pf);
+        build_b(pf, 0);
+        accumulate(pf, cur, full_cur);
+        if (ntiles > 1) {
+            load_offsets(bk0 + kDenseKT, pf);
+            load_inputs(pf);
         }
+    }
+    for (int kt = 0; kt < ntiles; ++kt) {
+        const int buf = kt & 1;
+        __syncthreads();  // histogram and G_t of this tile complete; last tile's H^T cleared
+        // touched histogram entries -> H^T terms (repeated entries write equal values)
+        if (!full_cur) {
 #pragma unroll
-        for (int h = 0; h < kBagsPerWarp; ++h) {
-            const int j = warp + h * kDenseWarps;
-            bp[h] = bq[h] = 0;
-            rpre[h] = 0xffff;
-            spre[h] = 0.f;
-            if (j < nb) {
-                bp[h] = __ldg(boff + b0 + j);
-                bq[h] = tmax<uint32_t>(__ldg(boff + b0 + j + 1), bp[h]);
-                const uint32_t p = bp[h] + lane;
-                if (p < bq[h]) {
-                    rpre[h] = __ldg(ws.hrow + p);
-                    spre[h] = has_scale ? __ldg(ws.scale + p) : 1.f;
-                }
-            }
-        }
-    };
-    if (bk0 < bk1) prefetch(bk0);
-
-    for (int b0 = bk0; b0 < bk1; b0 += kDenseKT) {
-        // clear A (all terms)
-        {
-            uint4* pa = reinterpret_cast<uint4*>(As);
-            const int n16 = (int)(kDenseSplit * dense_a_bytes(Mp) / 16);
-            for (int i = tid; i < n16; i += kDenseThreads) pa[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        // B from the prefetched gradient vectors (bags past the range are
-        // zeros); element (n = column, k = bag)
-        const int nb = tmin<int>(kDenseKT, bk1 - b0);
-#pragma unroll
-        for (int q = 0; q < kDenseKT * 256 / 4 / kDenseThreads; ++q) {  // dim <= 256
-            const int e = tid + q * kDenseThreads;
-            if (e >= kDenseKT * (D / 4)) continue;
-            const int j = e / (D / 4), c4 = (e % (D / 4)) * 4;
-            float4 gv4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (q < kGPre) {
-                gv4 = gpre[q];
-            } else if (j < nb) {
-                const float* gp = a.grad + (int64_t)(b0 + j) * a.total_d + td.doff + c4;
-                gv4 = make_float4(__ldg(gp), __ldg(gp + 1), __ldg(gp + 2), __ldg(gp + 3));
-            }
-            const float f[4] = {gv4.x, gv4.y, gv4.z, gv4.w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int kk = 0; kk < kDenseLk; ++kk) {
+                if (cur[kk] == kNoEntry) continue;
+                const uint32_t m = cur[kk] >> 5, j = cur[kk] & 31u;
                 uint16_t tt[kDenseSplit];
-                split3(f[c], tt);
+                split3(Hf[hf_index(m, j)], tt);
+                const uint32_t off = core_off((int)m, (int)j, sbo);
 #pragma unroll
                 for (int si = 0; si < kDenseSplit; ++si)
-                    *reinterpret_cast<uint16_t*>(Bs + si * dense_b_bytes(D) + core_off(c4 + c, j, sbo)) = tt[si];
+                    *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + off) = tt[si];
             }
-        }
-        __syncthreads();  // A cleared before the histogram is written
-        // H^T: warp w owns bags w and w + 16 of the tile; lookups in order,
-        // repeated rows merged so each entry has one writer
+        } else {
+            for (int e = tid; e < Mp * kDenseKT; e += kDenseThreads) {
+                const uint32_t m = (uint32_t)e / kDenseKT, j = (uint32_t)e % kDenseKT;
+                const float v = Hf[hf_index(m, j)];
+                if (v == 0.f) continue;
+                uint16_t tt[kDenseSplit];
+                split3(v, tt);
+                const uint32_t off = core_off((int)m, (int)j, sbo);
 #pragma unroll
-        for (int h = 0; h < kBagsPerWarp; ++h) {
-            const int j = warp + h * kDenseWarps;
-            for (uint32_t x = bp[h]; x < bq[h]; x += 32) {
-                int r;
-                float sc;
-                if (x == bp[h]) {  // the prefetched first 32 lookups
-                    r = rpre[h];
-                    sc = spre[h];
-                } else {
-                    const uint32_t p = x + lane;
-                    r = 0xffff;
-                    sc = 0.f;
-                    if (p < bq[h]) {
-                        r = __ldg(ws.hrow + p);
-                        sc = has_scale ? __ldg(ws.scale + p) : 1.f;
-                    }
-                }
-                const int m = r - row0;
-                const bool mine = r < R && m >= 0 && m < Mp;
-                const uint32_t lab = mine ? (uint32_t)m : 2047u;  // rows of other groups / skipped: one label
-                const uint32_t peers = match_label<11>(lab);
-                // the group's scales, added in lane order (groups of one: the scale)
-                float tot = sc;
-                if (__any_sync(0xffffffffu, mine && __popc(peers) > 1)) {
-                    tot = 0.f;
-                    for (int l = 0; l < 32; ++l) {
-                        const float v = __shfl_sync(0xffffffffu, sc, l);
-                        if ((peers >> l) & 1u) tot += v;
-                    }
-                }
-                if (mine && (peers & ((1u << lane) - 1u)) == 0) {
-                    // entry (m, j): value so far (earlier lookups of the bag) + tot
-                    float prev = 0.f;
-                    uint16_t tt[kDenseSplit];
-                    if (x != bp[h]) {
-#pragma unroll
-                        for (int si = 0; si < kDenseSplit; ++si)
-                            prev += bf16_value(
-                                *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + core_off(m, j, sbo)));
-                    }
-                    split3(prev + tot, tt);
-#pragma unroll
-                    for (int si = 0; si < kDenseSplit; ++si)
-                        *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + core_off(m, j, sbo)) = tt[si];
-                    atomicAdd(&s_cnt[m], (uint32_t)__popc(peers));
-                }
+                for (int si = 0; si < kDenseSplit; ++si)
+                    *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + off) = tt[si];
             }
         }
         fence_proxy_async_smem();  // generic-proxy writes of A and B -> tensor cores
@@ -321,12 +358,26 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         tcgen05_after_sync();
         if (tid == 0) {
             for (int q = 0; q < nmma; ++q)
-                mma_f16(tmem + s_dcol[q], s_adesc[q], s_bdesc[q], idesc, (first && s_init[q]) ? 0u : 1u);
+                mma_f16(tmem + s_dcol[q], s_adesc[q], s_bdesc[buf][q], idesc, (first && s_init[q]) ? 0u : 1u);
             mma_commit(&s_bar);
         }
         first = false;
-        // the next tile's inputs load while the MMAs run
-        if (b0 + kDenseKT < bk1) prefetch(b0 + kDenseKT);
+        // while the MMAs run: clear this tile's histogram entries, then build
+        // the next tile's histogram and G_t from the prefetched inputs
+        if (!full_cur) {
+#pragma unroll
+            for (int kk = 0; kk < kDenseLk; ++kk)
+                if (cur[kk] != kNoEntry) Hf[hf_index(cur[kk] >> 5, cur[kk] & 31u)] = 0.f;
+        } else {
+            for (int i = tid; i < Mp * kDenseKT; i += kDenseThreads) Hf[i] = 0.f;
+        }
+        __syncthreads();  // histogram clear before the next tile's additions
+        const bool more = kt + 1 < ntiles;
+        if (more) {
+            build_b(pf, buf ^ 1);
+            accumulate(pf, nxt, full_nxt);
+            if (kt + 2 < ntiles) load_offsets(bk0 + (kt + 2) * kDenseKT, pf);  // in flight during the wait
+        }
         // every thread waits; the block agrees on the outcome
         const bool ok = mbar_wait(&s_bar, phase);
         if (__syncthreads_or(!ok)) {
@@ -335,12 +386,51 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         }
         phase ^= 1u;
         tcgen05_after_sync();
-        // each thread reads and writes only its own accumulator rows and
-        // columns, and the sync before the next MMAs orders the reads first
-        if (++in_acc == kDenseFlush || b0 + kDenseKT >= bk1) flush();
+        if (more && kt + 2 < ntiles) load_inputs(pf);  // the tile after next: in flight from here on
+        // the MMAs have read H^T: clear what this tile wrote
+        if (!full_cur) {
+#pragma unroll
+            for (int kk = 0; kk < kDenseLk; ++kk) {
+                if (cur[kk] == kNoEntry) continue;
+                const uint32_t off = core_off((int)(cur[kk] >> 5), (int)(cur[kk] & 31u), sbo);
+#pragma unroll
+                for (int si = 0; si < kDenseSplit; ++si)
+                    *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + off) = 0;
+            }
+        } else {
+            uint4* pa = reinterpret_cast<uint4*>(As);
+            const int n16 = (int)(kDenseSplit * dense_a_bytes(Mp) / 16);
+            for (int i = tid; i < n16; i += kDenseThreads) pa[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        // each thread reads and writes only its own accumulator lanes and
+        // columns; the syncs before the next MMAs order this before them
+        if ((kt + 1) % kDensePromote == 0 || kt + 1 == ntiles) promote();
+#pragma unroll
+        for (int kk = 0; kk < kDenseLk; ++kk) cur[kk] = nxt[kk];
+        full_cur = full_nxt;
     }
     if (!timed_out) {
-        if (!written) flush();  // a part with no bags stores zeros
+        // long sum (zeros if the part had no bags) -> this part's gradient slice
+        float* dg = ws.dgrad + (size_t)sp * a.total_floats + a.goff[k];
+        for (int i = 0; i < mtiles; ++i) {
+            const int r = row0 + i * 128 + lg * 32 + lane;
+            for (int c = (warp >> 2) * 16; c < D; c += (kDenseWarps / 4) * 16) {
+                float v[16];
+                if (promoted) {
+                    tmem_ld16(tlane + long0 + (uint32_t)(i * D + c), v);  // whole warp
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                }
+                if (r < R) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<float4*>(dg + (int64_t)r * D + c)[q] =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+        }
+        __syncthreads();  // all row counts in
         uint32_t* dc = ws.dcount + a.roff[k] + row0;
         for (int i = tid; i < rows_here; i += kDenseThreads)
             if (s_cnt[i]) atomicAdd(dc + i, s_cnt[i]);

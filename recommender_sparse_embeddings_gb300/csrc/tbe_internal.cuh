@@ -306,6 +306,13 @@ struct DenseArgs {
 };
 cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s);
 
+// 128-row M tiles per dense-backward CTA for dim D: the short and the long
+// accumulator take D tensor-memory columns per tile each, 512 columns in all.
+__host__ __device__ inline int dense_mtiles(int D) {
+    const int by_tmem = 256 / D;
+    return by_tmem < 4 ? (by_tmem < 1 ? 1 : by_tmem) : 4;
+}
+
 // Streams the backward class kernels are spread over: each class kernel
 // takes its work from its own counter, so they may run side by side and one
 // class's tail overlaps the next class's work.

@@ -122,11 +122,11 @@ def _multi_table_batch(specs, B, max_len, seed, oob_table=None):
 
 
 def _dense_case(specs, B, pooling, weighted, optimizer, flags=0, seed=0, oob_table=None,
-                applies=1):
+                applies=1, max_len=70):
     from helpers import DT_NAME, table_bits, touched_rows, assert_tables_match
     g = torch.Generator().manual_seed(seed)
     tables = [(torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV) for r, d, dt in specs]
-    ind, off = _multi_table_batch(specs, B, 70, seed=seed + 11, oob_table=oob_table)
+    ind, off = _multi_table_batch(specs, B, max_len, seed=seed + 11, oob_table=oob_table)
     w = torch.rand(ind.numel(), generator=g) if weighted else None
     grad = torch.randn((B, sum(d for _, d, _ in specs)), generator=g)
     before = [table_bits(t) for t in tables]
@@ -172,6 +172,14 @@ def test_dense_backward_sgd_matches_oracle(dtype, rows, dim, pooling, weighted):
 def test_dense_backward_rowwise_adagrad_matches_oracle(dtype, rows, dim):
     specs = [(700, 64, torch.bfloat16), (rows, dim, dtype), (rows, dim, torch.float16)]
     _dense_case(specs, 257, "mean", True, "adagrad", seed=rows * 3 + dim)
+
+
+@pytest.mark.parametrize("rows,dim", [(512, 64), (200, 128)])
+def test_dense_backward_tiles_of_more_than_2048_lookups(rows, dim):
+    """Bags of up to 250 lookups: most 32-bag tiles hold more lookups than the
+    per-thread lists cover, so they take the whole-array clears."""
+    specs = [(rows, dim, torch.float16), (900, 32, torch.float32)]
+    _dense_case(specs, 96, "sum", True, "sgd", seed=rows + 5, max_len=250)
 
 
 def test_dense_backward_only_dense_tables():
