@@ -205,16 +205,18 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- profile
 
-def profile_traffic(segment: str):
-    """DRAM bytes per launch of a segment's main kernel, from the committed ncu
-    summary, or None if there is none or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{segment}.md")
+def profile_traffic(segment: str, cfg_id: int, T: int):
+    """DRAM bytes per launch of a call's main kernel on this workload, from the
+    committed ncu summary, or None if there is none (for this workload and
+    table count) or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{segment}_w{cfg_id}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    if not m or not h:
+    t = re.search(r"tables:\s*([0-9]+)", text)
+    if not m or not h or not t or int(t.group(1)) != T:
         return None
     src = os.path.join(ROOT, KERNEL_FILES[segment])
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
@@ -539,7 +541,7 @@ def run_ours(args):
             "breakdown_ms_sequential": brk,
             "algorithmic_bytes": nbytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profile_traffic(dominant),
+                         "frac": achieved / peak, "traffic": profile_traffic(dominant, cfg.cfg_id, T),
                          "kernel": DOMINANT_KERNELS[dominant], "call": dominant,
                          "ms_per_launch": call_ms[dominant], "bytes_per_launch": nbytes[dominant],
                          "timing": timing_src, "peak_source": peak_src,

@@ -20,10 +20,10 @@
 //     - one thread issues tcgen05.mma (kind::f16, bf16 operands, fp32
 //       accumulator in tensor memory, M = 128, N = dim, K = 16) for the six
 //       products x_i y_j with i + j <= 2, and commits to an mbarrier.
-//    While the tensor cores run, the threads clear the histogram entries
-//    they touched and build the next tile's histogram and G_t (G_t is
-//    double-buffered); after the MMAs, only the touched H^T entries are
-//    cleared.  Every kDensePromote tiles the tensor-memory accumulator is
+//    Reading a histogram entry for H^T clears it (atomic exchange).  While
+//    the tensor cores run, the threads build the next tile's histogram and
+//    G_t (G_t is double-buffered); after the MMAs, only the touched H^T
+//    entries are cleared.  Every kDensePromote tiles the tensor-memory accumulator is
 //    added (fp32, round to nearest) into a second tensor-memory sum and
 //    restarted, so the tensor cores' own accumulation rounds against a small
 //    partial sum.  At the end the CTA stores that sum into its own slice of
@@ -46,7 +46,6 @@ constexpr int kDenseThreads = 512;
 constexpr int kDenseWarps = kDenseThreads / 32;
 constexpr int kDenseKT = 32;      // bags per tile (two MMA K steps)
 constexpr int kDenseSplit = 3;    // bf16 terms per operand
-constexpr int kDenseMaxMp = 512;  // rows per CTA (four 128-row M tiles)
 constexpr int kDenseLk = 4;       // lookups per thread per tile remembered for the sparse clears
 constexpr int kDensePromote = 4;  // tiles summed in the tensor-memory accumulator before it is restarted
 constexpr uint32_t kNoEntry = 0xffffffffu;
@@ -105,10 +104,6 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     extern __shared__ __align__(1024) unsigned char dsm[];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
-    constexpr int kMaxMma = (kDenseMaxMp / 128) * (kDenseKT / 16) * 6;
-    __shared__ uint64_t s_adesc[kMaxMma], s_bdesc[2][kMaxMma];
-    __shared__ uint32_t s_dcol[kMaxMma];
-    __shared__ bool s_init[kMaxMma];
     const int splits = a.splits;
     const int per_table = groups_max * splits;
     const int k = blockIdx.x / per_table;
@@ -157,23 +152,15 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     const uint32_t tmem = s_tmem;
     const uint32_t idesc = mma_idesc(1, 128, D);  // bf16 x bf16 -> fp32
     const uint32_t abase = smem_u32(As), bbase = smem_u32(Bs);
-    // the tile's MMAs: the six products x_i * y_j with i + j <= 2 for every
-    // M tile and both K steps (descriptors are the same for every tile)
-    const int nmma = mtiles * (kDenseKT / 16) * 6;
-    if (tid < nmma) {
-        // product pr: terms (pa, pb) = (0,0) (0,1) (1,0) (0,2) (1,1) (2,0), two bits each
-        const int pr = tid % 6, ks = (tid / 6) % (kDenseKT / 16), i = tid / (6 * (kDenseKT / 16));
-        const int pa = (0x910 >> (2 * pr)) & 3, pb = (0x184 >> (2 * pr)) & 3;
-        const uint32_t ad = abase + (uint32_t)(pa * dense_a_bytes(Mp)) + (uint32_t)(i * 16) * sbo + 256u * ks;
-        s_adesc[tid] = smem_desc(ad, 128u, sbo);
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-            const uint32_t bd = bbase + (uint32_t)((bb * kDenseSplit + pb) * dense_b_bytes(D)) + 256u * ks;
-            s_bdesc[bb][tid] = smem_desc(bd, 128u, sbo);
-        }
-        s_dcol[tid] = (uint32_t)(i * D);
-        s_init[tid] = ks == 0 && pr == 0;  // the first MMA of each M tile starts the sum
-    }
+    // Descriptors of the tile's operands, computed in registers when the MMAs
+    // are issued: the start address field (bits 0-13, address >> 4) of the
+    // base descriptors plus the byte offset of the split term, the M tile and
+    // the K step >> 4 (addresses stay below 2^18 bytes, so the field does
+    // not carry).
+    const uint64_t adesc0 = smem_desc(abase, 128u, sbo);
+    const uint64_t bdesc0 = smem_desc(bbase, 128u, sbo);
+    const uint32_t a_split16 = (uint32_t)(dense_a_bytes(Mp) >> 4), b_split16 = (uint32_t)(dense_b_bytes(D) >> 4);
+    const uint32_t mtile16 = (16u * sbo) >> 4, kstep16 = 256u >> 4;
     __syncthreads();
 
     // A tile's inputs, loaded into registers one tile ahead so their latency
@@ -192,9 +179,18 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         float g[2 * kGItems];
     };
     const int bitems = (D / 8) * (kDenseKT / 8);
-    auto g_item = [&](const TileIn& in, int it, float& g0, float& g1) {
-        const int c = (it % (D / 8)) * 8 + (lane & 7);
-        const int j = (it / (D / 8)) * 8 + (lane >> 3) * 2;
+    // item it covers columns 8*(it % (D/8)) .. +7 and bags 8*(it / (D/8)) .. +7;
+    // this lane's column and first bag for item `it`
+    auto item_cj = [&](int it, int& c, int& j) {
+        const int cg = it % (D / 8);
+        c = cg * 8 + (lane & 7);
+        j = ((it - cg) / (D / 8)) * 8 + (lane >> 3) * 2;
+    };
+    // the warp's first kGItems items, decoded once (no divisions per tile)
+    int it_c[kGItems], it_j[kGItems];
+#pragma unroll
+    for (int i = 0; i < kGItems; ++i) item_cj(warp + i * kDenseWarps, it_c[i], it_j[i]);
+    auto g_at = [&](const TileIn& in, int c, int j, float& g0, float& g1) {
         const float* gp = a.grad + (int64_t)(in.b0 + j) * a.total_d + td.doff + c;
         g0 = j < in.nb ? __ldg(gp) : 0.f;
         g1 = j + 1 < in.nb ? __ldg(gp + a.total_d) : 0.f;
@@ -221,14 +217,14 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         for (int i = 0; i < kGItems; ++i) {
             const int it = warp + i * kDenseWarps;
             in.g[2 * i] = in.g[2 * i + 1] = 0.f;
-            if (it < bitems) g_item(in, it, in.g[2 * i], in.g[2 * i + 1]);
+            if (it < bitems) g_at(in, it_c[i], it_j[i], in.g[2 * i], in.g[2 * i + 1]);
         }
     };
-    auto put_b = [&](int it, int bb, float g0, float g1) {
+    auto put_b = [&](int c, int j, int bb, float g0, float g1) {
         uint16_t t0[kDenseSplit], t1[kDenseSplit];
         split3(g0, t0);
         split3(g1, t1);
-        const uint32_t off = core_off((it % (D / 8)) * 8 + (lane & 7), (it / (D / 8)) * 8 + (lane >> 3) * 2, sbo);
+        const uint32_t off = core_off(c, j, sbo);
 #pragma unroll
         for (int si = 0; si < kDenseSplit; ++si)
             *reinterpret_cast<uint32_t*>(Bs + (bb * kDenseSplit + si) * dense_b_bytes(D) + off) =
@@ -238,12 +234,14 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
 #pragma unroll
         for (int i = 0; i < kGItems; ++i) {
             const int it = warp + i * kDenseWarps;
-            if (it < bitems) put_b(it, bb, in.g[2 * i], in.g[2 * i + 1]);
+            if (it < bitems) put_b(it_c[i], it_j[i], bb, in.g[2 * i], in.g[2 * i + 1]);
         }
         for (int it = warp + kGItems * kDenseWarps; it < bitems; it += kDenseWarps) {
+            int c, j;
+            item_cj(it, c, j);
             float g0, g1;
-            g_item(in, it, g0, g1);
-            put_b(it, bb, g0, g1);
+            g_at(in, c, j, g0, g1);
+            put_b(c, j, bb, g0, g1);
         }
     };
 
@@ -253,6 +251,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     auto accumulate = [&](const TileIn& in, uint32_t(&ent)[kDenseLk], bool& full) {
         full = in.qend - in.q0 > (uint32_t)(kDenseThreads * kDenseLk);
         auto one = [&](uint32_t q, int r, float sc) -> uint32_t {
+            if (!__any_sync(0xffffffffu, q < in.qend)) return kNoEntry;  // no lookup in this warp's slot
             // bag of q: the last j < nb with first lookup <= q (whole warp)
             int j = 0;
 #pragma unroll
@@ -326,24 +325,30 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     for (int kt = 0; kt < ntiles; ++kt) {
         const int buf = kt & 1;
         __syncthreads();  // histogram and G_t of this tile complete; last tile's H^T cleared
-        // touched histogram entries -> H^T terms (repeated entries write equal values)
+        // touched histogram entries -> H^T terms.  Each entry is taken (and
+        // cleared for the next tile) by one atomic exchange; of the lookups
+        // that share it, the one that gets a nonzero sum writes H^T (a zero
+        // sum leaves the cleared entry as it is).
         if (!full_cur) {
 #pragma unroll
             for (int kk = 0; kk < kDenseLk; ++kk) {
                 if (cur[kk] == kNoEntry) continue;
                 const uint32_t m = cur[kk] >> 5, j = cur[kk] & 31u;
+                const float v = atomicExch(&Hf[hf_index(m, j)], 0.f);
+                if (v == 0.f) continue;
                 uint16_t tt[kDenseSplit];
-                split3(Hf[hf_index(m, j)], tt);
+                split3(v, tt);
                 const uint32_t off = core_off((int)m, (int)j, sbo);
 #pragma unroll
                 for (int si = 0; si < kDenseSplit; ++si)
                     *reinterpret_cast<uint16_t*>(As + si * dense_a_bytes(Mp) + off) = tt[si];
             }
         } else {
-            for (int e = tid; e < Mp * kDenseKT; e += kDenseThreads) {
+            for (int e = tid; e < Mp * kDenseKT; e += kDenseThreads) {  // one thread per entry
                 const uint32_t m = (uint32_t)e / kDenseKT, j = (uint32_t)e % kDenseKT;
                 const float v = Hf[hf_index(m, j)];
                 if (v == 0.f) continue;
+                Hf[hf_index(m, j)] = 0.f;
                 uint16_t tt[kDenseSplit];
                 split3(v, tt);
                 const uint32_t off = core_off((int)m, (int)j, sbo);
@@ -357,21 +362,29 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         __syncthreads();
         tcgen05_after_sync();
         if (tid == 0) {
-            for (int q = 0; q < nmma; ++q)
-                mma_f16(tmem + s_dcol[q], s_adesc[q], s_bdesc[buf][q], idesc, (first && s_init[q]) ? 0u : 1u);
+            // per M tile and K step, the six products x_i * y_j with i + j <= 2;
+            // the first MMA of each M tile starts the sum after a restart
+            const uint64_t bbuf = bdesc0 + (uint64_t)(buf * kDenseSplit) * b_split16;
+            for (int i = 0; i < mtiles; ++i) {
+#pragma unroll
+                for (int ks = 0; ks < kDenseKT / 16; ++ks) {
+                    const uint64_t a_ik = adesc0 + (uint64_t)(i * mtile16 + ks * kstep16);
+                    const uint64_t b_k = bbuf + (uint64_t)(ks * kstep16);
+                    const uint32_t d = tmem + (uint32_t)(i * D);
+#pragma unroll
+                    for (int pr = 0; pr < 6; ++pr) {
+                        constexpr uint32_t kPa = 0x910, kPb = 0x184;  // (pa, pb): (0,0) (0,1) (1,0) (0,2) (1,1) (2,0)
+                        const uint32_t pa = (kPa >> (2 * pr)) & 3u, pb = (kPb >> (2 * pr)) & 3u;
+                        mma_f16(d, a_ik + (uint64_t)(pa * a_split16), b_k + (uint64_t)(pb * b_split16), idesc,
+                                (first && ks == 0 && pr == 0) ? 0u : 1u);
+                    }
+                }
+            }
             mma_commit(&s_bar);
         }
         first = false;
-        // while the MMAs run: clear this tile's histogram entries, then build
-        // the next tile's histogram and G_t from the prefetched inputs
-        if (!full_cur) {
-#pragma unroll
-            for (int kk = 0; kk < kDenseLk; ++kk)
-                if (cur[kk] != kNoEntry) Hf[hf_index(cur[kk] >> 5, cur[kk] & 31u)] = 0.f;
-        } else {
-            for (int i = tid; i < Mp * kDenseKT; i += kDenseThreads) Hf[i] = 0.f;
-        }
-        __syncthreads();  // histogram clear before the next tile's additions
+        // while the MMAs run: the next tile's histogram (cleared before the
+        // sync above) and G_t from the prefetched inputs
         const bool more = kt + 1 < ntiles;
         if (more) {
             build_b(pf, buf ^ 1);

@@ -5,12 +5,13 @@
 //  1. bag_marks_kernel + keys_kernel: one (table,row) key per lookup, key =
 //     rowbase_t + idx (or the sentinel sum-of-rows for an index out of
 //     range), the flat bag of each position, the lookup's scale s_i when
-//     weights or mean pooling apply, and the digit histograms of every radix
-//     pass.  Positions are tiled evenly (the first bag of each tile is marked
-//     by a pass over the bags), so bag lengths do not unbalance the work.
+//     weights or mean pooling apply, and the first radix pass's digit counts.
+//     Positions are tiled evenly (the first bag of each tile is marked by a
+//     pass over the bags), so bag lengths do not unbalance the work.
 //  2. a stable LSD radix sort of (key, position), 8- or 9-bit digits,
-//     reduce-then-scan per pass: per-tile digit counts (the keys kernel gives
-//     the first pass's), a scan per digit over the tiles, and a scatter that
+//     reduce-then-scan per pass: per-tile digit counts and the pass's digit
+//     histogram (the keys kernel gives the first pass's, the upsweep the
+//     others), a scan per digit over the tiles, and a scatter that
 //     ranks each tile's keys by digit (ballot match + per-warp counters, in
 //     input order) and writes each digit's run contiguously.
 //  3. run-length encoding, reduce-then-scan: runs per tile
@@ -56,13 +57,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_
     return warp_excl + x - v;
 }
 
-// Exclusive scan of n counts in place by one 1024-thread block, each thread
-// taking a contiguous chunk (one block-wide scan in all), plus `start`;
-// returns the total on every thread.
-__device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
-                                                        uint32_t* s_warp) {
+// Exclusive scan of n counts in place by one block of THREADS threads, each
+// thread taking a contiguous chunk (one block-wide scan in all), plus
+// `start`; returns the total on every thread.
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_scan_row(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
+                                                   uint32_t* s_warp) {
+    constexpr int WARPS = THREADS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t chunk = (n + 1023) / 1024;
+    const uint32_t chunk = (n + THREADS - 1) / THREADS;
     const uint32_t i0 = tid * chunk, i1 = tmin<uint32_t>(i0 + chunk, n);
     uint32_t sum = 0;
     for (uint32_t i = i0; i < i1; ++i) sum += row[i];
@@ -75,7 +78,8 @@ __device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ r
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     uint32_t before = 0, total = 0;
-    for (int w = 0; w < 32; ++w) {
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
         const uint32_t c = s_warp[w];
         if (w < warp) before += c;
         total += c;
@@ -87,6 +91,11 @@ __device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ r
         run += c;
     }
     return start + total;
+}
+
+__device__ __forceinline__ uint32_t block_scan_row_1024(uint32_t* __restrict__ row, uint32_t n, uint32_t start,
+                                                        uint32_t* s_warp) {
+    return block_scan_row<1024>(row, n, start, s_warp);
 }
 
 // ------------------------------------------------------------------ keys
@@ -197,15 +206,14 @@ __device__ __forceinline__ uint32_t sorted_count(const PrepArgs& a, const Worksp
 // positions a ballot of the marks, the highest marked lane at or below each
 // lane, and a carry from the previous 32).  Warp w takes positions
 // w*512 + k*32 + lane (k < 16), so loads and stores are coalesced.  The first
-// radix pass's digit counts are kept per tile (for the sort's scan), and the
-// digit histograms of all passes per block, added to the global histograms
-// at the end; equal top digits of a warp (few distinct values) are added
-// once (lanes with equal digits found by ballots).
+// radix pass's digit counts are kept per tile (for the sort's scan) and per
+// block (added to the first pass's global histogram at the end); the later
+// passes count their digits in the upsweep.
 template <typename IDX>
 __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) {
     __shared__ int32_t s_off[kKeysWindow + 3];  // offsets bf .. bl+1 (N < 2^30)
     __shared__ int16_t s_mark[kSortTile];       // window index of the bag starting at each position
-    __shared__ uint32_t s_hist[kMaxPasses][kMaxRadix];
+    __shared__ uint32_t s_hist0[kMaxRadix];  // first-pass digit histogram of the block
     __shared__ uint32_t s_tc[kMaxRadix];  // first-pass digit counts of the current tile
     __shared__ int32_t s_wlast[kSortThreads / 32];
     __shared__ int64_t s_last;
@@ -214,13 +222,12 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
     const int64_t nbags = (int64_t)a.T * a.B;
     const int dbits = a.digit_bits;
     const uint32_t dmask = (1u << dbits) - 1u;
-    const int passes = (a.key_bits + dbits - 1) / dbits;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t Nc = a.N;  // offsets are clamped to [0, N] when staged
     const uint32_t ns = tmax<uint32_t>(sorted_count(a, ws), 1u);
     uint32_t err = 0;
 
-    for (int i = threadIdx.x; i < kMaxPasses * kMaxRadix; i += blockDim.x) (&s_hist[0][0])[i] = 0;
+    for (int i = threadIdx.x; i < kMaxRadix; i += blockDim.x) s_hist0[i] = 0;
     for (int i = threadIdx.x; i < kMaxRadix; i += blockDim.x) s_tc[i] = 0;
 
     const int64_t tiles = (a.N + kSortTile - 1) / kSortTile;
@@ -357,43 +364,27 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
                     ws.scale[p] = sc;
                 }
             }
-            // digit counts of the sorted keys; the top pass's digits take few
-            // values within a warp, so equal ones are added once
-            const bool counted = keyk != 0xffffffffu;
-            for (int q = 0; q < passes; ++q) {
-                const uint32_t d = (keyk >> (q * dbits)) & dmask;
-                uint32_t* c = q == 0 ? &s_tc[d] : &s_hist[q][d];
-                if (q == passes - 1) {
-                    const uint32_t lab = counted ? d : (uint32_t)kMaxRadix;
-                    const uint32_t vmask = __ballot_sync(0xffffffffu, counted);
-                    const uint32_t d_first = __shfl_sync(0xffffffffu, lab, vmask ? __ffs(vmask) - 1 : 0);
-                    if (__all_sync(0xffffffffu, !counted || lab == d_first)) {
-                        // one digit for the whole warp (a table narrower than the digit)
-                        if (vmask && lane == __ffs(vmask) - 1) atomicAdd(c, (uint32_t)__popc(vmask));
-                    } else {
-                        const uint32_t peers = match_label<kMaxRadixBits + 1>(lab);
-                        if (counted && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(c, (uint32_t)__popc(peers));
-                    }
-                } else if (counted) {
-                    atomicAdd(c, 1u);
-                }
-            }
+            // first-pass digit counts of this tile (the later passes' come
+            // from the upsweep); compacted keys do not follow these tiles,
+            // so then the sort counts every pass itself
+            if (keyk != 0xffffffffu && !ws.compact) atomicAdd(&s_tc[keyk & dmask], 1u);
         }
         // the tile's first-pass digit counts: to the sort's count table and
         // the block's first-pass histogram
-        // (compacted keys do not follow these tiles: the sort counts its own)
-        __syncthreads();
-        for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x) {
-            const uint32_t c = s_tc[d];
-            if (!ws.compact) ws.tcount[(size_t)d * tiles + tile] = c;
-            s_hist[0][d] += c;
-            s_tc[d] = 0;
+        if (!ws.compact) {
+            __syncthreads();
+            for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x) {
+                const uint32_t c = s_tc[d];
+                ws.tcount[(size_t)d * tiles + tile] = c;
+                s_hist0[d] += c;
+                s_tc[d] = 0;
+            }
         }
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < passes * kMaxRadix; i += blockDim.x) {
-        const uint32_t c = (&s_hist[0][0])[i];
-        if (c) atomicAdd(ws.hist + i, c);
+    if (!ws.compact) {
+        __syncthreads();
+        for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x)
+            if (s_hist0[d]) atomicAdd(ws.hist + d, s_hist0[d]);
     }
     if (err) atomicOr(&a.blk->error, err);
 }
@@ -408,59 +399,83 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
 // tile, so the time per tile does not grow with the number of tiles in
 // flight.
 
-// Digit counts of one tile of keys (one CTA per tile).
+// Digit counts of tiles of keys (a CTA walks tiles blockIdx.x + k*gridDim.x),
+// also summed per CTA and added once to the pass's global digit histogram.
 template <int RB>
 __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* __restrict__ keys, uint32_t N,
                                                                const uint32_t* __restrict__ nsp, int shift,
-                                                               uint32_t* __restrict__ tcount, uint32_t tiles) {
+                                                               uint32_t* __restrict__ tcount, uint32_t tiles,
+                                                               uint32_t* __restrict__ hist) {
     constexpr int RADIX = 1 << RB;
     __shared__ uint32_t s_c[RADIX];
+    __shared__ uint32_t s_g[RADIX];
     const int tid = threadIdx.x;
     if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
-    for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = 0;
-    __syncthreads();
-    const uint32_t base = blockIdx.x * kSortTile;
-    uint32_t key[kSortItems];
+    for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = s_g[d] = 0;
+    for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        __syncthreads();  // counts of the previous tile read and cleared
+        const uint32_t base = tile * kSortTile;
+        uint32_t key[kSortItems];
 #pragma unroll
-    for (int k = 0; k < kSortItems; ++k) {
-        const uint32_t idx = base + k * kSortThreads + tid;
-        key[k] = idx < N ? __ldg(keys + idx) : 0u;
+        for (int k = 0; k < kSortItems; ++k) {
+            const uint32_t idx = base + k * kSortThreads + tid;
+            key[k] = idx < N ? __ldg(keys + idx) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kSortItems; ++k)
+            if (base + k * kSortThreads + tid < N) atomicAdd(&s_c[(key[k] >> shift) & (RADIX - 1)], 1u);
+        __syncthreads();
+        for (int d = tid; d < RADIX; d += kSortThreads) {
+            const uint32_t c = s_c[d];
+            tcount[(size_t)d * tiles + tile] = c;
+            s_g[d] += c;
+            s_c[d] = 0;
+        }
     }
-#pragma unroll
-    for (int k = 0; k < kSortItems; ++k)
-        if (base + k * kSortThreads + tid < N) atomicAdd(&s_c[(key[k] >> shift) & (RADIX - 1)], 1u);
     __syncthreads();
-    for (int d = tid; d < RADIX; d += kSortThreads) tcount[(size_t)d * tiles + blockIdx.x] = s_c[d];
+    for (int d = tid; d < RADIX; d += kSortThreads)
+        if (s_g[d]) atomicAdd(hist + d, s_g[d]);  // the pass's global histogram
 }
 
-// Exclusive scan of one digit's row of tile counts (one CTA per digit),
-// offset by the number of keys with a smaller digit: the global start of the
-// digit's keys from each tile, in place.
-template <int RB>
-__global__ void __launch_bounds__(1024) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
-                                                    uint32_t tiles) {
-    __shared__ uint32_t s_warp[32];
+// Exclusive scan of one digit's row of tile counts (one CTA of THREADS per
+// digit), offset by the number of keys with a smaller digit: the global
+// start of the digit's keys from each tile, in place.
+template <int RB, int THREADS>
+__global__ void __launch_bounds__(THREADS) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
+                                                       uint32_t tiles) {
+    constexpr int WARPS = THREADS / 32;
+    __shared__ uint32_t s_warp[WARPS];
     __shared__ uint32_t s_start;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = blockIdx.x;
     // keys with a smaller digit
     {
         uint32_t v = 0;
-        for (int e = tid; e < d; e += 1024) v += __ldg(hist + e);
+        for (int e = tid; e < d; e += THREADS) v += __ldg(hist + e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) s_warp[warp] = v;
         __syncthreads();
         if (tid == 0) {
             uint32_t t = 0;
-            for (int w = 0; w < 32; ++w) t += s_warp[w];
+            for (int w = 0; w < WARPS; ++w) t += s_warp[w];
             s_start = t;
         }
         __syncthreads();
     }
     const uint32_t start = s_start;
     __syncthreads();  // s_warp is reused below
-    block_scan_row_1024(tcount + (size_t)d * tiles, tiles, start, s_warp);
+    block_scan_row<THREADS>(tcount + (size_t)d * tiles, tiles, start, s_warp);
+}
+
+// Scan of every digit's row: 256-thread CTAs (all resident at once) while a
+// thread's share of a row stays small, 1024-thread ones beyond.
+template <int RB>
+void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, cudaStream_t s) {
+    if (tiles <= 256u * 16u)
+        scan_kernel<RB, 256><<<1 << RB, 256, 0, s>>>(tcount, hist, tiles);
+    else
+        scan_kernel<RB, 1024><<<1 << RB, 1024, 0, s>>>(tcount, hist, tiles);
 }
 
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
@@ -835,8 +850,10 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     e = a.idx64 ? launch_keys<int64_t>(a, ws, tiles, sms, s) : launch_keys<int32_t>(a, ws, tiles, sms, s);
     if (e != cudaSuccess) return e;
     const uint32_t* nsp = a.compact ? ws.counters + CTR_NS : nullptr;  // sorted keys (device count)
+    // upsweep CTAs: each walks several tiles when there are more than four
+    // CTAs' worth per SM, so fewer partial histograms meet in global atomics
+    const unsigned ugrid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 4);
     int cur = 0;
-    const int radix = 1 << ws.digit_bits;
     for (int p = 0; p < ws.passes; ++p) {
         // the first pass numbers the positions itself unless the keys kernel
         // wrote them (compacted keys) and counted its tiles' digits otherwise
@@ -845,12 +862,12 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         const uint32_t* vin = gen ? nullptr : ws.vals[cur];
         uint32_t* kout = ws.keys[cur ^ 1];
         uint32_t* vout = ws.vals[cur ^ 1];
-        const uint32_t* hp = ws.hist + p * kMaxRadix;
+        uint32_t* hp = ws.hist + p * kMaxRadix;
         const int shift = p * ws.digit_bits;
         const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
-            if (!gen) upsweep_kernel<9><<<tiles, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt);
-            scan_kernel<9><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
+            if (!gen) upsweep_kernel<9><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
+            launch_scan<9>(ws.tcount, hp, nt, s);
             if (gen)
                 downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
                                                                          shift);
@@ -858,8 +875,8 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
                 downsweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
                                                                           shift);
         } else {
-            if (!gen) upsweep_kernel<8><<<tiles, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt);
-            scan_kernel<8><<<radix, 1024, 0, s>>>(ws.tcount, hp, nt);
+            if (!gen) upsweep_kernel<8><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
+            launch_scan<8>(ws.tcount, hp, nt, s);
             if (gen)
                 downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
                                                                          shift);
