@@ -31,6 +31,7 @@ constexpr int kHistThreads = 512;    // 16 warps; warp w reads tensor-memory lan
 constexpr int kHistTilesPerCta = 8;  // bag tiles per CTA (W^T is loaded once)
 
 constexpr float kHalfMax = 65504.f;
+constexpr int kHistBagofCap = 8192;  // positions of a tile whose bag is tabulated in shared memory
 
 // Fallback for a tile whose values do not fit the fp16 operands: warp per
 // bag, lanes over columns, fp32 accumulation straight from the table.
@@ -86,7 +87,10 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
     const uint32_t sbo = (uint32_t)(Kp / 8) * 128u;  // bytes per 8 rows of H (bags) and of W^T (columns)
     unsigned char* Hs = smem_raw;
     unsigned char* Ws = smem_raw + (size_t)kHistM * Kp * 2;
-    int64_t* s_off = reinterpret_cast<int64_t*>(Ws + (size_t)D * Kp * 2);  // the CTA's bag offsets
+    // the CTA's bag offsets (clamped to [-1, N + 1]: positions are below 2^30)
+    int32_t* s_off = reinterpret_cast<int32_t*>(Ws + (size_t)D * Kp * 2);
+    // bag within the tile of each of the tile's first kHistBagofCap positions
+    uint8_t* s_bagof = reinterpret_cast<uint8_t*>(s_off + kHistTilesPerCta * kHistM + 1);
     const int ntiles = (a.B + kHistM - 1) / kHistM;
     const int tile0 = cta * kHistTilesPerCta;
     if (tile0 >= ntiles) return;  // whole CTA leaves before allocating anything
@@ -107,7 +111,8 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
     }
     __syncthreads();
     // bag offsets of the CTA's tiles
-    for (int i = tid; i <= bag_hi - bag_lo; i += kHistThreads) s_off[i] = ld_index(off, (int64_t)t * a.B + bag_lo + i);
+    for (int i = tid; i <= bag_hi - bag_lo; i += kHistThreads)
+        s_off[i] = (int32_t)tmin<int64_t>(tmax<int64_t>(ld_index(off, (int64_t)t * a.B + bag_lo + i), -1), a.N + 1);
     // W^T as fp16: element (n, k) = W[k][n], zero for k >= R
     const unsigned short* W = reinterpret_cast<const unsigned short*>(td.data);
     int ovf = 0;
@@ -143,18 +148,25 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
     for (int tile = tile0; tile < tile1; ++tile) {
         const int b0 = tile * kHistM;
         const int nb = b0 + kHistM < a.B ? kHistM : a.B - b0;
-        const int64_t* toff = s_off + (b0 - bag_lo);  // toff[0..nb]
+        const int32_t* toff = s_off + (b0 - bag_lo);  // toff[0..nb]
         if (wovf) {  // the table does not fit fp16: every tile by fp32 gather
             hist_tile_gather<DT, IDX>(a, td, t, b0, nb, warp, lane, oob);
             continue;
         }
-        // zero H
+        // zero H; tabulate the bag of each position (four threads per bag)
         for (int e = tid; e < kHistM * Kp * 2 / 16; e += kHistThreads)
             reinterpret_cast<uint4*>(Hs)[e] = make_uint4(0u, 0u, 0u, 0u);
+        const int64_t P0 = toff[0], P1 = toff[nb];
+        {
+            const int m = tid >> 2, sub = tid & 3;
+            if (m < nb) {
+                const int64_t s0 = tmax<int64_t>(toff[m], P0), s1 = tmin<int64_t>(toff[m + 1], P0 + kHistBagofCap);
+                for (int64_t q = s0 + sub; q < s1; q += 4) s_bagof[q - P0] = (uint8_t)m;
+            }
+        }
         __syncthreads();
         // histogram of the tile: its lookups are the contiguous range
         // [toff[0], toff[nb]); each thread takes every 512th, four in flight
-        const int64_t P0 = toff[0], P1 = toff[nb];
         const bool range_ok = P0 >= 0 && P1 >= P0 && P1 <= a.N;
         if (!range_ok) bad_off = true;
         for (int64_t pb = P0 + tid; range_ok && pb < P1; pb += 4 * kHistThreads) {
@@ -174,14 +186,19 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
             for (int u = 0; u < 4; ++u) {
                 const int64_t p = pb + (int64_t)u * kHistThreads;
                 if (p >= P1) continue;
-                // bag of position p: last m with toff[m] <= p
-                int lo = 0, hi = nb - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (toff[mid] <= p)
-                        lo = mid;
-                    else
-                        hi = mid - 1;
+                // bag of position p: tabulated, else (a long tile, or offsets
+                // that do not partition the range) the last m with toff[m] <= p
+                int lo = p - P0 < kHistBagofCap ? s_bagof[p - P0] : 0;
+                if (!(p - P0 < kHistBagofCap && lo < nb && toff[lo] <= p && p < toff[lo + 1])) {
+                    lo = 0;
+                    int hi = nb - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (toff[mid] <= p)
+                            lo = mid;
+                        else
+                            hi = mid - 1;
+                    }
                 }
                 const int64_t L = toff[lo + 1] - toff[lo];
                 if (L <= 0) {  // malformed offsets: p belongs to no bag
@@ -264,7 +281,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
 // Shared memory of the histogram kernel for a table of R rows and dim D.
 size_t hist_smem_bytes(int64_t R, int D) {
     const int64_t Kp = (R + 15) & ~int64_t(15);
-    return (size_t)(kHistM + D) * Kp * 2 + sizeof(int64_t) * (kHistTilesPerCta * kHistM + 1);
+    return (size_t)(kHistM + D) * Kp * 2 + sizeof(int32_t) * (kHistTilesPerCta * kHistM + 1) + kHistBagofCap;
 }
 
 int hist_ctas_per_table(int B) {

@@ -213,6 +213,7 @@ template <typename IDX>
 __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) {
     __shared__ int32_t s_off[kKeysWindow + 3];  // offsets bf .. bl+1 (N < 2^30)
     __shared__ int16_t s_mark[kSortTile];       // window index of the bag starting at each position
+    __shared__ float s_w[kSortTile];            // the tile's per-sample weights
     __shared__ uint32_t s_hist0[kMaxRadix];  // first-pass digit histogram of the block
     __shared__ uint32_t s_tc[kMaxRadix];  // first-pass digit counts of the current tile
     __shared__ int32_t s_wlast[kSortThreads / 32];
@@ -249,11 +250,17 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
         const int64_t nwin = bl - bf + 2;  // offsets bf .. bl+1
         const bool staged = nwin <= kKeysWindow;
         // the tile's indices and weights, loaded before the bag map is built
+        // (the weights into shared memory, read after the next sync)
         IDX xv[kSortItems];
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k) {
             const int li = warp * (32 * kSortItems) + k * 32 + lane;
             xv[k] = li < n ? ind[p0 + li] : (IDX)0;
+        }
+        if (ws.scale && a.weights) {
+#pragma unroll 4
+            for (int i = threadIdx.x; i < n; i += kSortThreads) s_w[i] = __ldg(a.weights + p0 + i);
+            __syncthreads();
         }
         // window index of each item's bag (staged tiles), two per register
         uint32_t bj2[kSortItems / 2];
@@ -347,9 +354,11 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
                 const bool in_range = (uint64_t)(int64_t)xv[k] < (uint64_t)rows;
                 if (!in_range) err |= ERR_OOB;
                 if (dense) {
-                    // dense tables: the row for the shared-memory backward, no key
+                    // dense tables: the row for the shared-memory backward, no
+                    // key (and no bag: the dense backward walks bag offsets)
                     ws.hrow[p] = in_range ? (uint16_t)xv[k] : (uint16_t)0xffffu;
                 } else {
+                    ws.bag[p] = bag;
                     const uint32_t key = in_range ? rowbase + (uint32_t)xv[k] : a.total_rows;
                     keyk = key;
                     // malformed offsets could send a slot out of range: clamp
@@ -357,9 +366,8 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
                     ws.keys[0][c] = key;
                     if (ws.compact) ws.vals[0][c] = p;
                 }
-                ws.bag[p] = bag;
                 if (ws.scale) {
-                    float sc = a.weights ? __ldg(a.weights + p) : 1.f;
+                    float sc = a.weights ? s_w[li] : 1.f;
                     if (a.mean && L > 0) sc = __fdiv_rn(sc, (float)L);
                     ws.scale[p] = sc;
                 }
@@ -401,6 +409,9 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
 
 // Digit counts of tiles of keys (a CTA walks tiles blockIdx.x + k*gridDim.x),
 // also summed per CTA and added once to the pass's global digit histogram.
+// Only the tiles that hold keys are counted (with compacted keys the device
+// count of sorted keys can be far below N); the scan and the scatter skip the
+// rest too.
 template <int RB>
 __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* __restrict__ keys, uint32_t N,
                                                                const uint32_t* __restrict__ nsp, int shift,
@@ -411,8 +422,9 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
     __shared__ uint32_t s_g[RADIX];
     const int tid = threadIdx.x;
     if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
+    const uint32_t used = tmin<uint32_t>(tiles, (N + kSortTile - 1) / kSortTile);  // tiles holding keys
     for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = s_g[d] = 0;
-    for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (uint32_t tile = blockIdx.x; tile < used; tile += gridDim.x) {
         __syncthreads();  // counts of the previous tile read and cleared
         const uint32_t base = tile * kSortTile;
         uint32_t key[kSortItems];
@@ -442,7 +454,7 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
 // start of the digit's keys from each tile, in place.
 template <int RB, int THREADS>
 __global__ void __launch_bounds__(THREADS) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
-                                                       uint32_t tiles) {
+                                                       uint32_t tiles, uint32_t N, const uint32_t* __restrict__ nsp) {
     constexpr int WARPS = THREADS / 32;
     __shared__ uint32_t s_warp[WARPS];
     __shared__ uint32_t s_start;
@@ -465,17 +477,20 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(uint32_t* __restrict__ tc
     }
     const uint32_t start = s_start;
     __syncthreads();  // s_warp is reused below
-    block_scan_row<THREADS>(tcount + (size_t)d * tiles, tiles, start, s_warp);
+    if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
+    const uint32_t used = tmin<uint32_t>(tiles, (N + kSortTile - 1) / kSortTile);  // tiles holding keys
+    block_scan_row<THREADS>(tcount + (size_t)d * tiles, used, start, s_warp);
 }
 
 // Scan of every digit's row: 256-thread CTAs (all resident at once) while a
 // thread's share of a row stays small, 1024-thread ones beyond.
 template <int RB>
-void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, cudaStream_t s) {
-    if (tiles <= 256u * 16u)
-        scan_kernel<RB, 256><<<1 << RB, 256, 0, s>>>(tcount, hist, tiles);
+void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, uint32_t N, const uint32_t* nsp,
+                 cudaStream_t s) {
+    if (tiles <= 256u * 16u || nsp)  // compacted keys: usually few of the tiles hold keys
+        scan_kernel<RB, 256><<<1 << RB, 256, 0, s>>>(tcount, hist, tiles, N, nsp);
     else
-        scan_kernel<RB, 1024><<<1 << RB, 1024, 0, s>>>(tcount, hist, tiles);
+        scan_kernel<RB, 1024><<<1 << RB, 1024, 0, s>>>(tcount, hist, tiles, N, nsp);
 }
 
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
@@ -621,6 +636,11 @@ __device__ __forceinline__ int key_table(const PrepArgs& a, uint32_t key) {
     return lo;
 }
 
+// First key past table t's key range (all keys for the skipped-lookup key T).
+__device__ __forceinline__ uint32_t table_end(const PrepArgs& a, int t) {
+    return t >= a.T ? 0xffffffffu : (t + 1 < a.T ? (uint32_t)a.tabs[t + 1].rowbase : a.total_rows);
+}
+
 // Run-length encoding of the sorted keys, tile by tile with a warp-parallel
 // look-back for the running count of distinct keys: uniq/runstart and
 // ustart[t], the first distinct-key index of every table (keys are sorted and
@@ -700,6 +720,16 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
     const uint32_t excl = block_exclusive_scan_256(__popc(heads), s_scan, &tile_total);
     const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], N);
     uint32_t u = ws.tcount[tile] + excl;
+    // table of a key, kept with its key range [t_lo, t_hi): sorted neighbours
+    // mostly share a table, so the search runs about once per table change
+    // the table of the previous key: sorted neighbours mostly share a table,
+    // so the search runs about once per table change
+    int tprev = -1;
+    uint32_t t_hi = 0u;  // first key past tprev's range
+    if (p0 > 0 && p0 <= N) {
+        tprev = key_table(a, prev);
+        t_hi = table_end(a, tprev);
+    }
 #pragma unroll
     for (int q = 0; q < kSortItems; ++q) {
         if (!(heads & (1u << q))) continue;
@@ -709,9 +739,12 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
             ws.runstart[u] = p;
             // tables whose key range starts after the previous key and at or
             // before this one begin at u
-            const int tprev = p > 0 ? key_table(a, q > 0 ? k[q - 1] : prev) : -1;
-            const int tk = key_table(a, key);
-            for (int t2 = tprev + 1; t2 <= tk; ++t2) ws.ustart[t2] = u;
+            if (tprev < 0 || key >= t_hi) {
+                const int tk = key_table(a, key);
+                for (int t2 = tprev + 1; t2 <= tk; ++t2) ws.ustart[t2] = u;
+                tprev = tk;
+                t_hi = table_end(a, tk);
+            }
         }
         ++u;
     }
@@ -867,7 +900,7 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
             if (!gen) upsweep_kernel<9><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
-            launch_scan<9>(ws.tcount, hp, nt, s);
+            launch_scan<9>(ws.tcount, hp, nt, n, nsp, s);
             if (gen)
                 downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
                                                                          shift);
@@ -876,7 +909,7 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
                                                                           shift);
         } else {
             if (!gen) upsweep_kernel<8><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
-            launch_scan<8>(ws.tcount, hp, nt, s);
+            launch_scan<8>(ws.tcount, hp, nt, n, nsp, s);
             if (gen)
                 downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
                                                                          shift);
