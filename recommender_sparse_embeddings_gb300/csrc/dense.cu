@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     // A tile's inputs, loaded into registers one tile ahead so their latency
     // hides behind the previous tile's work: the bag offsets (lane l: first
     // lookup of bag l), the row and scale of this thread's lookups
-    // q0 + tid + 512*kk, and the gradient values of its G_t items (a warp
+    // q0 + perm + 512*kk, and the gradient values of its G_t items (a warp
     // item covers 8 columns x 8 bags; lane: column c0 + lane%8, bags
     // 2*(lane/8) and +1, so each split term is one 4-byte store and a warp's
     // stores fill distinct banks).
@@ -178,6 +178,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         float s[kDenseLk];
         float g[2 * kGItems];
     };
+    // lookup slot of this thread in every block of 512 positions: (t % 8) * 64
+    // + t / 8, so a warp's 32 lookups come from 8 runs of 4 (mostly 8 bags:
+    // their H^T entries spread over the shared-memory banks)
+    const int perm = (tid & 7) * 64 + (tid >> 3);
     const int bitems = (D / 8) * (kDenseKT / 8);
     // item it covers columns 8*(it % (D/8)) .. +7 and bags 8*(it / (D/8)) .. +7;
     // this lane's column and first bag for item `it`
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     auto load_inputs = [&](TileIn& in) {  // after load_offsets
 #pragma unroll
         for (int kk = 0; kk < kDenseLk; ++kk) {
-            const uint32_t q = in.q0 + (uint32_t)(tid + kk * kDenseThreads);
+            const uint32_t q = in.q0 + (uint32_t)(perm + kk * kDenseThreads);
             in.r[kk] = 0xffff;
             in.s[kk] = 0.f;
             if (q < in.qend) {
@@ -269,10 +273,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         };
 #pragma unroll
         for (int kk = 0; kk < kDenseLk; ++kk)
-            ent[kk] = one(in.q0 + (uint32_t)(tid + kk * kDenseThreads), in.r[kk], in.s[kk]);
+            ent[kk] = one(in.q0 + (uint32_t)(perm + kk * kDenseThreads), in.r[kk], in.s[kk]);
         if (full) {
             for (uint32_t base = in.q0 + kDenseThreads * kDenseLk; base < in.qend; base += kDenseThreads) {
-                const uint32_t q = base + (uint32_t)tid;
+                const uint32_t q = base + (uint32_t)perm;
                 int r = 0xffff;
                 float sc = 0.f;
                 if (q < in.qend) {

@@ -159,17 +159,26 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
         const int64_t P0 = toff[0], P1 = toff[nb];
         {
             const int m = tid >> 2, sub = tid & 3;
+            bool bad = false;
             if (m < nb) {
+                bad = toff[m + 1] < toff[m];
                 const int64_t s0 = tmax<int64_t>(toff[m], P0), s1 = tmin<int64_t>(toff[m + 1], P0 + kHistBagofCap);
                 for (int64_t q = s0 + sub; q < s1; q += 4) s_bagof[q - P0] = (uint8_t)m;
             }
+            // offsets that do not rise monotonically: every position searches
+            if (__syncthreads_or(bad)) bad_off = true;
         }
-        __syncthreads();
+        const bool tab_ok = !bad_off;
         // histogram of the tile: its lookups are the contiguous range
-        // [toff[0], toff[nb]); each thread takes every 512th, four in flight
+        // [toff[0], toff[nb]); per block of 512 positions, thread t takes
+        // position (t % 8) * 64 + t / 8, so a warp's 32 lookups come from 8
+        // runs of 4 (8 bags, mostly: their H entries spread over the banks)
+        // while its index loads stay 8 whole sectors; four in flight
         const bool range_ok = P0 >= 0 && P1 >= P0 && P1 <= a.N;
         if (!range_ok) bad_off = true;
-        for (int64_t pb = P0 + tid; range_ok && pb < P1; pb += 4 * kHistThreads) {
+        const int perm = (tid & 7) * 64 + (tid >> 3);
+        for (int64_t base = P0; range_ok && base < P1; base += 4 * kHistThreads) {
+            const int64_t pb = base + perm;
             int64_t x[4];
             float w[4];
 #pragma unroll
@@ -187,9 +196,9 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
                 const int64_t p = pb + (int64_t)u * kHistThreads;
                 if (p >= P1) continue;
                 // bag of position p: tabulated, else (a long tile, or offsets
-                // that do not partition the range) the last m with toff[m] <= p
+                // that do not rise monotonically) the last m with toff[m] <= p
                 int lo = p - P0 < kHistBagofCap ? s_bagof[p - P0] : 0;
-                if (!(p - P0 < kHistBagofCap && lo < nb && toff[lo] <= p && p < toff[lo + 1])) {
+                if (!(tab_ok && p - P0 < kHistBagofCap)) {
                     lo = 0;
                     int hi = nb - 1;
                     while (lo < hi) {

@@ -223,6 +223,23 @@ def test_malformed_offsets_are_reported():
     h.close()
 
 
+def test_malformed_offsets_on_a_histogram_table_are_reported():
+    """The same decreasing offsets on a small fp16 table: the histogram forward
+    and the dense backward report BAD_OFFSETS (every read stays inside the
+    batch: offsets are clamped to [0, N])."""
+    tables = make_tables([(64, 16, torch.float16)])
+    h = tbe.tbe_create(tables, "sum")
+    assert tbe.tbe_table_paths(h) == ["histogram"]
+    ind = torch.tensor([1, 2, 3, 4, 5, 6], dtype=torch.int64, device=DEV)
+    off = torch.tensor([0, 4, 2, 6], dtype=torch.int64, device=DEV)
+    tbe.tbe_forward(h, ind, off, 3)
+    assert tbe.tbe_get_error(h) == tbe.TBE_ERR_BAD_OFFSETS
+    ws = tbe.make_workspace(h, 6, 3)
+    tbe.tbe_backward_sgd(h, ind, off, 3, torch.zeros((3, 16), device=DEV), 0.1, ws)
+    assert tbe.tbe_get_error(h) == tbe.TBE_ERR_BAD_OFFSETS
+    h.close()
+
+
 def test_workspace_too_small_is_rejected_before_launch():
     tables = make_tables([(20, 16, torch.float32)])
     h = tbe.tbe_create(tables, "sum")
