@@ -90,6 +90,56 @@ def test_histogram_out_of_range_and_int32():
     h.close()
 
 
+def test_histogram_scales_beyond_fp16_fall_back_per_tile():
+    """Weights of 32768 on bags that repeat rows: an entry of H (the sum of a
+    bag's scales of one row) passes fp16's 65504, so that tile goes to the
+    fp32 gather; bags of distinct rows stay on the tensor cores."""
+    g = torch.Generator().manual_seed(11)
+    tables = [(torch.randn((256, 32), generator=g) * 0.01).half().to(DEV)]
+    B = 400
+    rng = np.random.default_rng(12)
+    lens = rng.integers(1, 40, B)
+    idx = []
+    for b in range(B):
+        if b < 128:  # first tile: rows drawn from 4, so repeats
+            idx.append(rng.integers(0, 4, lens[b]))
+        else:  # other tiles: distinct rows in each bag
+            idx.append(rng.permutation(256)[:lens[b]])
+    ind = torch.tensor(np.concatenate(idx), dtype=torch.int64)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int64)
+    w = torch.full((ind.numel(),), 32768.0)  # exact in fp16; two of them are not
+    h = tbe.tbe_create(tables, "sum")
+    assert tbe.tbe_table_paths(h) == ["histogram"]
+    out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, w.to(DEV))
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    ref, _ = oracle_forward(tables, ind, off, B, w)
+    got = out.cpu().numpy()
+    # the first tile (fp32 gather) to the fp32 tolerance; the others: exact
+    # fp16 H entries and table values, fp32 sums of up to 39 terms of about
+    # 330 (rtol 1e-4 and an absolute 1e-2 for outputs that cancel)
+    assert_close(got[:128], ref[:128], what="hist overflow tile", **FP32_TOL)
+    assert_close(got[128:], ref[128:], what="hist large scales", rtol=1e-4, atol=1e-2)
+    h.close()
+
+
+def test_histogram_bf16_table_beyond_fp16_takes_the_gather():
+    """A bf16 table holding values past fp16's range cannot enter the fp16
+    MMA: every tile of it is gathered in fp32 (exact to the fp32 tolerance)."""
+    g = torch.Generator().manual_seed(13)
+    t = torch.randn((128, 16), generator=g) * 0.01
+    t[5, 3] = 1.0e6
+    tables = [t.bfloat16().to(DEV)]
+    B = 200
+    ind, off = batch_for(128, B, 30, seed=14)
+    h = tbe.tbe_create(tables, "mean")
+    assert tbe.tbe_table_paths(h) == ["histogram"]
+    out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B)
+    assert tbe.tbe_get_error(h) == tbe.TBE_OK
+    ref, _ = oracle_forward(tables, ind, off, B, None, "mean")
+    assert_close(out.cpu().numpy(), ref, what="hist bf16 beyond fp16", **FP32_TOL)
+    h.close()
+
+
 def test_histogram_workload_small_tables():
     """The 64 fp16 512x64 tables plus one large fp32 table, B shrunk: the small
     tables run on the histogram path, the large one on the gather path."""
