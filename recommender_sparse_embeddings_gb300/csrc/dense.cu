@@ -20,15 +20,15 @@
 //     - one thread issues tcgen05.mma (kind::f16, bf16 operands, fp32
 //       accumulator in tensor memory, M = 128, N = dim, K = 16) for the six
 //       products x_i y_j with i + j <= 2, and commits to an mbarrier.
-//    Reading a histogram entry for H^T clears it (atomic exchange).  While
-//    the tensor cores run, the threads build the next tile's histogram and
-//    G_t (G_t is double-buffered); after the MMAs, only the touched H^T
-//    entries are cleared.  Every kDensePromote tiles the tensor-memory accumulator is
+//    The lookup that finds a histogram entry empty owns it: it writes the
+//    entry's H^T terms and clears the entry for the next tile.  While the
+//    tensor cores run, the threads build the next tile's histogram and G_t
+//    (G_t is double-buffered); after the MMAs, the owners clear their H^T
+//    entries.  Every kDensePromote tiles the tensor-memory accumulator is
 //    added (fp32, round to nearest) into a second tensor-memory sum and
 //    restarted, so the tensor cores' own accumulation rounds against a small
 //    partial sum.  At the end the CTA stores that sum into its own slice of
-//    the gradient buffer and adds its lookup counts per row (integer
-//    atomics).
+//    the gradient buffer and marks the rows its lookups touched.
 //  dense_update_kernel: one warp per row of every dense table; a row that
 //    some lookup touched adds its S partial sums in order, gets its optimizer
 //    step (the same SGD / row-wise Adagrad arithmetic as the sorted path) and
@@ -68,7 +68,7 @@ __device__ __forceinline__ void split3(float x, uint16_t (&t)[kDenseSplit]) {
 }
 
 // Shared-memory plan of one CTA for Mp rows and dim D (bytes): H^T terms,
-// two buffers of G_t terms, the fp32 histogram, the row counts.
+// two buffers of G_t terms, the fp32 histogram, the touched-row flags.
 __host__ __device__ inline size_t dense_a_bytes(int Mp) { return (size_t)Mp * kDenseKT * 2; }
 __host__ __device__ inline size_t dense_b_bytes(int D) { return (size_t)D * kDenseKT * 2; }
 __host__ __device__ inline size_t dense_smem_bytes(int Mp, int D) {
@@ -265,9 +265,12 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
             }
             const int m = r - row0;
             if (q < in.qend && r < R && m >= 0 && m < Mp) {
-                atomicAdd(&Hf[hf_index((uint32_t)m, (uint32_t)j)], sc);
-                atomicAdd(&s_cnt[m], 1u);
-                return ((uint32_t)m << 5) | (uint32_t)j;
+                // the lookup that finds the entry empty owns it (writes and
+                // clears its H^T terms); a sum that passes through zero can
+                // make a second owner, which writes the same terms
+                const float old = atomicAdd(&Hf[hf_index((uint32_t)m, (uint32_t)j)], sc);
+                s_cnt[m] = 1u;  // the row is touched
+                return old == 0.f ? (((uint32_t)m << 5) | (uint32_t)j) : kNoEntry;
             }
             return kNoEntry;
         };
@@ -329,17 +332,16 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     for (int kt = 0; kt < ntiles; ++kt) {
         const int buf = kt & 1;
         __syncthreads();  // histogram and G_t of this tile complete; last tile's H^T cleared
-        // touched histogram entries -> H^T terms.  Each entry is taken (and
-        // cleared for the next tile) by one atomic exchange; of the lookups
-        // that share it, the one that gets a nonzero sum writes H^T (a zero
-        // sum leaves the cleared entry as it is).
+        // owned histogram entries -> H^T terms, the entry cleared for the
+        // next tile (a zero sum leaves H^T's cleared entry as it is)
         if (!full_cur) {
 #pragma unroll
             for (int kk = 0; kk < kDenseLk; ++kk) {
                 if (cur[kk] == kNoEntry) continue;
                 const uint32_t m = cur[kk] >> 5, j = cur[kk] & 31u;
-                const float v = atomicExch(&Hf[hf_index(m, j)], 0.f);
+                const float v = Hf[hf_index(m, j)];
                 if (v == 0.f) continue;
+                Hf[hf_index(m, j)] = 0.f;
                 uint16_t tt[kDenseSplit];
                 split3(v, tt);
                 const uint32_t off = core_off((int)m, (int)j, sbo);
@@ -447,10 +449,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
                 }
             }
         }
-        __syncthreads();  // all row counts in
+        __syncthreads();  // all touched-row flags in
         uint32_t* dc = ws.dcount + a.roff[k] + row0;
         for (int i = tid; i < rows_here; i += kDenseThreads)
-            if (s_cnt[i]) atomicAdd(dc + i, s_cnt[i]);
+            if (s_cnt[i]) dc[i] = 1u;  // touched (several parts store the same flag)
     } else {
         if (tid == 0) atomicOr(&a.blk->error, ERR_TIMEOUT);
         mbar_wait(&s_bar, phase);  // a second bounded wait for the MMAs in flight
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(256) dense_update_kernel(DenseArgs a, Workspac
         dense_update_row<DT_F32>(a, td, g, r, lane);
 }
 
-// Clears the row counts, sums, updates (all on stream s).
+// Clears the touched-row flags, sums, updates (all on stream s).
 cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
     cudaError_t e = cudaMemsetAsync(ws.dcount, 0, sizeof(uint32_t) * (size_t)a.total_rows, s);
