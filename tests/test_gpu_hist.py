@@ -172,11 +172,12 @@ def _multi_table_batch(specs, B, max_len, seed, oob_table=None):
 
 
 def _dense_case(specs, B, pooling, weighted, optimizer, flags=0, seed=0, oob_table=None,
-                applies=1, max_len=70):
+                applies=1, max_len=70, index_dtype=torch.int64):
     from helpers import DT_NAME, table_bits, touched_rows, assert_tables_match
     g = torch.Generator().manual_seed(seed)
     tables = [(torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV) for r, d, dt in specs]
     ind, off = _multi_table_batch(specs, B, max_len, seed=seed + 11, oob_table=oob_table)
+    ind, off = ind.to(index_dtype), off.to(index_dtype)
     w = torch.rand(ind.numel(), generator=g) if weighted else None
     grad = torch.randn((B, sum(d for _, d, _ in specs)), generator=g)
     before = [table_bits(t) for t in tables]
@@ -238,9 +239,10 @@ def test_dense_backward_only_dense_tables():
     _dense_case(specs, 300, "sum", True, "adagrad", seed=7)
 
 
-def test_dense_backward_out_of_range_is_skipped():
+@pytest.mark.parametrize("index_dtype", [torch.int64, torch.int32])
+def test_dense_backward_out_of_range_is_skipped(index_dtype):
     specs = [(64, 32, torch.float16), (5000, 32, torch.float32)]
-    _dense_case(specs, 130, "sum", False, "sgd", seed=9, oob_table=0)
+    _dense_case(specs, 130, "sum", False, "sgd", seed=9, oob_table=0, index_dtype=index_dtype)
 
 
 def test_dense_backward_applies_twice():
