@@ -21,10 +21,11 @@
 //    each key gets its optimizer step and its row is stored.  Sums are plain
 //    fp32 (at most 255 terms).
 //  Long runs, "accumulate": a warp sums one 256-lookup chunk with compensated
-//    (Kahan) fp32 addition and writes the partial; the warp that completes the
-//    last chunk of a run (atomic count after a fence) adds the partials in a
-//    fixed order with Kahan addition, updates the row, and resets the count
-//    so the prepared workspace can be applied again.
+//    (Kahan) fp32 addition, five gradient rows (dim 256: two) in flight per
+//    row group, and writes the partial; the warp that completes the last
+//    chunk of a run (atomic count after a fence) adds the partials in a fixed
+//    order with Kahan addition, updates the row, and resets the count so the
+//    prepared workspace can be applied again.
 //
 // Lanes own columns: a row is read by a group of LPR lanes (8 for dim 32, 16
 // for dim 64, 32 otherwise), lane l holding columns blk*LPR*4 + (l%LPR)*4 +
@@ -473,7 +474,7 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
     using Sh = ShapeOf<CODE>;
     constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
     using S = Slice<DT, VW, NB, LPR>;
-    constexpr int GROUP = 4 / NB;  // gradient rows in flight per row group
+    constexpr int GROUP = NB == 1 ? 5 : 2;  // gradient rows in flight per row group
     constexpr int STEP = NG * GROUP;
     const int grp = lane / LPR;
     const int64_t tB = (int64_t)t * a.B;
