@@ -32,6 +32,7 @@ constexpr int kHistTilesPerCta = 8;  // bag tiles per CTA (W^T is loaded once)
 
 constexpr float kHalfMax = 65504.f;
 constexpr int kHistBagofCap = 8192;  // positions of a tile whose bag is tabulated in shared memory
+constexpr int kHistInFlight = 8;     // lookups per thread whose index and weight loads are in flight together
 
 // Fallback for a tile whose values do not fit the fp16 operands: warp per
 // bag, lanes over columns, fp32 accumulation straight from the table.
@@ -173,16 +174,16 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
         // [toff[0], toff[nb]); per block of 512 positions, thread t takes
         // position (t % 8) * 64 + t / 8, so a warp's 32 lookups come from 8
         // runs of 4 (8 bags, mostly: their H entries spread over the banks)
-        // while its index loads stay 8 whole sectors; four in flight
+        // while its index loads stay 8 whole sectors; kHistInFlight in flight
         const bool range_ok = P0 >= 0 && P1 >= P0 && P1 <= a.N;
         if (!range_ok) bad_off = true;
         const int perm = (tid & 7) * 64 + (tid >> 3);
-        for (int64_t base = P0; range_ok && base < P1; base += 4 * kHistThreads) {
+        for (int64_t base = P0; range_ok && base < P1; base += kHistInFlight * kHistThreads) {
             const int64_t pb = base + perm;
-            int64_t x[4];
-            float w[4];
+            int64_t x[kHistInFlight];
+            float w[kHistInFlight];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kHistInFlight; ++u) {
                 const int64_t p = pb + (int64_t)u * kHistThreads;
                 x[u] = -1;
                 w[u] = 1.f;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kHistInFlight; ++u) {
                 const int64_t p = pb + (int64_t)u * kHistThreads;
                 if (p >= P1) continue;
                 // bag of position p: tabulated, else (a long tile, or offsets
