@@ -34,6 +34,17 @@ constexpr float kHalfMax = 65504.f;
 constexpr int kHistBagofCap = 8192;  // positions of a tile whose bag is tabulated in shared memory
 constexpr int kHistInFlight = 8;     // lookups per thread whose index and weight loads are in flight together
 
+// fp16 add to a shared-memory half (the shared-space atomic, not the generic
+// one); returns the old value.
+__device__ __forceinline__ __half atomic_add_half_shared(unsigned char* p, __half v) {
+    unsigned short old;
+    asm volatile("atom.shared.add.noftz.f16 %0, [%1], %2;"
+                 : "=h"(old)
+                 : "r"(smem_u32(p)), "h"(__half_as_ushort(v))
+                 : "memory");
+    return __ushort_as_half(old);
+}
+
 // Fallback for a tile whose values do not fit the fp16 operands: warp per
 // bag, lanes over columns, fp32 accumulation straight from the table.
 template <int DT, typename IDX>
@@ -221,8 +232,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
                 }
                 float s = w[u];
                 if (mean) s = __fdiv_rn(s, (float)L);
-                const __half old =
-                    atomicAdd(reinterpret_cast<__half*>(Hs + core_off(lo, (int)x[u], sbo)), __float2half_rn(s));
+                const __half old = atomic_add_half_shared(Hs + core_off(lo, (int)x[u], sbo), __float2half_rn(s));
                 if (!(fabsf(__half2float(old) + s) <= kHalfMax)) s_ovf = 1;
             }
         }

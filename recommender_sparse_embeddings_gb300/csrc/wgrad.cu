@@ -10,9 +10,8 @@
 //
 // Schedule: one warp per bag.  Rows that are whole 16-byte vectors use the
 // forward pass's slot layout: a slot of G lanes covers 32 vectors of a row
-// (one per lane), a warp holds 32/G slots; the warp loads the row indices of
-// 32 lookups at once (one per lane) and each slot takes every (32/G)-th of
-// them, four rows in flight.  Each lane keeps the bag's
+// (one per lane), a warp holds 32/G slots and each slot takes every
+// (32/G)-th lookup of the bag, two at a time.  Each lane keeps the bag's
 // gradient for its vector in registers, multiplies it with the row's vector
 // and the slot adds its lanes' partial dots in a fixed butterfly order.
 // Other rows: the whole warp takes one lookup at a time, lane c owns columns
@@ -75,7 +74,7 @@ __device__ void wgrad_bag_vec(const TableDesc& td, const WgradArgs& a, int b, in
                               bool& oob) {
     constexpr int E = WVec<DT>::E;
     constexpr int S = 32 / G;  // slots per warp
-    constexpr int U = 4;       // lookups in flight per slot
+    constexpr int U = 2;       // lookups in flight per slot
     const int slot = lane / G, sub = lane % G;
     const unsigned mask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (slot * G));
     const int nvec = td.row_bytes >> 4, ncb = td.vecs;
@@ -86,66 +85,59 @@ __device__ void wgrad_bag_vec(const TableDesc& td, const WgradArgs& a, int b, in
     const int64_t L = end - start;
     float g0[E];  // column block 0 of the bag's gradient, held for the whole bag
     load_gvec<E>(grow, sub, nvec, gv, g0);
-    // 32 lookups at a time: lane l loads the row index of lookup c0 + l
-    // (coalesced), then the slots take them U at a time by shuffles
-    for (int64_t c0 = start; c0 < end; c0 += 32) {
-        const int n = (int)tmin<int64_t>(32, end - c0);
-        int rl = -1;
-        if (lane < n) {
-            const int64_t x = ld_index(indices, c0 + lane);
-            if (x >= 0 && x < td.rows)
-                rl = (int)x;
-            else
-                oob = true;
+    for (int64_t p0 = start + slot; p0 < end; p0 += (int64_t)S * U) {
+        int r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t p = p0 + (int64_t)u * S;
+            r[u] = -1;
+            if (p < end) {
+                const int64_t x = ld_index(indices, p);  // the slot's lanes read one address
+                if (x >= 0 && x < td.rows)
+                    r[u] = (int)x;
+                else
+                    oob = true;
+            }
         }
-        for (int k0 = 0; k0 < n; k0 += S * U) {  // the same trip count on every lane
-            int r[U];
+        float dot[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) dot[u] = 0.f;
+        for (int cb = 0; cb < ncb; ++cb) {
+            const int vi = cb * 32 + sub;
+            float g[E];
+            if (cb == 0) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) g[e] = g0[e];
+            } else {
+                load_gvec<E>(grow, vi, nvec, gv, g);
+            }
+            uint4 x[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int k = k0 + u * S + slot;
-                r[u] = __shfl_sync(0xffffffffu, rl, k & 31);
-                if (k >= n) r[u] = -1;
-            }
-            float dot[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) dot[u] = 0.f;
-            for (int cb = 0; cb < ncb; ++cb) {
-                const int vi = cb * 32 + sub;
-                float g[E];
-                if (cb == 0) {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) g[e] = g0[e];
-                } else {
-                    load_gvec<E>(grow, vi, nvec, gv, g);
-                }
-                uint4 x[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    x[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (r[u] >= 0 && vi < nvec) x[u] = __ldg(tab + (int64_t)r[u] * nvec + vi);
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    float f[E];
-                    unpack16<DT>(x[u], f);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) dot[u] = fmaf(g[e], f[e], dot[u]);
-                }
+                x[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (r[u] >= 0 && vi < nvec) x[u] = __ldg(tab + (int64_t)r[u] * nvec + vi);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                float f[E];
+                unpack16<DT>(x[u], f);
 #pragma unroll
-                for (int o = G / 2; o > 0; o >>= 1) dot[u] += __shfl_xor_sync(mask, dot[u], o, G);
+                for (int e = 0; e < E; ++e) dot[u] = fmaf(g[e], f[e], dot[u]);
             }
-            if (sub == 0) {
+        }
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int k = k0 + u * S + slot;
-                    if (k < n) {
-                        float v = r[u] >= 0 ? dot[u] : 0.f;
-                        if (a.mean && L > 0) v = __fdiv_rn(v, (float)L);
-                        a.out[c0 + k] = v;
-                    }
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1) dot[u] += __shfl_xor_sync(mask, dot[u], o, G);
+        }
+        if (sub == 0) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t p = p0 + (int64_t)u * S;
+                if (p < end) {
+                    float v = r[u] >= 0 ? dot[u] : 0.f;
+                    if (a.mean && L > 0) v = __fdiv_rn(v, (float)L);
+                    a.out[p] = v;
                 }
             }
         }
