@@ -421,6 +421,21 @@ def run_ours(args):
         if p == "histogram" and not args.sorted_backward:
             lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
             U += int(torch.unique(ind[lo:hi]).numel())
+    # compulsory bytes (each distinct row, the gradient and the batch once):
+    # the floor under the formula's bytes, which count every gathered row
+    u_row_bytes = 0
+    for t, sp in enumerate(specs):
+        lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
+        u_t = int(torch.unique(ind[lo:hi]).numel()) if hi > lo else 0
+        u_row_bytes += u_t * sp.dim * ELEM[sp.dtype]
+    total_d = sum(sp.dim for sp in specs)
+    ib = idx_dtype.itemsize
+    scale_b = 4 if (w is not None or cfg.pooling == "mean") else 0
+    compulsory = {
+        "forward": u_row_bytes + N * ib + (T * B + 1) * ib + (N * 4 if w is not None else 0) + B * total_d * 4,
+        "apply": B * total_d * 4 + N * (4 + 4 + scale_b) + U * 8 + 2 * u_row_bytes
+                 + (2 * U * 4 if cfg.optimizer == "adagrad" else 0),
+    }
     # radix passes of the sort: 8-bit digits, or 9-bit ones when they save a pass
     key_bits = max(1, h.total_rows.bit_length())
     passes = min((key_bits + 7) // 8, (key_bits + 8) // 9)
@@ -571,7 +586,10 @@ def run_ours(args):
                          "kernel": DOMINANT_KERNELS[dominant], "call": dominant,
                          "ms_per_launch": call_ms[dominant], "bytes_per_launch": nbytes[dominant],
                          "timing": timing_src, "peak_source": peak_src,
-                         "segment_fracs": {k: nbytes[k] / (v / 1e3) / 1e9 / peak for k, v in seg_ms.items()}},
+                         "segment_fracs": {k: nbytes[k] / (v / 1e3) / 1e9 / peak for k, v in seg_ms.items()},
+                         "compulsory": {k: {"bytes": compulsory[k],
+                                            "frac": compulsory[k] / (call_ms[k] / 1e3) / 1e9 / peak}
+                                        for k in ("forward", "apply")}},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
