@@ -424,24 +424,18 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
     if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
     const uint32_t used = tmin<uint32_t>(tiles, (N + kSortTile - 1) / kSortTile);  // tiles holding keys
     for (int d = tid; d < RADIX; d += kSortThreads) s_c[d] = s_g[d] = 0;
-    // a tile's digits (RADIX past the keys), loaded one tile ahead
-    auto load_digits = [&](uint32_t tile, uint32_t (&dg)[kSortItems]) {
+    for (uint32_t tile = blockIdx.x; tile < used; tile += gridDim.x) {
+        __syncthreads();  // counts of the previous tile read and cleared
         const uint32_t base = tile * kSortTile;
+        uint32_t key[kSortItems];
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k) {
             const uint32_t idx = base + k * kSortThreads + tid;
-            dg[k] = (tile < used && idx < N) ? ((__ldg(keys + idx) >> shift) & (RADIX - 1)) : (uint32_t)RADIX;
+            key[k] = idx < N ? __ldg(keys + idx) : 0u;
         }
-    };
-    uint32_t dig[kSortItems];
-    load_digits(blockIdx.x, dig);
-    for (uint32_t tile = blockIdx.x; tile < used; tile += gridDim.x) {
-        __syncthreads();  // counts of the previous tile read and cleared
-        uint32_t nxt[kSortItems];
-        load_digits(tile + gridDim.x, nxt);  // in flight while this tile is counted
 #pragma unroll
         for (int k = 0; k < kSortItems; ++k)
-            if (dig[k] < (uint32_t)RADIX) atomicAdd(&s_c[dig[k]], 1u);
+            if (base + k * kSortThreads + tid < N) atomicAdd(&s_c[(key[k] >> shift) & (RADIX - 1)], 1u);
         __syncthreads();
         for (int d = tid; d < RADIX; d += kSortThreads) {
             const uint32_t c = s_c[d];
@@ -449,8 +443,6 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
             s_g[d] += c;
             s_c[d] = 0;
         }
-#pragma unroll
-        for (int k = 0; k < kSortItems; ++k) dig[k] = nxt[k];
     }
     __syncthreads();
     for (int d = tid; d < RADIX; d += kSortThreads)
@@ -464,44 +456,30 @@ template <int RB, int THREADS>
 __global__ void __launch_bounds__(THREADS) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
                                                        uint32_t tiles, uint32_t N, const uint32_t* __restrict__ nsp) {
     constexpr int WARPS = THREADS / 32;
-    __shared__ uint32_t s_warp[WARPS], s_hwarp[WARPS];
+    __shared__ uint32_t s_warp[WARPS];
+    __shared__ uint32_t s_start;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = blockIdx.x;
+    // keys with a smaller digit
+    {
+        uint32_t v = 0;
+        for (int e = tid; e < d; e += THREADS) v += __ldg(hist + e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_warp[warp] = v;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t t = 0;
+            for (int w = 0; w < WARPS; ++w) t += s_warp[w];
+            s_start = t;
+        }
+        __syncthreads();
+    }
+    const uint32_t start = s_start;
+    __syncthreads();  // s_warp is reused below
     if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
     const uint32_t used = tmin<uint32_t>(tiles, (N + kSortTile - 1) / kSortTile);  // tiles holding keys
-    uint32_t* row = tcount + (size_t)d * tiles;
-    // this thread's contiguous chunk of the row, and (loaded alongside) its
-    // share of the keys with a smaller digit
-    const uint32_t chunk = (used + THREADS - 1) / THREADS;
-    const uint32_t i0 = tid * chunk, i1 = tmin<uint32_t>(i0 + chunk, used);
-    uint32_t sum = 0;
-    for (uint32_t i = i0; i < i1; ++i) sum += row[i];
-    uint32_t v = 0;
-    for (int e = tid; e < d; e += THREADS) v += __ldg(hist + e);
-    // block: inclusive scan of the chunk sums, total of the smaller digits
-    uint32_t x = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 31) s_warp[warp] = x;
-    if (lane == 0) s_hwarp[warp] = v;
-    __syncthreads();
-    uint32_t before = 0, start = 0;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) {
-        if (w < warp) before += s_warp[w];
-        start += s_hwarp[w];
-    }
-    uint32_t run = start + before + x - sum;
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint32_t c = row[i];
-        row[i] = run;
-        run += c;
-    }
+    block_scan_row<THREADS>(tcount + (size_t)d * tiles, used, start, s_warp);
 }
 
 // Scan of every digit's row: 256-thread CTAs (all resident at once) while a
