@@ -350,6 +350,21 @@ def run_ours(args):
     rc = tbe.tbe_get_error(h)
     if rc != tbe.TBE_OK:
         raise RuntimeError(f"device error during warm-up: {tbe.tbe_strerror(rc)}")
+    run_fp, run_ap = fwd_prep, apply
+    if args.graph:
+        # the same calls captured once as two CUDA graphs (the library's side
+        # streams fork from and join back into the capturing stream)
+        g_fp, g_ap = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fp):
+            fwd_prep()
+        with torch.cuda.graph(g_ap):
+            apply()
+        torch.cuda.synchronize()
+        run_fp, run_ap = g_fp.replay, g_ap.replay
+        for _ in range(args.warmup):
+            flush.zero_()
+            run_fp(); run_ap()
+        torch.cuda.synchronize()
 
     # timed region: one step = forward + preparation (concurrent), then apply
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -360,8 +375,8 @@ def run_ours(args):
         for k in range(args.steps):
             flush.zero_()
             e = ev[k]
-            e[0].record(stream); fwd_prep()
-            e[1].record(stream); apply()
+            e[0].record(stream); run_fp()
+            e[1].record(stream); run_ap()
             e[2].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
@@ -567,6 +582,7 @@ def run_ours(args):
                        "config_id": cfg.cfg_id, "T": T, "B": B,
                        "N_lookups": N, "unique_rows": U, "index_dtype": args.index_dtype,
                        "optimizer": cfg.optimizer, "parallelism": f"replicas x{world}",
+                       "launch": "CUDA graph replay" if args.graph else "stream launches",
                        "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
             "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
                     "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
@@ -650,6 +666,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", type=int, default=2)
     p.add_argument("--index-dtype", choices=["int64", "int32"], default="int64")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the step's two calls as captured CUDA graphs")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
