@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
     tcgen05_after_sync();
     const uint32_t tmem = s_tmem;
     const uint32_t idesc = mma_idesc(0, kHistM, D);  // fp16 x fp16 -> fp32
-    const uint32_t hbase = smem_u32(Hs), wbase = smem_u32(Ws);
+    const uint64_t hdesc0 = smem_desc(smem_u32(Hs), 128u, sbo), wdesc0 = smem_desc(smem_u32(Ws), 128u, sbo);
     const bool mean = a.mean != 0;
     const bool wovf = s_wovf != 0;
     uint32_t phase = 0;
@@ -248,9 +248,10 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
             continue;
         }
         if (tid == 0) {
+            // K step j: both descriptors' start address field (address >> 4)
+            // moves by 256 bytes (the field does not carry: addresses < 2^18)
             for (int j = 0; j < Kp / 16; ++j)
-                mma_f16(tmem, smem_desc(hbase + 256u * j, 128u, sbo), smem_desc(wbase + 256u * j, 128u, sbo), idesc,
-                        j > 0 ? 1u : 0u);
+                mma_f16(tmem, hdesc0 + (uint64_t)(16 * j), wdesc0 + (uint64_t)(16 * j), idesc, j > 0 ? 1u : 0u);
             mma_commit(&s_bar);
         }
         // every thread waits; the block agrees on the outcome so all threads
