@@ -19,8 +19,9 @@
 // Both operands are fp16 (the tensor cores take A and B in one type): fp16
 // tables as they are, bf16 tables converted (exact within fp16's normal
 // range), H entries as fp16 sums of lookup scales.  Products and sums are
-// fp32.  A value that does not fit fp16 (a bf16 entry or an H sum beyond
-// 65504) sends the tile to an fp32 gather instead.
+// fp32.  A table value that does not fit fp16 sends the table to an fp32
+// gather; an H sum beyond 65504 (seen as non-finite outputs of its bag)
+// sends its tile there.
 #include "tbe_internal.cuh"
 #include "tcgen05.cuh"
 
@@ -34,15 +35,10 @@ constexpr float kHalfMax = 65504.f;
 constexpr int kHistBagofCap = 8192;  // positions of a tile whose bag is tabulated in shared memory
 constexpr int kHistInFlight = 8;     // lookups per thread whose index and weight loads are in flight together
 
-// fp16 add to a shared-memory half (the shared-space atomic, not the generic
-// one); returns the old value.
-__device__ __forceinline__ __half atomic_add_half_shared(unsigned char* p, __half v) {
-    unsigned short old;
-    asm volatile("atom.shared.add.noftz.f16 %0, [%1], %2;"
-                 : "=h"(old)
-                 : "r"(smem_u32(p)), "h"(__half_as_ushort(v))
-                 : "memory");
-    return __ushort_as_half(old);
+// fp16 add to a shared-memory half (a shared-space reduction: nothing waits
+// for its result).
+__device__ __forceinline__ void red_add_half_shared(unsigned char* p, __half v) {
+    asm volatile("red.shared.add.noftz.f16 [%0], %1;" ::"r"(smem_u32(p)), "h"(__half_as_ushort(v)) : "memory");
 }
 
 // Fallback for a tile whose values do not fit the fp16 operands: warp per
@@ -89,7 +85,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_ovf, s_wovf;
+    __shared__ int s_wovf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = hist_tables[blockIdx.x / ctas_per_table];
     const int cta = blockIdx.x % ctas_per_table;
@@ -116,7 +112,6 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
 
     if (warp == 0) tmem_alloc(&s_tmem, ncols);
     if (tid == 0) {
-        s_ovf = 0;
         s_wovf = 0;
         mbar_init(&s_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -232,21 +227,13 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
                 }
                 float s = w[u];
                 if (mean) s = __fdiv_rn(s, (float)L);
-                const __half old = atomic_add_half_shared(Hs + core_off(lo, (int)x[u], sbo), __float2half_rn(s));
-                if (!(fabsf(__half2float(old) + s) <= kHalfMax)) s_ovf = 1;
+                red_add_half_shared(Hs + core_off(lo, (int)x[u], sbo), __float2half_rn(s));
             }
         }
         fence_proxy_async_smem();  // generic-proxy writes of H -> tensor cores
         tcgen05_before_sync();
         __syncthreads();
         tcgen05_after_sync();
-        if (s_ovf) {  // uniform: written before the barrier above
-            hist_tile_gather<DT, IDX>(a, td, t, b0, nb, warp, lane, oob);
-            __syncthreads();
-            if (tid == 0) s_ovf = 0;
-            __syncthreads();
-            continue;
-        }
         if (tid == 0) {
             // K step j: both descriptors' start address field (address >> 4)
             // moves by 256 bytes (the field does not carry: addresses < 2^18)
@@ -268,10 +255,13 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
         const int lg = warp & 3;
         const int b = b0 + lg * 32 + lane;
         float* orow = a.out + (int64_t)b * a.total_d + td.doff;
+        bool nonfinite = false;
         for (int c = (warp >> 2) * 16; c < D; c += (kHistThreads / 128) * 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)c, v);  // whole warp, aligned
             if (b < a.B) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) nonfinite |= !isfinite(v[q]);
                 if (a.vec_out) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -283,6 +273,9 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const 
                 }
             }
         }
+        // an H entry past fp16's range makes its bag's outputs inf or NaN
+        // (so do inf/NaN inputs): such a tile is redone by the fp32 gather
+        if (__syncthreads_or(nonfinite)) hist_tile_gather<DT, IDX>(a, td, t, b0, nb, warp, lane, oob);
         tcgen05_before_sync();
         __syncthreads();  // accumulator read and H consumed before the next tile
         tcgen05_after_sync();
