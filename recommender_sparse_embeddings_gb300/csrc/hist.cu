@@ -33,7 +33,7 @@ constexpr int kHistTilesPerCta = 8;  // bag tiles per CTA (W^T is loaded once)
 
 constexpr float kHalfMax = 65504.f;
 constexpr int kHistBagofCap = 8192;  // positions of a tile whose bag is tabulated in shared memory
-constexpr int kHistInFlight = 8;     // lookups per thread whose index and weight loads are in flight together
+constexpr int kHistInFlight = 12;    // lookups per thread whose index and weight loads are in flight together
 
 // fp16 add to a shared-memory half (a shared-space reduction: nothing waits
 // for its result).
