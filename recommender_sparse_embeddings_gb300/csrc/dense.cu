@@ -49,6 +49,7 @@ constexpr int kDenseSplit = 3;    // bf16 terms per operand
 constexpr int kDenseLk = 4;       // lookups per thread per tile remembered for the sparse clears
 constexpr int kDensePromote = 4;  // tiles summed in the tensor-memory accumulator before it is restarted
 constexpr uint32_t kNoEntry = 0xffffffffu;
+constexpr int kDenseTab = kDenseThreads * kDenseLk;  // lookups of a tile whose bag is tabulated
 
 // bf16 bits of x rounded to nearest even, and the value they stand for.
 __device__ __forceinline__ uint16_t to_bf16(float x, float& back) {
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     extern __shared__ __align__(1024) unsigned char dsm[];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
+    __shared__ uint8_t s_bagtab[2][kDenseTab];  // bag of each lookup, for two tiles
     const int splits = a.splits;
     const int per_table = groups_max * splits;
     const int k = blockIdx.x / per_table;
@@ -252,16 +254,32 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     // Histogram of a tile: the lookups of `in` (remembered in ent[kk]); the
     // rest (tiles of more than 2048 lookups) marks the tile `full`, whose
     // clears then cover whole arrays.
-    auto accumulate = [&](const TileIn& in, uint32_t(&ent)[kDenseLk], bool& full) {
+    // bag within the tile of each of its first 2048 lookups (16 threads per
+    // bag), built two tiles ahead into one of two buffers
+    auto build_tab = [&](const TileIn& in, int slot) {
+        const int m = tid >> 4, sub = tid & 15;
+        const uint32_t lo = __shfl_sync(0xffffffffu, in.ol, m);
+        const uint32_t nx = __shfl_sync(0xffffffffu, in.ol, (m + 1) & 31);
+        const uint32_t hi = m + 1 < in.nb ? nx : in.qend;
+        if (m < in.nb)
+            for (uint32_t q = lo + (uint32_t)sub; q < hi && q - in.q0 < (uint32_t)kDenseTab; q += 16)
+                s_bagtab[slot][q - in.q0] = (uint8_t)m;
+    };
+    auto accumulate = [&](const TileIn& in, int slot, uint32_t(&ent)[kDenseLk], bool& full) {
         full = in.qend - in.q0 > (uint32_t)(kDenseThreads * kDenseLk);
-        auto one = [&](uint32_t q, int r, float sc) -> uint32_t {
+        auto one = [&](uint32_t q, int r, float sc, bool tab) -> uint32_t {
             if (!__any_sync(0xffffffffu, q < in.qend)) return kNoEntry;  // no lookup in this warp's slot
-            // bag of q: the last j < nb with first lookup <= q (whole warp)
+            // bag of q: from the table, else the last j < nb with first
+            // lookup <= q (whole warp)
             int j = 0;
+            if (tab) {
+                if (q < in.qend) j = s_bagtab[slot][q - in.q0];
+            } else {
 #pragma unroll
-            for (int step = 16; step > 0; step >>= 1) {
-                const uint32_t v = __shfl_sync(0xffffffffu, in.ol, j + step);
-                if (j + step < in.nb && v <= q) j += step;
+                for (int step = 16; step > 0; step >>= 1) {
+                    const uint32_t v = __shfl_sync(0xffffffffu, in.ol, j + step);
+                    if (j + step < in.nb && v <= q) j += step;
+                }
             }
             const int m = r - row0;
             if (q < in.qend && r < R && m >= 0 && m < Mp) {
@@ -276,7 +294,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         };
 #pragma unroll
         for (int kk = 0; kk < kDenseLk; ++kk)
-            ent[kk] = one(in.q0 + (uint32_t)(perm + kk * kDenseThreads), in.r[kk], in.s[kk]);
+            ent[kk] = one(in.q0 + (uint32_t)(perm + kk * kDenseThreads), in.r[kk], in.s[kk], true);
         if (full) {
             for (uint32_t base = in.q0 + kDenseThreads * kDenseLk; base < in.qend; base += kDenseThreads) {
                 const uint32_t q = base + (uint32_t)perm;
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
                     r = __ldg(ws.hrow + q);
                     sc = has_scale ? __ldg(ws.scale + q) : 1.f;
                 }
-                (void)one(q, r, sc);
+                (void)one(q, r, sc, false);
             }
         }
     };
@@ -322,11 +340,14 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     if (ntiles > 0) {
         load_offsets(bk0, pf);
         load_inputs(pf);
+        build_tab(pf, 0);
         build_b(pf, 0);
-        accumulate(pf, cur, full_cur);
+        __syncthreads();  // the bag table
+        accumulate(pf, 0, cur, full_cur);
         if (ntiles > 1) {
             load_offsets(bk0 + kDenseKT, pf);
             load_inputs(pf);
+            build_tab(pf, 1);  // read after the loop's first syncs
         }
     }
     for (int kt = 0; kt < ntiles; ++kt) {
@@ -394,7 +415,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         const bool more = kt + 1 < ntiles;
         if (more) {
             build_b(pf, buf ^ 1);
-            accumulate(pf, nxt, full_nxt);
+            accumulate(pf, buf ^ 1, nxt, full_nxt);
             if (kt + 2 < ntiles) load_offsets(bk0 + (kt + 2) * kDenseKT, pf);  // in flight during the wait
         }
         // every thread waits; the block agrees on the outcome
@@ -405,7 +426,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         }
         phase ^= 1u;
         tcgen05_after_sync();
-        if (more && kt + 2 < ntiles) load_inputs(pf);  // the tile after next: in flight from here on
+        if (more && kt + 2 < ntiles) {  // the tile after next: in flight from here on
+            load_inputs(pf);
+            build_tab(pf, buf);  // this tile's table is no longer read
+        }
         // the MMAs have read H^T: clear what this tile wrote
         if (!full_cur) {
 #pragma unroll
