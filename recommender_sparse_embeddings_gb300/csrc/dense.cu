@@ -44,12 +44,14 @@ namespace tbe {
 
 constexpr int kDenseThreads = 512;
 constexpr int kDenseWarps = kDenseThreads / 32;
+constexpr int kMmaWarp = kDenseWarps - 1;              // issues the MMAs and takes no lookups
+constexpr int kDenseWorkers = kDenseThreads - 32;      // threads of the other warps
 constexpr int kDenseKT = 32;      // bags per tile (two MMA K steps)
 constexpr int kDenseSplit = 3;    // bf16 terms per operand
-constexpr int kDenseLk = 4;       // lookups per thread per tile remembered for the sparse clears
+constexpr int kDenseLk = 5;       // lookups per worker thread per tile remembered for the sparse clears
 constexpr int kDensePromote = 4;  // tiles summed in the tensor-memory accumulator before it is restarted
 constexpr uint32_t kNoEntry = 0xffffffffu;
-constexpr int kDenseTab = kDenseThreads * kDenseLk;  // lookups of a tile whose bag is tabulated
+constexpr int kDenseTab = kDenseWorkers * kDenseLk;  // lookups of a tile whose bag is tabulated
 
 // bf16 bits of x rounded to nearest even, and the value they stand for.
 __device__ __forceinline__ uint16_t to_bf16(float x, float& back) {
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     // A tile's inputs, loaded into registers one tile ahead so their latency
     // hides behind the previous tile's work: the bag offsets (lane l: first
     // lookup of bag l), the row and scale of this thread's lookups
-    // q0 + perm + 512*kk, and the gradient values of its G_t items (a warp
+    // q0 + perm + 480*kk, and the gradient values of its G_t items (a warp
     // item covers 8 columns x 8 bags; lane: column c0 + lane%8, bags
     // 2*(lane/8) and +1, so each split term is one 4-byte store and a warp's
     // stores fill distinct banks).
@@ -180,10 +182,13 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         float s[kDenseLk];
         float g[2 * kGItems];
     };
-    // lookup slot of this thread in every block of 512 positions: (t % 8) * 64
-    // + t / 8, so a warp's 32 lookups come from 8 runs of 4 (mostly 8 bags:
-    // their H^T entries spread over the shared-memory banks)
-    const int perm = (tid & 7) * 64 + (tid >> 3);
+    // lookup slot of worker thread t in every block of 480 positions:
+    // (t % 8) * 60 + t / 8, so a warp's 32 lookups come from 8 runs of 4
+    // (mostly 8 bags: their H^T entries spread over the shared-memory banks);
+    // the MMA warp takes no lookups, so issuing the MMAs (which can wait for
+    // room in the tensor pipe) delays no histogram work
+    const bool worker = warp < kMmaWarp;
+    const int perm = (tid & 7) * (kDenseWorkers / 8) + (tid >> 3);
     const int bitems = (D / 8) * (kDenseKT / 8);
     // item it covers columns 8*(it % (D/8)) .. +7 and bags 8*(it / (D/8)) .. +7;
     // this lane's column and first bag for item `it`
@@ -194,8 +199,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     };
     // the warp's first kGItems items, decoded once (no divisions per tile)
     int it_c[kGItems], it_j[kGItems];
+    // G_t items go to the worker warps (the MMA warp's item numbers start past them all)
+    const int wbase = worker ? warp : (1 << 20);
 #pragma unroll
-    for (int i = 0; i < kGItems; ++i) item_cj(warp + i * kDenseWarps, it_c[i], it_j[i]);
+    for (int i = 0; i < kGItems; ++i) item_cj(wbase + i * kMmaWarp, it_c[i], it_j[i]);
     auto g_at = [&](const TileIn& in, int c, int j, float& g0, float& g1) {
         const float* gp = a.grad + (int64_t)(in.b0 + j) * a.total_d + td.doff + c;
         g0 = j < in.nb ? __ldg(gp) : 0.f;
@@ -211,17 +218,17 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     auto load_inputs = [&](TileIn& in) {  // after load_offsets
 #pragma unroll
         for (int kk = 0; kk < kDenseLk; ++kk) {
-            const uint32_t q = in.q0 + (uint32_t)(perm + kk * kDenseThreads);
+            const uint32_t q = in.q0 + (uint32_t)(perm + kk * kDenseWorkers);
             in.r[kk] = 0xffff;
             in.s[kk] = 0.f;
-            if (q < in.qend) {
+            if (worker && q < in.qend) {
                 in.r[kk] = __ldg(ws.hrow + q);
                 in.s[kk] = has_scale ? __ldg(ws.scale + q) : 1.f;
             }
         }
 #pragma unroll
         for (int i = 0; i < kGItems; ++i) {
-            const int it = warp + i * kDenseWarps;
+            const int it = wbase + i * kMmaWarp;
             in.g[2 * i] = in.g[2 * i + 1] = 0.f;
             if (it < bitems) g_at(in, it_c[i], it_j[i], in.g[2 * i], in.g[2 * i + 1]);
         }
@@ -239,10 +246,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     auto build_b = [&](const TileIn& in, int bb) {
 #pragma unroll
         for (int i = 0; i < kGItems; ++i) {
-            const int it = warp + i * kDenseWarps;
+            const int it = wbase + i * kMmaWarp;
             if (it < bitems) put_b(it_c[i], it_j[i], bb, in.g[2 * i], in.g[2 * i + 1]);
         }
-        for (int it = warp + kGItems * kDenseWarps; it < bitems; it += kDenseWarps) {
+        for (int it = wbase + kGItems * kMmaWarp; it < bitems; it += kMmaWarp) {
             int c, j;
             item_cj(it, c, j);
             float g0, g1;
@@ -252,9 +259,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
     };
 
     // Histogram of a tile: the lookups of `in` (remembered in ent[kk]); the
-    // rest (tiles of more than 2048 lookups) marks the tile `full`, whose
+    // rest (tiles of more than 2400 lookups) marks the tile `full`, whose
     // clears then cover whole arrays.
-    // bag within the tile of each of its first 2048 lookups (16 threads per
+    // bag within the tile of each of its first 2400 lookups (16 threads per
     // bag), built two tiles ahead into one of two buffers
     auto build_tab = [&](const TileIn& in, int slot) {
         const int m = tid >> 4, sub = tid & 15;
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
                 s_bagtab[slot][q - in.q0] = (uint8_t)m;
     };
     auto accumulate = [&](const TileIn& in, int slot, uint32_t(&ent)[kDenseLk], bool& full) {
-        full = in.qend - in.q0 > (uint32_t)(kDenseThreads * kDenseLk);
+        full = in.qend - in.q0 > (uint32_t)(kDenseWorkers * kDenseLk);
         auto one = [&](uint32_t q, int r, float sc, bool tab) -> uint32_t {
             if (!__any_sync(0xffffffffu, q < in.qend)) return kNoEntry;  // no lookup in this warp's slot
             // bag of q: from the table, else the last j < nb with first
@@ -294,10 +301,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         };
 #pragma unroll
         for (int kk = 0; kk < kDenseLk; ++kk)
-            ent[kk] = one(in.q0 + (uint32_t)(perm + kk * kDenseThreads), in.r[kk], in.s[kk], true);
+            ent[kk] = one(worker ? in.q0 + (uint32_t)(perm + kk * kDenseWorkers) : 0xffffffffu, in.r[kk], in.s[kk],
+                          true);
         if (full) {
-            for (uint32_t base = in.q0 + kDenseThreads * kDenseLk; base < in.qend; base += kDenseThreads) {
-                const uint32_t q = base + (uint32_t)perm;
+            for (uint32_t base = in.q0 + kDenseWorkers * kDenseLk; base < in.qend; base += kDenseWorkers) {
+                const uint32_t q = worker ? base + (uint32_t)perm : 0xffffffffu;
                 int r = 0xffff;
                 float sc = 0.f;
                 if (q < in.qend) {
@@ -388,7 +396,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1) dense_mma_kernel(DenseArgs a
         tcgen05_before_sync();
         __syncthreads();
         tcgen05_after_sync();
-        if (tid == 0) {
+        if (tid == kMmaWarp * 32) {
             // per M tile and K step, the six products x_i * y_j with i + j <= 2;
             // the first MMA of each M tile starts the sum after a restart
             const uint64_t bbuf = bdesc0 + (uint64_t)(buf * kDenseSplit) * b_split16;

@@ -226,7 +226,7 @@ def test_dense_backward_rowwise_adagrad_matches_oracle(dtype, rows, dim):
 
 
 @pytest.mark.parametrize("rows,dim", [(512, 64), (200, 128)])
-def test_dense_backward_tiles_of_more_than_2048_lookups(rows, dim):
+def test_dense_backward_tiles_past_the_held_lookups(rows, dim):
     """Bags of up to 250 lookups: most 32-bag tiles hold more lookups than the
     per-thread lists cover, so they take the whole-array clears."""
     specs = [(rows, dim, torch.float16), (900, 32, torch.float32)]
