@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
             __syncthreads();
         }
         // window index of each item's bag (staged tiles), two per register
-        uint32_t bj2[kSortItems / 2];
+        uint32_t bj2[kSortItems / 2] = {};
         auto bj_get = [&](int q) -> int { return (int)((bj2[q >> 1] >> (16 * (q & 1))) & 0xffffu); };
         auto bj_set = [&](int q, int v) {
             const uint32_t h = (uint32_t)v & 0xffffu;
