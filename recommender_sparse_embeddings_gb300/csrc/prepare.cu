@@ -12,8 +12,8 @@
 //     reduce-then-scan per pass: per-tile digit counts and the pass's digit
 //     histogram (the keys kernel gives the first pass's, the upsweep the
 //     others), a scan per digit over the tiles, and a scatter that
-//     ranks each tile's keys by digit (ballot match + per-warp counters, in
-//     input order) and writes each digit's run contiguously.
+//     ranks each tile's keys by digit (warp match of equal digits + per-warp
+//     counters, in input order) and writes each digit's run contiguously.
 //  3. run-length encoding, reduce-then-scan: runs per tile
 //     (rle_count_kernel), a scan over the tiles, then rle_kernel writes the
 //     distinct keys with their first sorted slot (runstart[U] = N) and the
@@ -494,7 +494,7 @@ void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, uint32_
 }
 
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
-// input order (ballot match + per-warp counters), places them by digit in
+// input order (warp match of equal digits + per-warp counters), places them by digit in
 // shared memory and writes each digit's run to its global start from the
 // scan.  The first pass generates the values (positions) instead of
 // reading them.
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32
 #pragma unroll
     for (int k = 0; k < kSortItems; ++k) {
         const int d = digit_of(k);
-        const uint32_t peers = match_label<RB + 1>((uint32_t)d);  // RADIX (past the end) is a label too
+        const uint32_t peers = __match_any_sync(0xffffffffu, (uint32_t)d);  // RADIX (past the end) too
         uint32_t cnt = 0;
         if (d < RADIX) cnt = s_whist[warp][d];
         const uint32_t r = cnt + __popc(peers & lt_mask);

@@ -124,20 +124,6 @@ __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
     }
 }
 
-// Lanes of the warp whose BITS-bit label equals this lane's, from one ballot
-// per label bit (labels of BITS bits; all lanes must call it).
-template <int BITS>
-__device__ __forceinline__ uint32_t match_label(uint32_t label) {
-    uint32_t peers = 0xffffffffu;
-#pragma unroll
-    for (int b = 0; b < BITS; ++b) {
-        const bool bit = (label >> b) & 1u;
-        const uint32_t v = __ballot_sync(0xffffffffu, bit);
-        peers &= bit ? v : ~v;
-    }
-    return peers;
-}
-
 template <typename IDX>
 __device__ __forceinline__ int64_t ld_index(const IDX* p, int64_t k) {
     return (int64_t)__ldg(p + k);
