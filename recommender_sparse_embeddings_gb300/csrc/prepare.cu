@@ -143,6 +143,8 @@ __device__ __forceinline__ int64_t upper_bound_global(const IDX* off, int64_t lo
 // kernel only uses marks to narrow its search and stays in range regardless.
 template <typename IDX>
 __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws) {
+    chain_wait();
+
     const IDX* off = reinterpret_cast<const IDX*>(a.offsets);
     const int64_t nbags = (int64_t)a.T * a.B;
     uint32_t err = 0;
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(256) bag_marks_kernel(PrepArgs a, Workspace ws
 // lookups are not sorted): cbase[t] = the lookups of the sorted-path tables
 // before t, cbase[T] and counters[CTR_NS] = all of them (one CTA).
 __global__ void __launch_bounds__(1024) compact_kernel(PrepArgs a, Workspace ws) {
+    chain_wait();
+
     __shared__ uint32_t s_warp[32];
     for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
         uint32_t c = 0;
@@ -211,6 +215,8 @@ __device__ __forceinline__ uint32_t sorted_count(const PrepArgs& a, const Worksp
 // passes count their digits in the upsweep.
 template <typename IDX>
 __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) {
+    chain_wait();
+
     __shared__ int32_t s_off[kKeysWindow + 3];  // offsets bf .. bl+1 (N < 2^30)
     __shared__ int16_t s_mark[kSortTile];       // window index of the bag starting at each position
     __shared__ float s_w[kSortTile];            // the tile's per-sample weights
@@ -417,6 +423,8 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
                                                                const uint32_t* __restrict__ nsp, int shift,
                                                                uint32_t* __restrict__ tcount, uint32_t tiles,
                                                                uint32_t* __restrict__ hist) {
+    chain_wait();
+
     constexpr int RADIX = 1 << RB;
     __shared__ uint32_t s_c[RADIX];
     __shared__ uint32_t s_g[RADIX];
@@ -455,6 +463,8 @@ __global__ void __launch_bounds__(kSortThreads) upsweep_kernel(const uint32_t* _
 template <int RB, int THREADS>
 __global__ void __launch_bounds__(THREADS) scan_kernel(uint32_t* __restrict__ tcount, const uint32_t* __restrict__ hist,
                                                        uint32_t tiles, uint32_t N, const uint32_t* __restrict__ nsp) {
+    chain_wait();
+
     constexpr int WARPS = THREADS / 32;
     __shared__ uint32_t s_warp[WARPS];
     __shared__ uint32_t s_start;
@@ -488,9 +498,9 @@ template <int RB>
 void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, uint32_t N, const uint32_t* nsp,
                  cudaStream_t s) {
     if (tiles <= 256u * 16u || nsp)  // compacted keys: usually few of the tiles hold keys
-        scan_kernel<RB, 256><<<1 << RB, 256, 0, s>>>(tcount, hist, tiles, N, nsp);
+        launch_chained(scan_kernel<RB, 256>, dim3(1 << RB), dim3(256), s, tcount, hist, tiles, N, nsp);
     else
-        scan_kernel<RB, 1024><<<1 << RB, 1024, 0, s>>>(tcount, hist, tiles, N, nsp);
+        launch_chained(scan_kernel<RB, 1024>, dim3(1 << RB), dim3(1024), s, tcount, hist, tiles, N, nsp);
 }
 
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
@@ -506,6 +516,8 @@ __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32
                                                                     const uint32_t* __restrict__ tstart_g,
                                                                     uint32_t tiles, uint32_t N,
                                                                     const uint32_t* __restrict__ nsp, int shift) {
+    chain_wait();
+
     constexpr int RADIX = 1 << RB;
     constexpr int DPT = RADIX / kSortThreads;  // digits per thread (consecutive)
     static_assert(DPT >= 1 && DPT * kSortThreads == RADIX, "digits must split evenly over the threads");
@@ -679,6 +691,8 @@ __device__ __forceinline__ uint32_t rle_load_heads(const uint32_t* __restrict__ 
 __global__ void __launch_bounds__(kSortThreads) rle_count_kernel(const uint32_t* __restrict__ skeys, uint32_t N,
                                                                  const uint32_t* __restrict__ nsp,
                                                                  uint32_t* __restrict__ tcount) {
+    chain_wait();
+
     __shared__ uint32_t s_scan[8];
     if (nsp) N = tmin<uint32_t>(*nsp, N);  // sorted keys (device count)
     uint32_t k[kSortItems], prev;
@@ -692,6 +706,8 @@ __global__ void __launch_bounds__(kSortThreads) rle_count_kernel(const uint32_t*
 // goes to *total_out.
 __global__ void __launch_bounds__(1024) tile_scan_kernel(uint32_t* __restrict__ cnt, uint32_t n,
                                                          uint32_t* __restrict__ total_out) {
+    chain_wait();
+
     __shared__ uint32_t s_warp[32];
     const uint32_t total = block_scan_row_1024(cnt, n, 0u, s_warp);
     if (threadIdx.x == 0) *total_out = total;
@@ -702,6 +718,8 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(uint32_t* __restrict__ 
 // = N) and ustart[t], the first distinct-key index of every table (keys are
 // sorted and each table owns a consecutive key range), ustart[T] the end.
 __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace ws, const uint32_t* __restrict__ skeys) {
+    chain_wait();
+
     __shared__ uint32_t s_scan[8];
     const uint32_t N = sorted_count(a, ws);
     const int tid = threadIdx.x;
@@ -796,6 +814,8 @@ __device__ __forceinline__ void run_chunks(const PrepArgs& a, const Workspace& w
 
 // Chunks per tile of distinct keys (tiles past the distinct keys count 0).
 __global__ void __launch_bounds__(kSortThreads) chunk_count_kernel(PrepArgs a, Workspace ws, uint32_t tiles) {
+    chain_wait();
+
     __shared__ uint32_t s_scan[8];
     const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], (uint32_t)a.N);
     for (uint32_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -815,6 +835,8 @@ __global__ void __launch_bounds__(kSortThreads) chunk_count_kernel(PrepArgs a, W
 
 // The chunk records and cstart, from the scanned chunk counts.
 __global__ void __launch_bounds__(kSortThreads) chunk_write_kernel(PrepArgs a, Workspace ws, uint32_t tiles) {
+    chain_wait();
+
     __shared__ uint32_t s_scan[8];
     __shared__ uint32_t s_base[kSortTile];  // exclusive chunk base of each distinct key of the tile
     const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], (uint32_t)a.N);
@@ -856,8 +878,7 @@ __global__ void __launch_bounds__(kSortThreads) chunk_write_kernel(PrepArgs a, W
 template <typename IDX>
 static cudaError_t launch_keys(const PrepArgs& a, Workspace& ws, int64_t tiles, int sms, cudaStream_t s) {
     const unsigned grid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 3);
-    keys_kernel<IDX><<<grid, 256, 0, s>>>(a, ws);
-    return cudaGetLastError();
+    return launch_chained(keys_kernel<IDX>, dim3(grid), dim3(256), s, a, ws);
 }
 
 // ------------------------------------------------------------------ launch
@@ -879,7 +900,7 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     else
         bag_marks_kernel<int32_t><<<mgrid, 256, 0, s>>>(a, ws);
     // dense tables present: only the other tables' keys are sorted, compacted
-    if (a.compact) compact_kernel<<<1, 1024, 0, s>>>(a, ws);
+    if (a.compact) launch_chained(compact_kernel, dim3(1), dim3(1024), s, a, ws);
     e = a.idx64 ? launch_keys<int64_t>(a, ws, tiles, sms, s) : launch_keys<int32_t>(a, ws, tiles, sms, s);
     if (e != cudaSuccess) return e;
     const uint32_t* nsp = a.compact ? ws.counters + CTR_NS : nullptr;  // sorted keys (device count)
@@ -899,38 +920,34 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         const int shift = p * ws.digit_bits;
         const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
-            if (!gen) upsweep_kernel<9><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
+            if (!gen) launch_chained(upsweep_kernel<9>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<9>(ws.tcount, hp, nt, n, nsp, s);
             if (gen)
-                downsweep_kernel<true, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
-                                                                         shift);
+                launch_chained(downsweep_kernel<true, 9>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
             else
-                downsweep_kernel<false, 9><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
-                                                                          shift);
+                launch_chained(downsweep_kernel<false, 9>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         } else {
-            if (!gen) upsweep_kernel<8><<<ugrid, kSortThreads, 0, s>>>(kin, n, nsp, shift, ws.tcount, nt, hp);
+            if (!gen) launch_chained(upsweep_kernel<8>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<8>(ws.tcount, hp, nt, n, nsp, s);
             if (gen)
-                downsweep_kernel<true, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
-                                                                         shift);
+                launch_chained(downsweep_kernel<true, 8>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
             else
-                downsweep_kernel<false, 8><<<tiles, kSortThreads, 0, s>>>(kin, vin, kout, vout, ws.tcount, nt, n, nsp,
-                                                                          shift);
+                launch_chained(downsweep_kernel<false, 8>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cur ^= 1;
     }
     ws.sorted_buf = cur;
-    rle_count_kernel<<<tiles, kSortThreads, 0, s>>>(ws.keys[cur], (uint32_t)a.N, nsp, ws.tcount);
-    tile_scan_kernel<<<1, 1024, 0, s>>>(ws.tcount, (uint32_t)tiles, ws.counters + CTR_U);
-    rle_kernel<<<tiles, kSortThreads, 0, s>>>(a, ws, ws.keys[cur]);
+    launch_chained(rle_count_kernel, dim3(tiles), dim3(kSortThreads), s, (const uint32_t*)ws.keys[cur], (uint32_t)a.N, nsp, ws.tcount);
+    launch_chained(tile_scan_kernel, dim3(1), dim3(1024), s, ws.tcount, (uint32_t)tiles, ws.counters + CTR_U);
+    launch_chained(rle_kernel, dim3(tiles), dim3(kSortThreads), s, a, ws, (const uint32_t*)ws.keys[cur]);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned cgrid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 4);
-    chunk_count_kernel<<<cgrid, kSortThreads, 0, s>>>(a, ws, (uint32_t)tiles);
-    tile_scan_kernel<<<1, 1024, 0, s>>>(ws.tcount, (uint32_t)tiles, ws.counters + CTR_NCHUNK);
-    chunk_write_kernel<<<cgrid, kSortThreads, 0, s>>>(a, ws, (uint32_t)tiles);
+    launch_chained(chunk_count_kernel, dim3(cgrid), dim3(kSortThreads), s, a, ws, (uint32_t)tiles);
+    launch_chained(tile_scan_kernel, dim3(1), dim3(1024), s, ws.tcount, (uint32_t)tiles, ws.counters + CTR_NCHUNK);
+    launch_chained(chunk_write_kernel, dim3(cgrid), dim3(kSortThreads), s, a, ws, (uint32_t)tiles);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,31 @@ __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
     }
 }
 
+// Chained launches (programmatic dependent launch).  A kernel started with
+// launch_chained may be launched before the kernel ahead of it on the stream
+// has completed: once every CTA of that kernel has exited, its CTAs are
+// placed at once instead of after the grid's completion is processed.  Its
+// first statement, chain_wait(), waits until that kernel has completed and
+// its writes are visible, so every kernel launched this way keeps the order
+// of the stream.  No kernel releases its dependents early: CTAs waiting on
+// an SM would hold resources that a kernel on another stream could use.
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <typename IDX>
 __device__ __forceinline__ int64_t ld_index(const IDX* p, int64_t k) {
     return (int64_t)__ldg(p + k);
