@@ -665,6 +665,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 // workspace.
 template <int DT, int CODE>
 __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
+    chain_wait();  // returns at once unless launched chained
     __shared__ uint32_t s_ibase[kMaxTables + 1];  // first work item of each class table
     __shared__ uint32_t s_warp[8];
     a.has_scale = ws.counters[CTR_HAS_SCALE] != 0;
@@ -764,17 +765,25 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
     }
 }
 
+template <int DT, int CODE>
+static cudaError_t launch_class(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos, unsigned grid,
+                                cudaStream_t s, bool chained) {
+    if (chained) return launch_chained(apply_class_kernel<DT, CODE>, dim3(grid), dim3(256), s, a, ws, pos);
+    apply_class_kernel<DT, CODE><<<grid, 256, 0, s>>>(a, ws, pos);
+    return cudaGetLastError();
+}
+
+// chained: another class kernel of this call runs just before on stream s
 template <int DT>
 static cudaError_t launch_dtype(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos, int code,
-                                unsigned grid, cudaStream_t s) {
+                                unsigned grid, cudaStream_t s, bool chained) {
     switch (code) {
-        case SHAPE_D32: apply_class_kernel<DT, SHAPE_D32><<<grid, 256, 0, s>>>(a, ws, pos); break;
-        case SHAPE_D64: apply_class_kernel<DT, SHAPE_D64><<<grid, 256, 0, s>>>(a, ws, pos); break;
-        case SHAPE_D128: apply_class_kernel<DT, SHAPE_D128><<<grid, 256, 0, s>>>(a, ws, pos); break;
-        case SHAPE_D256: apply_class_kernel<DT, SHAPE_D256><<<grid, 256, 0, s>>>(a, ws, pos); break;
-        default: apply_class_kernel<DT, SHAPE_GENERIC><<<grid, 256, 0, s>>>(a, ws, pos); break;
+        case SHAPE_D32: return launch_class<DT, SHAPE_D32>(a, ws, pos, grid, s, chained);
+        case SHAPE_D64: return launch_class<DT, SHAPE_D64>(a, ws, pos, grid, s, chained);
+        case SHAPE_D128: return launch_class<DT, SHAPE_D128>(a, ws, pos, grid, s, chained);
+        case SHAPE_D256: return launch_class<DT, SHAPE_D256>(a, ws, pos, grid, s, chained);
+        default: return launch_class<DT, SHAPE_GENERIC>(a, ws, pos, grid, s, chained);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32_t* class_tables,
@@ -810,14 +819,15 @@ cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32
         // an unaligned gradient buffer rules out vector loads: element-wise
         const int code = a.grad_vec ? cls % NUM_SHAPES : SHAPE_GENERIC;
         cudaStream_t cs = fork ? streams[k % kApplyStreams] : s;
+        const bool chained = fork && k >= kApplyStreams;  // the stream ran a group of this call already
         ++k;
         cudaError_t e;
         if (dt == DT_F32)
-            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, cs);
+            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, cs, chained);
         else if (dt == DT_F16)
-            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, cs);
+            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, cs, chained);
         else
-            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, cs);
+            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, cs, chained);
         if (e != cudaSuccess) return e;
     }
     if (fork) {

@@ -531,6 +531,7 @@ __device__ __forceinline__ void dense_update_row(const DenseArgs& a, const Table
 }
 
 __global__ void __launch_bounds__(256) dense_update_kernel(DenseArgs a, Workspace ws) {
+    chain_wait();  // returns at once unless launched chained
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // one warp per row
     if (gw >= a.total_rows) return;
@@ -579,8 +580,7 @@ cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned ublocks = (unsigned)((a.total_rows * 32 + 255) / 256);
-    dense_update_kernel<<<ublocks, 256, 0, s>>>(a, ws);
-    return cudaGetLastError();
+    return launch_chained(dense_update_kernel, dim3(ublocks), dim3(256), s, a, ws);
 }
 
 }  // namespace tbe

@@ -391,6 +391,7 @@ __device__ void long_bag_scalar(const TableDesc& td, const FwdArgs& a, int64_t s
 
 template <typename IDX>
 __global__ void __launch_bounds__(256) fwd_long_kernel(FwdArgs a) {
+    chain_wait();  // returns at once unless launched chained
     __shared__ float part[kLongWarps][kLongMaxFloats];
     const uint32_t cnt = tmin(*(volatile uint32_t*)&a.blk->long_count[a.parity], (uint32_t)kLongBagCap);
     bool oob = false;
@@ -455,6 +456,9 @@ cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const unsigned lgrid = (unsigned)(a.num_sms > 0 ? a.num_sms : 1);
+    if (a.total_warps > 0)  // chained after the pooling kernel
+        return a.idx64 ? launch_chained(fwd_long_kernel<int64_t>, dim3(lgrid), dim3(256), s, a)
+                       : launch_chained(fwd_long_kernel<int32_t>, dim3(lgrid), dim3(256), s, a);
     if (a.idx64)
         fwd_long_kernel<int64_t><<<lgrid, 256, 0, s>>>(a);
     else

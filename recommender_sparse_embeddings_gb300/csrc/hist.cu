@@ -82,6 +82,7 @@ __device__ void hist_tile_gather(const FwdArgs& a, const TableDesc& td, int t, i
 template <int DT, typename IDX>
 __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(FwdArgs a, const int32_t* hist_tables,
                                                              int ctas_per_table) {
+    chain_wait();  // returns at once unless launched chained
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
@@ -314,8 +315,9 @@ static cudaError_t launch_hist_t(const FwdArgs& a, const int32_t* hist_tables, i
         configured = smem;
     }
     const int per = hist_ctas_per_table(a.B);
-    hist_kernel<DT, IDX><<<(unsigned)(nhist * per), kHistThreads, smem, s>>>(a, hist_tables, per);
-    return cudaGetLastError();
+    // the forward's long-bag kernel (or the other dtype's launch) runs just before
+    return launch_chained_smem(hist_kernel<DT, IDX>, dim3((unsigned)(nhist * per)), dim3(kHistThreads), smem, s, a,
+                               hist_tables, per);
 }
 
 // One launch per table dtype (f16, bf16) that has histogram tables.
