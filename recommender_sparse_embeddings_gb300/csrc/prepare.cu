@@ -503,12 +503,30 @@ void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, uint32_
         launch_chained(scan_kernel<RB, 1024>, dim3(1 << RB), dim3(1024), s, tcount, hist, tiles, N, nsp);
 }
 
+// Lanes of the warp holding the same digit d (RADIX, past the end, counts as a
+// digit too).  MATCH: one match.any per key, fewer instructions but a longer
+// latency; otherwise one ballot per bit of the (RB+1)-bit label.  Many waves
+// of tiles hide the match's latency and gain from its instruction count; one
+// wave is latency bound and takes the ballots.
+template <bool MATCH, int RB>
+__device__ __forceinline__ uint32_t lanes_with_digit(uint32_t d) {
+    if (MATCH) return __match_any_sync(0xffffffffu, d);
+    uint32_t peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b <= RB; ++b) {
+        const bool bit = (d >> b) & 1u;
+        const uint32_t v = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? v : ~v;
+    }
+    return peers;
+}
+
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
-// input order (warp match of equal digits + per-warp counters), places them by digit in
+// input order (lanes_with_digit + per-warp counters), places them by digit in
 // shared memory and writes each digit's run to its global start from the
 // scan.  The first pass generates the values (positions) instead of
 // reading them.
-template <bool FIRST, int RB>
+template <bool FIRST, int RB, bool MATCH>
 __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32_t* __restrict__ keys_in,
                                                                     const uint32_t* __restrict__ vals_in,
                                                                     uint32_t* __restrict__ keys_out,
@@ -559,7 +577,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32
 #pragma unroll
     for (int k = 0; k < kSortItems; ++k) {
         const int d = digit_of(k);
-        const uint32_t peers = __match_any_sync(0xffffffffu, (uint32_t)d);  // RADIX (past the end) too
+        const uint32_t peers = lanes_with_digit<MATCH, RB>((uint32_t)d);
         uint32_t cnt = 0;
         if (d < RADIX) cnt = s_whist[warp][d];
         const uint32_t r = cnt + __popc(peers & lt_mask);
@@ -874,6 +892,17 @@ __global__ void __launch_bounds__(kSortThreads) chunk_write_kernel(PrepArgs a, W
     }
 }
 
+// One downsweep pass: positions generated (first pass) or read, ranking by
+// warp match or by ballots.
+template <int RB>
+static void launch_downsweep(bool first, bool match, int tiles, cudaStream_t s, const uint32_t* kin,
+                             const uint32_t* vin, uint32_t* kout, uint32_t* vout, const uint32_t* tstart,
+                             uint32_t nt, uint32_t n, const uint32_t* nsp, int shift) {
+    auto* k = first ? (match ? downsweep_kernel<true, RB, true> : downsweep_kernel<true, RB, false>)
+                    : (match ? downsweep_kernel<false, RB, true> : downsweep_kernel<false, RB, false>);
+    launch_chained(k, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, tstart, nt, n, nsp, shift);
+}
+
 // One wave of keys_kernel CTAs (three per SM).
 template <typename IDX>
 static cudaError_t launch_keys(const PrepArgs& a, Workspace& ws, int64_t tiles, int sms, cudaStream_t s) {
@@ -907,6 +936,8 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     // upsweep CTAs: each walks several tiles when there are more than four
     // CTAs' worth per SM, so fewer partial histograms meet in global atomics
     const unsigned ugrid = (unsigned)tmin<int64_t>(tiles, (int64_t)sms * 4);
+    // downsweep ranking: warp match beyond one wave of tiles (3 CTAs per SM)
+    const bool match = tiles > sms * 3;
     int cur = 0;
     for (int p = 0; p < ws.passes; ++p) {
         // the first pass numbers the positions itself unless the keys kernel
@@ -922,17 +953,11 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         if (ws.digit_bits == 9) {
             if (!gen) launch_chained(upsweep_kernel<9>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<9>(ws.tcount, hp, nt, n, nsp, s);
-            if (gen)
-                launch_chained(downsweep_kernel<true, 9>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
-            else
-                launch_chained(downsweep_kernel<false, 9>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
+            launch_downsweep<9>(gen, match, tiles, s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         } else {
             if (!gen) launch_chained(upsweep_kernel<8>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<8>(ws.tcount, hp, nt, n, nsp, s);
-            if (gen)
-                launch_chained(downsweep_kernel<true, 8>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
-            else
-                launch_chained(downsweep_kernel<false, 8>, dim3(tiles), dim3(kSortThreads), s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
+            launch_downsweep<8>(gen, match, tiles, s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
