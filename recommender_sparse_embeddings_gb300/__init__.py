@@ -194,6 +194,8 @@ def tbe_create(tables: Sequence[torch.Tensor], pooling: str = "sum", flags: int 
     for i, t in enumerate(tables):
         if t.dim() != 2 or t.dtype not in _DTYPES:
             raise ValueError("tables must be 2-D fp32/fp16/bf16 CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("tables must be contiguous (row-major, rows packed)")
         arr[i] = _Table(t.shape[0], t.shape[1], _DTYPES[t.dtype], _ptr(t))
     out = ctypes.c_void_p()
     _check(lib.tbe_create(arr, len(tables), _POOL[pooling], flags, ctypes.byref(out)), "tbe_create")

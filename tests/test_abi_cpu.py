@@ -67,3 +67,14 @@ def test_calls_reject_null_handle():
     assert lib.tbe_get_error(None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_backward_apply(None, 0, 0, None, None, None, 0, None) == tbe.TBE_ERR_INVALID_ARG
     lib.tbe_destroy(None)  # no-op
+
+
+def test_binding_rejects_tables_that_are_not_packed_rows():
+    """A table view whose rows are not packed (an expanded row, a column
+    slice) has no row-major layout for the library to index."""
+    import torch
+
+    with pytest.raises(ValueError, match="contiguous"):
+        tbe.tbe_create([torch.zeros(1, 16).expand(100, 16)])
+    with pytest.raises(ValueError, match="contiguous"):
+        tbe.tbe_create([torch.zeros(100, 32)[:, :16]])

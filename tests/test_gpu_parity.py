@@ -3,6 +3,8 @@ the same seeded inputs.  Workload shapes follow the five synthetic configs,
 shrunk (fewer bags, fewer rows) so the oracle finishes in seconds while the
 batches still span many warps, several sort tiles and a ragged tail."""
 
+import types
+
 import numpy as np
 import pytest
 import torch
@@ -58,6 +60,53 @@ def test_forward_matches_oracle(cid, index_dtype):
 @pytest.mark.parametrize("cid,flags", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (5, tbe.TBE_FLAG_SORTED_BACKWARD)])
 def test_prepare_sort_and_rle_bit_exact(cid, flags):
     cfg, tables, batch, _ = make_problem(cid)
+    check_prepare(cfg, tables, batch, flags)
+
+
+def test_prepare_sort_bit_exact_many_waves():
+    """A batch of many more 4096-key tiles than one wave of sort CTAs (three
+    per SM): the downsweep then ranks by warp match instead of ballots.
+    Workload 3's tables (rows / 100) with B = 4096: about 2.5 M lookups,
+    20-bit keys, three 8-bit passes."""
+    cfg = workloads.get_config(3).scaled(B=4096, rows_div=100, rows_min=64)
+    specs = workloads.realize_tables(cfg)
+    tables = [t.to(DEV) for t in workloads.make_tables(cfg, "cpu", specs)]
+    batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (batch.N + 4095) // 4096 > 3 * sms
+    check_prepare(cfg, tables, batch, 0)
+
+
+def test_prepare_sort_bit_exact_many_waves_9bit_digits():
+    """The same beyond one wave with 25-bit keys, which take three 9-bit
+    passes: two fp16 tables of 2^24 and 2^20 + 7 rows (dim 16, zeros: the
+    preparation reads only the indices), uniform and repeated indices,
+    B = 65536 bags of 0..40 lookups."""
+    rng = np.random.default_rng(11)
+    rows = [1 << 24, (1 << 20) + 7]
+    tables = [torch.zeros((r, 16), dtype=torch.float16, device=DEV) for r in rows]
+    B = 65536
+    lens = rng.integers(0, 41, 2 * B)
+    idx = []
+    for t, r in enumerate(rows):
+        n = int(lens[t * B:(t + 1) * B].sum())
+        ii = rng.integers(0, r, n)
+        hot = rng.integers(0, r, 8)  # rows repeated often enough for long runs
+        m = rng.random(n) < 0.2
+        ii[m] = hot[rng.integers(0, 8, int(m.sum()))]
+        idx.append(ii)
+    batch = types.SimpleNamespace(
+        indices=torch.from_numpy(np.concatenate(idx).astype(np.int64)),
+        offsets=torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)),
+        weights=None)
+    batch.N = batch.indices.numel()
+    cfg = types.SimpleNamespace(B=B, pooling="sum")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (batch.N + 4095) // 4096 > 3 * sms
+    check_prepare(cfg, tables, batch, 0)
+
+
+def check_prepare(cfg, tables, batch, flags):
     h = tbe.tbe_create(tables, cfg.pooling, flags)
     ind, off = batch.indices.to(DEV), batch.offsets.to(DEV)
     w = None if batch.weights is None else batch.weights.to(DEV)
