@@ -245,7 +245,7 @@ __device__ __forceinline__ void bag_range(const FwdArgs& a, int64_t bag, int64_t
 }
 
 template <typename IDX>
-__global__ void __launch_bounds__(256) fwd_pool_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(256, 4) fwd_pool_kernel(FwdArgs a) {
     const int gw = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (gw >= a.total_warps) return;
     const int lane = threadIdx.x & 31;
