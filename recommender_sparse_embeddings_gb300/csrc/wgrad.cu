@@ -11,7 +11,8 @@
 // Schedule: one warp per bag.  Rows that are whole 16-byte vectors use the
 // forward pass's slot layout: a slot of G lanes covers 32 vectors of a row
 // (one per lane), a warp holds 32/G slots and each slot takes every
-// (32/G)-th lookup of the bag, two at a time.  Each lane keeps the bag's
+// (32/G)-th lookup of the bag, four at a time (four CTAs of 256 per SM, 64
+// registers: the gathers are latency bound).  Each lane keeps the bag's
 // gradient for its vector in registers, multiplies it with the row's vector
 // and the slot adds its lanes' partial dots in a fixed butterfly order.
 // Other rows: the whole warp takes one lookup at a time, lane c owns columns
@@ -74,7 +75,7 @@ __device__ void wgrad_bag_vec(const TableDesc& td, const WgradArgs& a, int b, in
                               bool& oob) {
     constexpr int E = WVec<DT>::E;
     constexpr int S = 32 / G;  // slots per warp
-    constexpr int U = 2;       // lookups in flight per slot
+    constexpr int U = 4;       // lookups in flight per slot
     const int slot = lane / G, sub = lane % G;
     const unsigned mask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (slot * G));
     const int nvec = td.row_bytes >> 4, ncb = td.vecs;
@@ -189,7 +190,7 @@ __device__ __forceinline__ void wgrad_bag(const TableDesc& td, const WgradArgs& 
 }
 
 template <typename IDX>
-__global__ void __launch_bounds__(256) wgrad_kernel(WgradArgs a) {
+__global__ void __launch_bounds__(256, 4) wgrad_kernel(WgradArgs a) {
     const int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // one warp per bag
     if (bag >= (int64_t)a.T * a.B) return;
     const int lane = threadIdx.x & 31;
