@@ -507,7 +507,8 @@ void launch_scan(uint32_t* tcount, const uint32_t* hist, uint32_t tiles, uint32_
 // digit too).  MATCH: one match.any per key, fewer instructions but a longer
 // latency; otherwise one ballot per bit of the (RB+1)-bit label.  Many waves
 // of tiles hide the match's latency and gain from its instruction count; one
-// wave is latency bound and takes the ballots.
+// wave is latency bound and takes the ballots.  The match form also runs four
+// CTAs per SM (64 registers) to hide more of that latency.
 template <bool MATCH, int RB>
 __device__ __forceinline__ uint32_t lanes_with_digit(uint32_t d) {
     if (MATCH) return __match_any_sync(0xffffffffu, d);
@@ -527,7 +528,7 @@ __device__ __forceinline__ uint32_t lanes_with_digit(uint32_t d) {
 // scan.  The first pass generates the values (positions) instead of
 // reading them.
 template <bool FIRST, int RB, bool MATCH>
-__global__ void __launch_bounds__(kSortThreads, 3) downsweep_kernel(const uint32_t* __restrict__ keys_in,
+__global__ void __launch_bounds__(kSortThreads, MATCH ? 4 : 3) downsweep_kernel(const uint32_t* __restrict__ keys_in,
                                                                     const uint32_t* __restrict__ vals_in,
                                                                     uint32_t* __restrict__ keys_out,
                                                                     uint32_t* __restrict__ vals_out,
