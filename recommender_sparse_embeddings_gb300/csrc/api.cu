@@ -27,8 +27,7 @@ struct tbe_handle {
     TableDesc* dtabs = nullptr;
     int32_t* dclass_tables = nullptr;
     int32_t* dhist_tables = nullptr;  // histogram-path tables: f16 ones, then bf16 ones
-    int n_hist_f16 = 0, n_hist_bf16 = 0;
-    size_t hist_smem_f16 = 0, hist_smem_bf16 = 0;
+    HistGroup hist_f16{}, hist_bf16{};
     // dense-backward tables (the histogram tables unless TBE_FLAG_SORTED_BACKWARD)
     int n_dense = 0;
     int32_t* ddense_tables = nullptr;   // device [n_dense]
@@ -69,14 +68,27 @@ size_t dev_block_bytes(int T) { return dense_off_offset(T) + 2 * sizeof(int64_t)
 
 // Small tables the tensor-core histogram path can take: 16-bit rows whose
 // dim is a multiple of 16 in [16, 256] (the MMA's N), 16-byte aligned data,
-// at most max_rows rows (the MMA's K, padded to 16), and H plus W^T within
-// the shared memory of one CTA.
-bool hist_eligible(const TableDesc& d, int64_t max_rows, size_t smem_limit) {
+// at most max_rows rows (the MMA's K, padded to 16).  Whether its A operand
+// and W^T fit one CTA's shared memory next to the other tables of its dtype
+// is checked when the group is formed.
+bool hist_eligible(const TableDesc& d, int64_t max_rows) {
     if (d.dtype != TBE_F16 && d.dtype != TBE_BF16) return false;
     if (d.dim % 16 != 0 || d.dim < 16 || d.dim > 256) return false;
     if (((uintptr_t)d.data % 16) != 0) return false;
-    if (d.rows > max_rows) return false;
-    return hist_smem_bytes(d.rows, d.dim) + 4096 <= smem_limit;
+    return d.rows <= max_rows;
+}
+
+// Adds table d to a histogram group if the group's shared memory (with some
+// room for the kernel's static arrays) still fits `limit`.
+bool hist_join(HistGroup& g, const TableDesc& d, size_t limit) {
+    const size_t ab = std::max(g.ab_bytes, hist_ab_bytes(d.rows, d.dim));
+    const size_t smem = hist_smem_bytes(ab);
+    if (smem + 4096 > limit) return false;
+    g.ab_bytes = ab;
+    g.smem = smem;
+    g.dmax = std::max(g.dmax, (int)d.dim);
+    ++g.n;
+    return true;
 }
 
 // Backward class of a table: dtype and row shape (vector lanes for dim 32,
@@ -224,9 +236,18 @@ Workspace bind(const tbe_handle* h, const Layout& L, void* base, bool scale) {
 // the batch shape.
 constexpr bool kLayoutWithScale = true;
 
+// The handle's kernels, streams and descriptor block belong to the device
+// that was current at tbe_create; a call made with another device current
+// is refused before anything launches.
+bool on_handle_device(const tbe_handle* h) {
+    int d = -1;
+    return cudaGetDevice(&d) == cudaSuccess && d == h->device;
+}
+
 int check_batch(const tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                 int64_t N, int32_t B) {
     if (!h) return TBE_ERR_INVALID_ARG;
+    if (!on_handle_device(h)) return TBE_ERR_INVALID_ARG;
     if (index_dtype != TBE_I32 && index_dtype != TBE_I64) return TBE_ERR_INVALID_ARG;
     if (N < 0 || B < 0) return TBE_ERR_INVALID_ARG;
     if (N >= (int64_t(1) << 30)) return TBE_ERR_UNSUPPORTED;
@@ -339,28 +360,28 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
         return cuda_fail(e);
     }
     std::vector<int32_t> hist_f16, hist_bf16;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+    // the tensor-core kernels may use up to the opt-in shared memory on this
+    // device (the limit is a per-device attribute of each kernel)
+    if (e == cudaSuccess) e = hist_configure(optin);
+    if (e == cudaSuccess) e = dense_configure(optin);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e);
+    }
     if (!(flags & TBE_FLAG_NO_HISTOGRAM)) {
-        int optin = 0;
-        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
-            optin = 0;
         // default: tables of at most 512 rows; forced: up to 1024
         const int64_t max_rows = (flags & TBE_FLAG_FORCE_HISTOGRAM) ? 1024 : 512;
         for (int t = 0; t < num_tables; ++t) {
             TableDesc& d = h->tabs[t];
-            if (!hist_eligible(d, max_rows, (size_t)optin)) continue;
+            if (!hist_eligible(d, max_rows)) continue;
+            HistGroup& g = d.dtype == TBE_F16 ? h->hist_f16 : h->hist_bf16;
+            if (!hist_join(g, d, (size_t)optin)) continue;
             d.path = PATH_HIST;
-            const size_t sm = hist_smem_bytes(d.rows, d.dim);
-            if (d.dtype == TBE_F16) {
-                hist_f16.push_back(t);
-                h->hist_smem_f16 = std::max(h->hist_smem_f16, sm);
-            } else {
-                hist_bf16.push_back(t);
-                h->hist_smem_bf16 = std::max(h->hist_smem_bf16, sm);
-            }
+            (d.dtype == TBE_F16 ? hist_f16 : hist_bf16).push_back(t);
         }
     }
-    h->n_hist_f16 = (int)hist_f16.size();
-    h->n_hist_bf16 = (int)hist_bf16.size();
     // dense backward: the histogram tables, unless the sorted path is asked for
     std::vector<int32_t> dense;
     std::vector<int64_t> dense_off;  // goff[0..n], then roff[0..n]
@@ -412,6 +433,8 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     h->dtabs = reinterpret_cast<TableDesc*>(static_cast<char*>(h->dev) + tabs_offset());
     h->dclass_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + class_list_offset(num_tables));
     h->dhist_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + hist_list_offset(num_tables));
+    h->hist_f16.tables = h->dhist_tables;
+    h->hist_bf16.tables = h->dhist_tables + hist_f16.size();
     h->ddense_tables = reinterpret_cast<int32_t*>(static_cast<char*>(h->dev) + dense_list_offset(num_tables));
     h->ddense_goff = reinterpret_cast<int64_t*>(static_cast<char*>(h->dev) + dense_off_offset(num_tables));
     h->ddense_roff = h->ddense_goff + (h->n_dense + 1);
@@ -504,9 +527,8 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
     a.parity = h->parity;
     a.num_sms = h->num_sms;
     rc = cuda_status(launch_forward(a, s));
-    if (rc == TBE_OK && h->n_hist_f16 + h->n_hist_bf16 > 0)
-        rc = cuda_status(launch_hist(a, h->dhist_tables, h->n_hist_f16, h->hist_smem_f16,
-                                     h->dhist_tables + h->n_hist_f16, h->n_hist_bf16, h->hist_smem_bf16, s));
+    if (rc == TBE_OK && h->hist_f16.n + h->hist_bf16.n > 0)
+        rc = cuda_status(launch_hist(a, h->hist_f16, h->hist_bf16, s));
     if (rc == TBE_OK) h->parity ^= 1;
     return rc;
 }
@@ -620,6 +642,7 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
 int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, const float* grad_out,
                        const tbe_optimizer* opt, void* workspace, size_t workspace_bytes, void* stream) {
     if (!h || !opt || !workspace) return TBE_ERR_INVALID_ARG;
+    if (!on_handle_device(h)) return TBE_ERR_INVALID_ARG;
     if (num_indices < 0 || batch_size < 0) return TBE_ERR_INVALID_ARG;
     if (num_indices >= (int64_t(1) << 30)) return TBE_ERR_UNSUPPORTED;
     if (opt->kind != TBE_OPT_SGD && opt->kind != TBE_OPT_ROWWISE_ADAGRAD) return TBE_ERR_INVALID_ARG;
@@ -698,7 +721,7 @@ int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void*
 }
 
 int tbe_get_error(tbe_handle* h, void* stream) {
-    if (!h) return TBE_ERR_INVALID_ARG;
+    if (!h || !on_handle_device(h)) return TBE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t bits = 0;
     cudaError_t e = cudaMemcpyAsync(&bits, &h->blk->error, sizeof bits, cudaMemcpyDeviceToHost, s);

@@ -555,6 +555,18 @@ __global__ void __launch_bounds__(256) dense_update_kernel(DenseArgs a, Workspac
         dense_update_row<DT_F32>(a, td, g, r, lane);
 }
 
+// The dense kernel's dynamic shared-memory limit, raised to the device's
+// opt-in maximum less its static shared memory (on the current device; the
+// attribute is per device).
+cudaError_t dense_configure(int optin) {
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, dense_mma_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(dense_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)fa.sharedSizeBytes);
+    return e;
+}
+
 // Clears the touched-row flags, sums, updates (all on stream s).
 cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
@@ -568,12 +580,6 @@ cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s
         const int Mp = tmin<int>(Mg, (a.max_rows + 127) / 128 * 128);
         smem = tmax<size_t>(smem, dense_smem_bytes(Mp, D));
         groups_max = tmax<int>(groups_max, (a.max_rows + Mg - 1) / Mg);
-    }
-    static size_t configured = 0;  // largest dynamic shared memory set so far
-    if (smem > configured) {
-        e = cudaFuncSetAttribute(dense_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
     }
     const unsigned grid = (unsigned)(a.n * groups_max * a.splits);
     dense_mma_kernel<<<grid, kDenseThreads, smem, s>>>(a, ws, groups_max);

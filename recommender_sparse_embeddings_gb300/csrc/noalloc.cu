@@ -64,8 +64,12 @@ extern "C" int tbe_backward_sgd_noalloc(tbe_handle* h, const void* indices, cons
     const int rc = scratch_address(&scratch);
     if (rc != TBE_OK) return rc;
     // The existing backward path clears the parts of the workspace that must
-    // start at zero (counters, histograms, look-back status) on `stream`
-    // before its kernels run, so the previous call's contents do no harm.
+    // start at zero (the counter block, the radix digit histograms, the first
+    // bag of every key tile) on `stream` before its kernels run, and its
+    // kernels reset the per-run chunk counters they use, so the previous
+    // call's contents do no harm.  It also refuses, before launching
+    // anything, a call made while a device other than the handle's is
+    // current (the scratch looked up above is then simply not used).
     return tbe_backward_sgd(h, indices, offsets, index_dtype, num_indices, batch_size,
                             per_sample_weights, grad_out, lr, scratch, kStaticScratchBytes, stream);
 }

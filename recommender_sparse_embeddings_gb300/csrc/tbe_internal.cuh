@@ -203,10 +203,18 @@ struct WgradArgs {
 
 cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s);
 
-// Small-table tensor-core path (hist.cu).
-size_t hist_smem_bytes(int64_t rows, int dim);
-cudaError_t launch_hist(const FwdArgs& a, const int32_t* hist_tables_f16, int n_f16, size_t smem_f16,
-                        const int32_t* hist_tables_bf16, int n_bf16, size_t smem_bf16, cudaStream_t s);
+// Small-table tensor-core path (hist.cu).  One launch per table dtype.
+struct HistGroup {
+    const int32_t* tables;  // device: the group's tables
+    int n;
+    int dmax;         // largest dim
+    size_t ab_bytes;  // largest (128 + dim) x rows padded to 64 x 2: one table's A and W^T operands
+    size_t smem;      // dynamic shared memory of the launch
+};
+size_t hist_ab_bytes(int64_t rows, int dim);
+size_t hist_smem_bytes(size_t ab_bytes);
+cudaError_t hist_configure(int optin_smem);
+cudaError_t launch_hist(const FwdArgs& a, const HistGroup& f16, const HistGroup& bf16, cudaStream_t s);
 
 struct Workspace {
     uint32_t* counters;   // [64]
@@ -321,6 +329,7 @@ struct DenseArgs {
     int splits;              // parts each table's bags are split into (one gradient slice each)
     int grad_vec;            // grad is 16-byte aligned with total_d % 4 == 0 (float4 rows)
 };
+cudaError_t dense_configure(int optin_smem);
 cudaError_t launch_dense(const DenseArgs& a, const Workspace& ws, cudaStream_t s);
 
 // 128-row M tiles per dense-backward CTA for dim D: the short and the long

@@ -23,6 +23,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     return d;
 }
 
+// The same descriptor for a K-major operand in the 128-byte swizzled layout:
+// atoms of 8 rows x 128 bytes (1024-byte aligned), the 16-byte chunk c of row
+// r of an atom stored at chunk c ^ r; SBO = bytes between 8-row groups.  The
+// leading offset is unused in this layout (one MMA's K slice, 32 bytes, lies
+// inside the atom); a K step within the atom moves the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo) {
+    return smem_desc(addr, 16u, sbo) | ((uint64_t)2u << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B of the same
 // 16-bit type (0 = f16, 1 = bf16), both K-major, N >> 3 at bit 17, M >> 4 at
 // bit 24.

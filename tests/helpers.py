@@ -51,6 +51,36 @@ def accumulation_allowance(terms_abs_sum, n_terms, scale) -> np.ndarray:
     return 4.0 * np.sqrt(n) * 2.0 ** -24 * np.asarray(terms_abs_sum, np.float64) * np.asarray(scale, np.float64)
 
 
+def pooled_abs_sum(tables, indices, offsets, B, weights=None, pooling="sum"):
+    """Per output element, the sum of the magnitudes of its terms,
+    sum_i |s_i| * |W[idx_i, j]| (the oracle run on |W| and |w|), and the
+    length of each output row's bag (per table, broadcast over its columns)."""
+    abs_tabs = [t.abs() for t in tables]
+    absw = None if weights is None else weights.abs()
+    a, _ = oracle_forward(abs_tabs, indices, offsets, B, absw, pooling)
+    off = np.asarray(np_index(offsets), dtype=np.int64)
+    lens = np.diff(off).reshape(len(tables), B)
+    n = np.concatenate([np.repeat(lens[t][:, None], int(tables[t].shape[1]), axis=1) for t in range(len(tables))],
+                       axis=1)
+    return a, n
+
+
+def histogram_allowance(abs_sum, n_terms) -> np.ndarray:
+    """Absolute error allowance of a pooled output of the tensor-core
+    histogram path beyond the fp32 tolerance.
+
+    Each histogram entry reaches the tensor cores as two fp16 terms hi + lo
+    (bag-wise scaled into fp16's range), so it carries a relative error of at
+    most 2^-22 (one fp16 rounding of lo, which is at most 2^-11 of the entry);
+    2^-21 * abs_sum covers that.  The products are then summed in fp32, which
+    rounds like any fp32 sum of n terms: 4 * sqrt(n) * 2^-24 * abs_sum, as in
+    accumulation_allowance.  The allowance matters only where the output
+    cancels to far below its terms."""
+    n = np.maximum(np.asarray(n_terms, dtype=np.float64), 1.0)
+    a = np.asarray(abs_sum, dtype=np.float64)
+    return 2.0 ** -21 * a + 4.0 * np.sqrt(n) * 2.0 ** -24 * a
+
+
 def assert_close(got, ref, rtol, atol, what=""):
     """|got - ref| <= atol + rtol * |ref| element-wise (atol may be an array)."""
     got = np.asarray(got, dtype=np.float64)

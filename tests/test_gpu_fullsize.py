@@ -23,12 +23,12 @@ import torch
 import oracle
 import recommender_sparse_embeddings_gb300 as tbe
 import workloads
-from helpers import DT_NAME, FP32_TOL, LOWP_TOL, accumulation_allowance, assert_close, table_bits
+from helpers import (DT_NAME, FP32_TOL, LOWP_TOL, accumulation_allowance, assert_close, histogram_allowance,
+                     table_bits)
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-HIST_TOL = dict(rtol=1e-2, atol=1e-4)
 
 
 def _rows_host(t: torch.Tensor, rows: np.ndarray) -> torch.Tensor:
@@ -94,14 +94,25 @@ def test_full_size(cid):
         if w is not None:
             c_w.append(w[pos])
     c_off = np.concatenate([[0], np.cumsum(c_len)]).astype(np.int64)
-    ref, skipped = oracle.forward(c_tabs, c_dt, np.concatenate(c_ind).astype(np.int64), c_off, len(bsample),
-                                  weights=None if w is None else np.concatenate(c_w), pooling=cfg.pooling)
+    c_ind_all = np.concatenate(c_ind).astype(np.int64)
+    c_w_all = None if w is None else np.concatenate(c_w)
+    ref, skipped = oracle.forward(c_tabs, c_dt, c_ind_all, c_off, len(bsample), weights=c_w_all,
+                                  pooling=cfg.pooling)
     assert skipped == 0
+    # the histogram path's allowance: the terms' magnitudes (the oracle on
+    # |W| and |w|) and the bag lengths
+    abs_tabs = [np.abs(tb) if dt == "f32" else tb & np.uint16(0x7fff) for dt, tb in zip(c_dt, c_tabs)]
+    abs_ref, _ = oracle.forward(abs_tabs, c_dt, c_ind_all, c_off, len(bsample),
+                                weights=None if c_w_all is None else np.abs(c_w_all), pooling=cfg.pooling)
+    c_lens = np.diff(c_off).reshape(T, len(bsample))
     got = out[torch.from_numpy(bsample).to(DEV)].cpu().numpy()
     for t in range(T):
         cols = slice(doff[t], doff[t + 1])
-        tol = HIST_TOL if paths[t] == "histogram" else FP32_TOL
-        assert_close(got[:, cols], ref[:, cols], what=f"cfg{cid} forward table {t}", **tol)
+        atol = FP32_TOL["atol"]
+        if paths[t] == "histogram":
+            atol = atol + histogram_allowance(abs_ref[:, cols], c_lens[t][:, None])
+        assert_close(got[:, cols], ref[:, cols], what=f"cfg{cid} forward table {t}", rtol=FP32_TOL["rtol"],
+                     atol=atol)
 
     # ---- backward: sampled rows
     t_of = bag_of // B
