@@ -2,15 +2,19 @@
 run-length encoding, segment reduction, fused optimizer update) per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 2] [--index-dtype int64] [--no-e2e] [--no-cpu-baseline]
+                  [--config 4] [--extra 2,3,5] [--index-dtype int64] [--no-e2e]
+                  [--no-cpu-baseline]
 
-Prints one JSON line on rank 0.  The default workload is the 8-table fp32
-config (T=8, 1M rows x 128, B=8192, Poisson(20) bags, Zipf(1.05) indices, SGD).
-Timing: CUDA events on the launching stream around each step, L2 flushed
-(256 MiB write) before every step outside the timed interval, W untimed
-warm-up steps, barrier + synchronize around the K timed steps, max over ranks.
-Under torchrun every rank runs its own replica (the path does not shard:
-weak scaling, no collective on the data path).
+Prints one JSON line on rank 0.  The headline workload (default) is the
+hot-row backward stress case: T=16 bf16 tables of 5M rows x 128, B=65536,
+pooling factor 32, Zipf(1.2) indices, row-wise Adagrad.  The other workloads
+named by --extra are measured in the same run with the same step counts and
+reported under "workloads".  Timing: CUDA events on the launching stream
+around each step, L2 flushed (256 MiB write) before every step outside the
+timed interval, W untimed warm-up steps, barrier + synchronize around the K
+timed steps; ms_per_step is the median of the K per-step intervals, max over
+ranks.  Under torchrun every rank runs its own replica (the path does not
+shard: weak scaling, no collective on the data path).
 """
 
 from __future__ import annotations
@@ -124,15 +128,16 @@ def wgrad_bytes(specs, batch_lengths, N, B, T, idx_bytes):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) read by a thread; summary() keeps the
-    samples taken between mark_start() and mark_end()."""
+    """nvidia-smi samples (every period_ms) read by a thread; summary() keeps
+    the samples taken between mark_start() and mark_end()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.samples = []  # (host time, line)
         self.t0 = self.t1 = None
@@ -143,7 +148,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -178,11 +183,14 @@ class ClockSampler:
             self.thread.join(timeout=5)
         return False
 
-    def summary(self):
+    def summary(self, window=None):
+        """Median SM clock, max clock and throttle reasons seen between
+        mark_start() and mark_end() (or inside `window` = (t0, t1))."""
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        t0 = self.t0 if self.t0 is not None else -1e30
-        t1 = (self.t1 + 0.1) if self.t1 is not None else 1e30
+        w0, w1 = window if window is not None else (self.t0, self.t1)
+        t0 = w0 if w0 is not None else -1e30
+        t1 = (w1 + 0.1) if w1 is not None else 1e30
         for ts, l in self.samples:
             if not (t0 <= ts <= t1):
                 continue
@@ -241,7 +249,7 @@ class OracleSample:
     first `tables_in_sample` tables with the full B and the same laws.  One
     step = oracle forward + oracle backward (with the workload's optimizer)."""
 
-    def __init__(self, cfg, tables_in_sample: int = 2, bags: int = 0):
+    def __init__(self, cfg, tables_in_sample: int = 2, bags: int = 0, threads: int = 1):
         import numpy as np
 
         total_tables = len(workloads.realize_tables(cfg))
@@ -260,12 +268,18 @@ class OracleSample:
         self.state = (np.zeros(sum(s.rows for s in specs), np.float32)
                       if cfg.optimizer == "adagrad" else None)
         self.N = batch.N
+        self.threads = threads
         self.sample = (f"{tables_in_sample} of {total_tables} tables, "
-                       f"B={cfg.B}, {batch.N} lookups per fwd+bwd step, one core")
+                       f"B={cfg.B}, {batch.N} lookups per fwd+bwd step")
 
     def step(self) -> float:
         import oracle
 
+        # the pinned one-thread build, or the OpenMP timing build on `threads` cores
+        if self.threads == 1:
+            oracle.use_plain_build()
+        else:
+            oracle.use_timing_build(self.threads)
         c = self.cfg
         t0 = time.perf_counter()
         oracle.forward(self.tabs, self.names, self.ind, self.off, c.B, weights=self.w,
@@ -291,26 +305,36 @@ def _mean_bag_length(spec) -> float:
     return (spec.length[1] + spec.length[2]) / 2.0
 
 
-def cpu_oracle_run(cfg, seconds: float = 10.0):
-    s = OracleSample(cfg)
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_run(cfg, seconds: float = 10.0, threads: int = 1, sample=None):
+    """The oracle as it stands on a bounded sample of the workload: one core
+    (the pinned build) or `threads` cores (the OpenMP timing build of the
+    same source).  Runs whole steps until `seconds` of CPU time pass."""
+    s = sample if sample is not None else OracleSample(cfg)
+    s.threads = threads
+    s.step()  # first touch of the sample's memory, untimed
     steps, el = 0, 0.0
     while steps == 0 or el < seconds:
         el += s.step()
         steps += 1
     return {"lookups": s.N * steps, "seconds": el, "steps": steps,
-            "sample": s.sample + f", {steps} steps"}
+            "sample": s.sample + f", {steps} steps on {threads} thread(s)", "oracle_sample": s}
 
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args):
-    import recommender_sparse_embeddings_gb300 as tbe
-
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    cfg = workloads.get_config(args.config)
+def measure(tbe, cfg_id, args, dev, clk, headline):
+    """One workload: generate, warm up, time K steps (forward + preparation,
+    then apply), time each call alone, and (headline only) the end-to-end
+    run through pinned host buffers.  Returns the workload's record."""
+    world, rank, _ = dist_env()
+    cfg = workloads.get_config(cfg_id)
     specs = workloads.realize_tables(cfg)
     if args.tables:
         specs = specs[:args.tables]
@@ -368,31 +392,29 @@ def run_ours(args):
 
     # timed region: one step = forward + preparation (concurrent), then apply
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        clk.mark_start()
-        for k in range(args.steps):
-            flush.zero_()
-            e = ev[k]
-            e[0].record(stream); run_fp()
-            e[1].record(stream); run_ap()
-            e[2].record(stream)
-        torch.cuda.synchronize()
-        clk.mark_end()
-        barrier()
-    seg = {"forward+prepare": 0.0, "apply": 0.0}
-    for e in ev:
-        seg["forward+prepare"] += e[0].elapsed_time(e[1])
-        seg["apply"] += e[1].elapsed_time(e[2])
-    local_ms = sum(seg.values())
-    total_ms = reduce_max(local_ms, dev)
-    units = reduce_sum(float(N) * args.steps, dev)
+    barrier()
+    torch.cuda.synchronize()
+    t_start = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        e = ev[k]
+        e[0].record(stream); run_fp()
+        e[1].record(stream); run_ap()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter()
+    barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    seg_lists = {"forward+prepare": [e[0].elapsed_time(e[1]) for e in ev],
+                 "apply": [e[1].elapsed_time(e[2]) for e in ev]}
+    med_ms = reduce_max(statistics.median(step_ms), dev)
+    mean_ms = reduce_max(sum(step_ms) / len(step_ms), dev)
+    units = reduce_sum(float(N), dev)  # lookups of one step over all ranks
     rc = tbe.tbe_get_error(h)
     if rc != tbe.TBE_OK:
         raise RuntimeError(f"device error in timed region: {tbe.tbe_strerror(rc)}")
 
-    # per-call breakdown (a separate run, each call timed alone)
+    # per-call breakdown (a separate run, each call timed alone; medians)
     nb_steps = min(args.steps, 200)
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb_steps)]
     for k in range(nb_steps):
@@ -403,11 +425,8 @@ def run_ours(args):
         e[2].record(stream); apply()
         e[3].record(stream)
     torch.cuda.synchronize()
-    brk = {"forward": 0.0, "prepare": 0.0, "apply": 0.0}
-    for e in evb:
-        brk["forward"] += e[0].elapsed_time(e[1]) / nb_steps
-        brk["prepare"] += e[1].elapsed_time(e[2]) / nb_steps
-        brk["apply"] += e[2].elapsed_time(e[3]) / nb_steps
+    brk = {name: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evb)
+           for i, name in enumerate(("forward", "prepare", "apply"))}
 
     # per-sample weight gradient (weighted batches): timed alone, after a flush
     wg_ms = None
@@ -421,7 +440,7 @@ def run_ours(args):
             tbe.tbe_per_sample_weight_grad(h, ind, off, B, grad, gw_out)
             evw[k][1].record(stream)
         torch.cuda.synchronize()
-        wg_ms = sum(a.elapsed_time(b) for a, b in evw) / nb_steps
+        wg_ms = statistics.median(a.elapsed_time(b) for a, b in evw)
         rc = tbe.tbe_get_error(h)
         if rc != tbe.TBE_OK:
             raise RuntimeError(f"device error in the weight gradient: {tbe.tbe_strerror(rc)}")
@@ -432,7 +451,8 @@ def run_ours(args):
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
     offs = off.to(torch.int64).cpu()
-    for t, p in enumerate(tbe.tbe_table_paths(h)):
+    paths = tbe.tbe_table_paths(h)
+    for t, p in enumerate(paths):
         if p == "histogram" and not args.sorted_backward:
             lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
             U += int(torch.unique(ind[lo:hi]).numel())
@@ -457,10 +477,9 @@ def run_ours(args):
     nbytes = algorithmic_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize, w is not None,
                                cfg.optimizer, U, passes)
     nbytes["forward+prepare"] = nbytes["forward"] + nbytes["prepare"]
-    ms_step = total_ms / args.steps
-    value = units / (total_ms / 1e3)
+    value = units / (med_ms / 1e3)
     peak, peak_src = measured_hbm_peak()
-    seg_ms = {k: v / args.steps for k, v in seg.items()}
+    seg_ms = {k: statistics.median(v) for k, v in seg_lists.items()}
     # roofline of the dominant call (forward, prepare or apply: the one that
     # takes longest alone).  The apply is timed inside the timed region on the
     # caller's stream (its side streams join back before the closing event);
@@ -469,14 +488,14 @@ def run_ours(args):
     call_ms["apply"] = seg_ms["apply"]
     dominant = max(call_ms, key=call_ms.get)
     achieved = nbytes[dominant] / (call_ms[dominant] / 1e3) / 1e9
-    timing_src = ("timed region, CUDA events on the caller's stream" if dominant == "apply"
-                  else "per-call run, CUDA events on the caller's stream")
+    timing_src = ("timed region, CUDA events on the caller's stream, median of the steps" if dominant == "apply"
+                  else "per-call run, CUDA events on the caller's stream, median of the steps")
+    traffic = profile_traffic(dominant, cfg.cfg_id, T)
     # our kernels per step: forward (gather pool if any gather table, long
     # bags, one histogram launch per dtype with histogram tables); prepare
     # (bag marks, [compaction], keys, per radix pass [upsweep] + scan +
     # downsweep, run-length count/scan/write, chunk count/scan/write); apply
     # (one per backward class of the sorted-path tables, dense sums + update)
-    paths = tbe.tbe_table_paths(h)
     hist_dtypes = {s.dtype for s, p in zip(specs, paths) if p == "histogram"}
     dense = bool(hist_dtypes) and not args.sorted_backward  # histogram tables' dense backward
     fwd_launches = (1 if any(p != "histogram" for p in paths) else 0) + 1 + len(hist_dtypes)
@@ -485,12 +504,53 @@ def run_ours(args):
     apply_launches = backward_classes(sorted_specs) + (2 if dense else 0)
     launches_per_step = fwd_launches + prep_launches + apply_launches
 
+    rec = {
+        "value": value,
+        "unit": "lookups/s",
+        "ms_per_step": med_ms,
+        "ms_per_step_mean": mean_ms,
+        "timed_region_s": t_end - t_start,
+        "dtype": "f32" if all(sp.dtype == "f32" for sp in specs) else "mixed(f32 accumulate)",
+        "paths": sorted(set(paths)),
+        "config": {"workload": cfg.description + (f" (first {T} of the tables)" if args.tables else ""),
+                   "config_id": cfg.cfg_id, "T": T, "B": B, "N_lookups": N, "unique_rows": U,
+                   "index_dtype": args.index_dtype, "optimizer": cfg.optimizer,
+                   "parallelism": f"replicas x{world}",
+                   "launch": "CUDA graph replay" if args.graph else "stream launches",
+                   "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
+        "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
+                "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
+                "frac": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9 / peak,
+                "ms": brk["forward"]},
+        "wgrad": None if wg_ms is None else {
+            "ms": wg_ms, "bytes": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize),
+            "gbs": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9,
+            "frac": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9 / peak,
+            "note": "per-sample weight gradient, timed alone outside the step"},
+        "step_gbs": nbytes["step"] / (med_ms / 1e3) / 1e9,
+        "segments_ms": seg_ms,
+        "breakdown_ms_sequential": brk,
+        "algorithmic_bytes": nbytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "dram_frac": None if traffic is None else traffic / (call_ms[dominant] / 1e3) / 1e9 / peak,
+                     "kernel": DOMINANT_KERNELS[dominant], "call": dominant,
+                     "ms_per_launch": call_ms[dominant], "bytes_per_launch": nbytes[dominant],
+                     "timing": timing_src, "peak_source": peak_src,
+                     "segment_fracs": {k: nbytes[k] / (v / 1e3) / 1e9 / peak for k, v in seg_ms.items()},
+                     "compulsory": {k: {"bytes": compulsory[k],
+                                        "frac": compulsory[k] / (call_ms[k] / 1e3) / 1e9 / peak}
+                                    for k in ("forward", "apply")}},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary((t_start, t_end)),
+    }
+
     # end-to-end through the public API: inputs from pinned host memory every
     # step, pooled output read back every step.  Two sets of device buffers:
     # the next step's inputs copy in while this step computes, and this
     # step's output copies out while the next one starts.
-    e2e = None
-    if not args.no_e2e:
+    rec["e2e"] = None
+    if headline and not args.no_e2e:
         h_ind = ind.cpu().pin_memory()
         h_off = off.cpu().pin_memory()
         h_w = None if w is None else w.cpu().pin_memory()
@@ -548,71 +608,76 @@ def run_ours(args):
         e2e_ms = reduce_max(e_start.elapsed_time(e_end), dev)
         h2d = ind.numel() * ind.element_size() + off.numel() * off.element_size() + \
             (0 if w is None else w.numel() * 4) + grad.numel() * 4
-        e2e = {"value": units / (e2e_ms / 1e3), "unit": "lookups/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": out.numel() * 4, "ms_per_step": e2e_ms / args.steps,
-               "pipelining": "two buffer sets: step k+1's inputs copy in during step k, step k's "
-                             "output copies out beside its apply",
-               "l2": "not flushed between steps (one timed interval over all steps); the tables "
-                     "exceed L2"}
+        rec["e2e"] = {"value": units * args.steps / (e2e_ms / 1e3), "unit": "lookups/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": out.numel() * 4, "ms_per_step": e2e_ms / args.steps,
+                      "pipelining": "two buffer sets: step k+1's inputs copy in during step k, step k's "
+                                    "output copies out beside its apply",
+                      "l2": "not flushed between steps (one timed interval over all steps); the tables "
+                            "exceed L2"}
+        rc = tbe.tbe_get_error(h)
+        if rc != tbe.TBE_OK:
+            raise RuntimeError(f"device error in the end-to-end run: {tbe.tbe_strerror(rc)}")
+    h.close()
+    del tables, batch, grad, ws, out, state, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import recommender_sparse_embeddings_gb300 as tbe
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    extra = [c for c in args.extra if c != args.config]
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        head = measure(tbe, args.config, args, dev, clk, headline=True)
+        others = {str(c): measure(tbe, c, args, dev, clk, headline=False) for c in extra}
+        clk.mark_end()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = cpu_oracle_run(cfg, seconds=args.cpu_seconds)
-        cpu = {"value": r["lookups"] / r["seconds"], "unit": "lookups/s", "cores": 1,
-               "kind": "oracle", "sample": r["sample"]}
+        cfg = workloads.get_config(args.config)
+        one = cpu_oracle_run(cfg, seconds=args.cpu_seconds, threads=1)
+        cores = host_cores()
+        allc = cpu_oracle_run(cfg, seconds=args.cpu_seconds, threads=cores, sample=one["oracle_sample"])
+        cpu = {"value": allc["lookups"] / allc["seconds"], "unit": "lookups/s", "cores": cores,
+               "kind": "oracle", "sample": allc["sample"],
+               "one_core": {"value": one["lookups"] / one["seconds"], "cores": 1, "sample": one["sample"]},
+               "note": "all host cores: the oracle's OpenMP build of the same source (parallel over bags "
+                       "and over runs; the sort is one qsort); one core: the pinned plain build"}
 
     if rank == 0:
         line = {
             "metric": METRIC,
-            "value": value,
+            "value": head["value"],
             "unit": "lookups/s",
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": ms_step,
+            "ms_per_step": head["ms_per_step"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32" if all(s.dtype == "f32" for s in specs) else "mixed(f32 accumulate)",
+            "dtype": head["dtype"],
             "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
                     "pages' production shard configurations)",
-            "paths": sorted(set(paths)),
-            "config": {"workload": cfg.description + (
-                           f" (first {T} of the tables)" if args.tables else ""),
-                       "config_id": cfg.cfg_id, "T": T, "B": B,
-                       "N_lookups": N, "unique_rows": U, "index_dtype": args.index_dtype,
-                       "optimizer": cfg.optimizer, "parallelism": f"replicas x{world}",
-                       "launch": "CUDA graph replay" if args.graph else "stream launches",
-                       "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
-            "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
-                    "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
-                    "frac": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9 / peak,
-                    "ms": brk["forward"]},
-            "wgrad": None if wg_ms is None else {
-                "ms": wg_ms, "bytes": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize),
-                "gbs": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9,
-                "frac": wgrad_bytes(specs, batch.lengths, N, B, T, idx_dtype.itemsize) / (wg_ms / 1e3) / 1e9 / peak,
-                "note": "per-sample weight gradient, timed alone outside the step"},
-            "step_gbs": nbytes["step"] / (ms_step / 1e3) / 1e9,
-            "segments_ms": seg_ms,
-            "breakdown_ms_sequential": brk,
-            "algorithmic_bytes": nbytes,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profile_traffic(dominant, cfg.cfg_id, T),
-                         "kernel": DOMINANT_KERNELS[dominant], "call": dominant,
-                         "ms_per_launch": call_ms[dominant], "bytes_per_launch": nbytes[dominant],
-                         "timing": timing_src, "peak_source": peak_src,
-                         "segment_fracs": {k: nbytes[k] / (v / 1e3) / 1e9 / peak for k, v in seg_ms.items()},
-                         "compulsory": {k: {"bytes": compulsory[k],
-                                            "frac": compulsory[k] / (call_ms[k] / 1e3) / 1e9 / peak}
-                                        for k in ("forward", "apply")}},
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
         }
+        for k in ("paths", "config", "fwd", "wgrad", "step_gbs", "segments_ms", "breakdown_ms_sequential",
+                  "algorithmic_bytes", "roofline", "ms_per_step_mean", "timed_region_s"):
+            line[k] = head[k]
+        line["cpu_baseline"] = cpu
+        line["e2e"] = head["e2e"]
+        line["gpu_launches"] = head["gpu_launches"]
+        line["clocks"] = head["clocks"]
+        line["clocks_all_workloads"] = clk.summary()
+        line["timing"] = ("ms_per_step and every *_ms: median of the K per-step CUDA-event intervals "
+                          "(L2 flushed before each step); value = lookups per step / median step time")
+        line["workloads"] = {c: {k: v for k, v in r.items() if k not in ("e2e",)} for c, r in others.items()}
         print(json.dumps(line), flush=True)
-    h.close()
 
 
 # ---------------------------------------------------------- reference arm
@@ -623,12 +688,14 @@ def run_reference(args):
         return
     cfg = workloads.get_config(args.config)
     # bound the per-step sample so warm-up + timed steps take about two minutes
-    # (the oracle does on the order of 1e6 lookups per second on one core)
+    # (the oracle does on the order of 1e6 lookups per second per core; the
+    # sort stays on one core)
     specs = workloads.realize_tables(cfg)
     per_bag = max(1.0, _mean_bag_length(specs[0]))
     budget_lookups = 120.0 * 1.0e6 / (args.steps + args.warmup)
     bags = int(min(cfg.B, max(64, budget_lookups / per_bag)))
-    sample = OracleSample(cfg, tables_in_sample=1, bags=bags)
+    cores = host_cores()
+    sample = OracleSample(cfg, tables_in_sample=1, bags=bags, threads=cores)
     for _ in range(args.warmup):
         sample.step()
     total_s = sum(sample.step() for _ in range(args.steps))
@@ -648,10 +715,10 @@ def run_reference(args):
         "dtype": "f64 accumulate",
         "data": "synthetic: seeded generators with the workload's laws",
         "config": {"workload": cfg.description, "config_id": cfg.cfg_id,
-                   "reference": "CPU oracle (plain C, one core); the pages ship no "
+                   "reference": "CPU oracle (plain C, OpenMP build on all host cores); the pages ship no "
                                 "implementation to run"},
-        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "kind": "oracle",
-                         "sample": sample.sample},
+        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": cores, "kind": "oracle",
+                         "sample": sample.sample + f", {cores} threads"},
         "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -664,7 +731,9 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--config", type=int, default=4, help="headline workload")
+    p.add_argument("--extra", type=lambda x: [int(c) for c in x.split(",") if c.strip()], default=[2, 3, 5],
+                   help="other workloads measured in the same run (comma list; empty: none)")
     p.add_argument("--index-dtype", choices=["int64", "int32"], default="int64")
     p.add_argument("--graph", action="store_true",
                    help="replay the step's two calls as captured CUDA graphs")

@@ -31,7 +31,9 @@
  *    stream).  Every call is asynchronous on that stream and performs no host
  *    synchronisation, except tbe_get_error.
  *  - A handle must not be used from two host threads, or on two streams whose
- *    work overlaps, at the same time.
+ *    work overlaps, at the same time.  It belongs to the device that was
+ *    current at tbe_create; a call made while another device is current
+ *    returns TBE_ERR_INVALID_ARG before anything is launched.
  *  - Return value: TBE_OK (0) or a negative TBE_ERR_* code.  Argument errors
  *    are reported synchronously and nothing is launched.  Problems only the
  *    GPU can see (an index out of range, malformed offsets, a bounded wait
@@ -139,7 +141,13 @@ typedef struct {
 /* ------------------------------------------------------------------ handle */
 
 /* Validates the table list and builds the device descriptor block (row
- * bases, column offsets, per-table lookup schedule).  `tables`: host array
+ * bases, column offsets, per-table lookup schedule).  Defining passages: the
+ * operator holds the tables it pools ("Optimizing Recommendation Systems
+ * with FBTriton Table Batched Embeddings", "Implementation Guide: Integrating
+ * TBE": the call takes the embedding tables); the choice of the histogram
+ * tensor-core path for eligible small tables is made here (kimbodo "What
+ * Happened"; the pages give no eligibility rule, this library's is stated
+ * under TBE_FLAG_*).  `tables`: host array
  * of num_tables entries (copied; the data pointers are kept).  pooling:
  * tbe_pooling.  flags: TBE_FLAG_*.  On success *out receives the handle.
  * Errors: INVALID_ARG (null/zero/negative sizes, bad enums), UNSUPPORTED
@@ -148,7 +156,8 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
                tbe_handle** out);
 
 /* Frees the descriptor block.  The caller's memory is untouched.  Must not be
- * called while work that uses the handle may still run. */
+ * called while work that uses the handle may still run.  (Resource
+ * management of this library; the pages have no counterpart.) */
 void tbe_destroy(tbe_handle* h);
 
 /* ----------------------------------------------------------------- forward */
@@ -165,10 +174,18 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
 
 /* ---------------------------------------------------------------- backward */
 
-/* Bytes of device workspace the backward calls need for this batch shape. */
+/* Bytes of device workspace the backward calls need for this batch shape:
+ * the arrays of the backward's preparation steps (one key, position, bag and
+ * scale per lookup; the sort's ping-pong buffers and digit counts; distinct
+ * keys and run starts; partial sums of the runs of at least 256 lookups), as
+ * kimbodo "Kimbodo Engineering Perspective" (transpose, sort, run-length
+ * encoding) and "What Happened" (separate accumulation for long runs) define
+ * them.  0 for a null handle or a negative count. */
 size_t tbe_backward_workspace_bytes(const tbe_handle* h, int64_t num_indices, int32_t batch_size);
 
-/* Where the preparation step leaves its arrays inside the workspace. */
+/* Where the preparation step leaves its arrays inside the workspace (the
+ * sorted keys and run-length encoding of kimbodo "Kimbodo Engineering
+ * Perspective"), for tests and inspection. */
 int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int32_t batch_size,
                                   tbe_ws_layout* out);
 
@@ -211,13 +228,24 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size,
                        const float* grad_out, const tbe_optimizer* opt, void* workspace,
                        size_t workspace_bytes, void* stream);
 
-/* prepare + apply with SGD. */
+/* prepare + apply with SGD: the backward pass of "FBTriton Rewrites Table
+ * Batched Embedding", "Responsibilities of the forward and backward passes"
+ * (scatter the upstream gradient to the looked-up rows, accumulating repeated
+ * rows) with kimbodo "What Happened"'s grouping by (table, row) and one
+ * optimizer update per row.  The pages name no optimizer; SGD is the plain
+ * w <- w - lr * g (no momentum, no weight decay).  Arguments as
+ * tbe_backward_prepare and tbe_backward_apply. */
 int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                      int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
                      const float* grad_out, float lr, void* workspace, size_t workspace_bytes,
                      void* stream);
 
-/* prepare + apply with row-wise Adagrad (state as in tbe_optimizer). */
+/* prepare + apply with row-wise Adagrad (state as in tbe_optimizer): the same
+ * backward pass as tbe_backward_sgd ("FBTriton Rewrites Table Batched
+ * Embedding", "Responsibilities of the forward and backward passes"; kimbodo
+ * "What Happened"), with the row-wise Adagrad step defined at tbe_optimizer.
+ * The pages do not define row-wise Adagrad; that formula is this library's
+ * reading (eps outside the root, the mean of g_j^2 added to the state). */
 int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void* offsets,
                                  int32_t index_dtype, int64_t num_indices, int32_t batch_size,
                                  const float* per_sample_weights, const float* grad_out,
@@ -273,10 +301,16 @@ int tbe_per_sample_weight_grad(tbe_handle* h, const void* indices, const void* o
 
 /* Synchronises `stream`, returns the first device-detected error since the
  * last call (TBE_ERR_TIMEOUT before TBE_ERR_BAD_OFFSETS before
- * TBE_ERR_INDEX_OOB) or TBE_OK, and clears it. */
+ * TBE_ERR_INDEX_OOB) or TBE_OK, and clears it.  The pages define no error
+ * reporting; this reports the conditions of the batch layout read from
+ * "Optimizing Recommendation Systems with FBTriton Table Batched
+ * Embeddings", "Implementation Guide: Integrating TBE" (offsets cut one flat
+ * index list into bags, so they must rise from 0 to N; an index names a row
+ * of its table), plus the bounded waits of the tensor-core kernels. */
 int tbe_get_error(tbe_handle* h, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code.  (Library plumbing; the pages have no
+ * counterpart.) */
 const char* tbe_strerror(int code);
 
 /* The cudaError_t of the last CUDA call that failed in a tbe_* call of this
@@ -285,7 +319,8 @@ int tbe_last_cuda_error(void);
 
 /* Per-table schedule chosen at create time, for tests and tuning:
  * out_path[t] = 0 gather path (vector), 1 gather path (element-wise),
- * 2 histogram tensor-core path. */
+ * 2 histogram tensor-core path (kimbodo "What Happened": eligible small
+ * tables take the histogram path). */
 int tbe_table_paths(const tbe_handle* h, int32_t* out_path);
 
 #ifdef __cplusplus

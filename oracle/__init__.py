@@ -28,6 +28,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tbe_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libtbe_oracle.so")
+# The timing build: the same source at -O3 with OpenMP, whose parallel loops
+# (bags of the forward pass, runs of the backward pass) run on the host's
+# cores.  Each bag's and each run's sums are the same sequence of additions
+# as in the plain build; only the CPU baseline of bench.py loads it.
+_OMP_LIB_PATH = os.path.join(_HERE, "libtbe_oracle_omp.so")
 
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 OPT_CODES = {"none": 0, "sgd": 1, "adagrad": 2, "rowwise_adagrad": 2}
@@ -44,16 +49,54 @@ def build(force: bool = False) -> str:
             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
-                               "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+                               "-ffp-contract=off", "-Wall", "-Wextra", "-Wno-unknown-pragmas", "-o", tmp,
+                               _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def build_timing(force: bool = False) -> str:
+    """Compile the timing build ``oracle/libtbe_oracle_omp.so`` (gcc -O3
+    -fopenmp, contraction still off)."""
+    if force or not os.path.exists(_OMP_LIB_PATH) or (
+            os.path.getmtime(_OMP_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _OMP_LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O3", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _OMP_LIB_PATH)
+    return _OMP_LIB_PATH
+
+
+_timing = False
+
+
+def use_timing_build(threads: int) -> int:
+    """Route the calls below to the timing build with `threads` threads;
+    returns the thread count in effect.  (For bench.py's CPU baseline.)"""
+    global _timing, _lib
+    if not _timing:
+        build_timing()
+        _timing, _lib = True, None
+    return int(_load().oracle_set_threads(int(threads)))
+
+
+def use_plain_build() -> None:
+    """Route the calls back to the plain (pinned, one-thread) build."""
+    global _timing, _lib
+    if _timing:
+        _timing, _lib = False, None
 
 
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB_PATH)
+        if _timing:
+            lib = ctypes.CDLL(_OMP_LIB_PATH)
+        else:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+        lib.oracle_set_threads.argtypes = [ctypes.c_int32]
+        lib.oracle_set_threads.restype = ctypes.c_int
         P = ctypes.c_void_p
         i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
         lib.oracle_forward.argtypes = [i32, P, P, P, P, i32, i32, P, P, i64, P, i32, P, P]

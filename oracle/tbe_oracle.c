@@ -47,6 +47,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_F32 0
 #define OR_F16 1
@@ -56,6 +59,18 @@
 #define OR_BAD_ARG -1
 #define OR_BAD_OFFSETS -2
 #define OR_NO_MEMORY -3
+
+/* Threads of the parallel loops in the timing build (compiled with OpenMP);
+ * returns the count in effect.  The plain build runs on one thread. */
+int oracle_set_threads(int32_t n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* ---------------------------------------------------------------- storage */
 
@@ -165,18 +180,28 @@ int oracle_forward(int32_t T, const int64_t* rows, const int32_t* dims, const in
     if (T <= 0 || B < 0 || N < 0) return OR_BAD_ARG;
     int rc = check_offsets(offsets, index_is64, (int64_t)T * B, N);
     if (rc) return rc;
-    int64_t total_d = 0, maxd = 0;
+    int64_t total_d = 0, maxd = 1;
+    int64_t* doffs = (int64_t*)malloc(sizeof(int64_t) * (size_t)T);
+    if (!doffs) return OR_NO_MEMORY;
     for (int t = 0; t < T; ++t) {
+        doffs[t] = total_d;
         total_d += dims[t];
         if (dims[t] > maxd) maxd = dims[t];
     }
-    double* acc = (double*)malloc(sizeof(double) * (size_t)(maxd > 0 ? maxd : 1));
-    if (!acc) return OR_NO_MEMORY;
-    int64_t skipped = 0, doff = 0;
-    for (int t = 0; t < T; ++t) {
-        const int D = dims[t];
-        for (int b = 0; b < B; ++b) {
-            const int64_t bag = (int64_t)t * B + b;
+    int64_t skipped = 0;
+    int nomem = 0;
+    /* bags are independent: the timing build runs them on all host cores
+     * (OpenMP); every bag's sum is the same sequence of additions either way */
+#pragma omp parallel reduction(+ : skipped, nomem)
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)maxd);
+        if (!acc) nomem = 1;
+#pragma omp for schedule(static)
+        for (int64_t bag = 0; bag < (int64_t)T * B; ++bag) {
+            if (!acc) continue;
+            const int t = (int)(bag / B);
+            const int64_t b = bag - (int64_t)t * B;
+            const int D = dims[t];
             const int64_t start = load_index(offsets, index_is64, bag);
             const int64_t end = load_index(offsets, index_is64, bag + 1);
             for (int j = 0; j < D; ++j) acc[j] = 0.0;
@@ -193,12 +218,13 @@ int oracle_forward(int32_t T, const int64_t* rows, const int32_t* dims, const in
             for (int j = 0; j < D; ++j) {
                 double v = acc[j];
                 if (mean_pooling && L > 0) v = v / (double)L;
-                out[(int64_t)b * total_d + doff + j] = (float)v;
+                out[b * total_d + doffs[t] + j] = (float)v;
             }
         }
-        doff += D;
+        free(acc);
     }
-    free(acc);
+    free(doffs);
+    if (nomem) return OR_NO_MEMORY;
     if (n_skipped) *n_skipped = skipped;
     return OR_OK;
 }
@@ -348,9 +374,9 @@ int oracle_backward(int32_t T, const int64_t* rows, const int32_t* dims, const i
     int maxd = 1;
     for (int t = 0; t < T; ++t)
         if (dims[t] > maxd) maxd = dims[t];
-    double* g = (double*)malloc(sizeof(double) * (size_t)maxd);
+    int64_t* rstart = (int64_t*)malloc(sizeof(int64_t) * (size_t)(N + 1));
     int rc = OR_OK;
-    if (!keys || !bag_of || !skeys || !spos || !rowbase || !doff || !g) {
+    if (!keys || !bag_of || !skeys || !spos || !rowbase || !doff || !rstart) {
         rc = OR_NO_MEMORY;
         goto done;
     }
@@ -371,14 +397,25 @@ int oracle_backward(int32_t T, const int64_t* rows, const int32_t* dims, const i
         goto done;
     }
 
-    int64_t nr = 0;
-    int64_t i = 0;
-    while (i < N) {
-        /* run-length: the run of equal keys starting at sorted slot i */
-        int64_t e = i;
-        while (e < N && skeys[e] == skeys[i]) ++e;
-        const int64_t key = skeys[i];
-        if (key < total_rows) {
+    /* run-length: the runs of equal keys (first sorted slot of each) */
+    int64_t nruns = 0;
+    for (int64_t i = 0; i < N; ++i)
+        if (i == 0 || skeys[i] != skeys[i - 1]) rstart[nruns++] = i;
+    rstart[nruns] = N;
+    /* the key of skipped lookups (sum of rows) is the largest, so every run
+     * before it is a valid row; runs update distinct rows and state entries,
+     * so the timing build runs them on all host cores (OpenMP) */
+    const int64_t nr = (nruns > 0 && skeys[rstart[nruns - 1]] >= total_rows) ? nruns - 1 : nruns;
+    int nomem = 0;
+#pragma omp parallel reduction(+ : nomem)
+    {
+        double* g = (double*)malloc(sizeof(double) * (size_t)maxd);
+        if (!g) nomem = 1;
+#pragma omp for schedule(dynamic, 64)
+        for (int64_t u = 0; u < nr; ++u) {
+            if (!g) continue;
+            const int64_t i = rstart[u], e = rstart[u + 1];
+            const int64_t key = skeys[i];
             int t = 0;
             while (rowbase[t + 1] <= key) ++t;
             const int64_t r = key - rowbase[t];
@@ -398,10 +435,9 @@ int oracle_backward(int32_t T, const int64_t* rows, const int32_t* dims, const i
                 for (int j = 0; j < D; ++j) g[j] += s * (double)grow[j];
             }
             if (row_grads) {
-                for (int j = 0; j < maxd; ++j) row_grads[nr * maxd + j] = j < D ? g[j] : 0.0;
-                row_keys[nr] = key;
+                for (int j = 0; j < maxd; ++j) row_grads[u * maxd + j] = j < D ? g[j] : 0.0;
+                row_keys[u] = key;
             }
-            ++nr;
             /* one optimizer step for this row */
             if (optimizer == OPT_SGD) {
                 for (int j = 0; j < D; ++j) {
@@ -420,7 +456,11 @@ int oracle_backward(int32_t T, const int64_t* rows, const int32_t* dims, const i
                 }
             }
         }
-        i = e;
+        free(g);
+    }
+    if (nomem) {
+        rc = OR_NO_MEMORY;
+        goto done;
     }
     if (n_rows) *n_rows = nr;
 
@@ -431,6 +471,6 @@ done:
     free(spos);
     free(rowbase);
     free(doff);
-    free(g);
+    free(rstart);
     return rc;
 }

@@ -6,6 +6,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/tbe.h"
 #include "tbe_internal.cuh"
 
@@ -56,6 +58,15 @@ struct tbe_handle {
 };
 
 namespace {
+
+// A named NVTX range around one ABI call, so a profiler's timeline shows
+// which call queued which kernels (a no-op unless a tool is attached).
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -282,6 +293,7 @@ extern "C" {
 
 int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uint32_t flags,
                tbe_handle** out) {
+    CallRange range("tbe_create");
     if (!out) return TBE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
@@ -494,6 +506,7 @@ void tbe_destroy(tbe_handle* h) {
 int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                 int64_t num_indices, int32_t batch_size, const float* per_sample_weights, float* out,
                 void* stream) {
+    CallRange range("tbe_forward");
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (batch_size == 0) return TBE_OK;
@@ -536,6 +549,7 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
 int tbe_per_sample_weight_grad(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                                int64_t num_indices, int32_t batch_size, const float* grad_out,
                                float* grad_weights, void* stream) {
+    CallRange range("tbe_per_sample_weight_grad");
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (batch_size == 0 || num_indices == 0) return TBE_OK;
@@ -582,6 +596,7 @@ int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int3
 int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                          int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
                          void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange range("tbe_backward_prepare");
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (!workspace) return TBE_ERR_INVALID_ARG;
@@ -617,6 +632,7 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
 int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
                         int64_t num_indices, int32_t batch_size, const float* per_sample_weights, float* out,
                         void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange range("tbe_forward_prepare");
     int rc = check_batch(h, indices, offsets, index_dtype, num_indices, batch_size);
     if (rc) return rc;
     if (!workspace || (batch_size > 0 && !out)) return TBE_ERR_INVALID_ARG;
@@ -641,6 +657,7 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
 
 int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, const float* grad_out,
                        const tbe_optimizer* opt, void* workspace, size_t workspace_bytes, void* stream) {
+    CallRange range("tbe_backward_apply");
     if (!h || !opt || !workspace) return TBE_ERR_INVALID_ARG;
     if (!on_handle_device(h)) return TBE_ERR_INVALID_ARG;
     if (num_indices < 0 || batch_size < 0) return TBE_ERR_INVALID_ARG;
@@ -700,6 +717,7 @@ int tbe_backward_sgd(tbe_handle* h, const void* indices, const void* offsets, in
                      int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
                      const float* grad_out, float lr, void* workspace, size_t workspace_bytes,
                      void* stream) {
+    CallRange range("tbe_backward_sgd");
     int rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size,
                                   per_sample_weights, workspace, workspace_bytes, stream);
     if (rc) return rc;
@@ -712,6 +730,7 @@ int tbe_backward_rowwise_adagrad(tbe_handle* h, const void* indices, const void*
                                  const float* per_sample_weights, const float* grad_out, float* state,
                                  float lr, float eps, void* workspace, size_t workspace_bytes,
                                  void* stream) {
+    CallRange range("tbe_backward_rowwise_adagrad");
     if (!state) return TBE_ERR_INVALID_ARG;
     int rc = tbe_backward_prepare(h, indices, offsets, index_dtype, num_indices, batch_size,
                                   per_sample_weights, workspace, workspace_bytes, stream);

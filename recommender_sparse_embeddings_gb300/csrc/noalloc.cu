@@ -14,6 +14,8 @@
 // loads this library keeps the array until the process exits.  All calls on a
 // device share one array, so two calls whose GPU work overlaps (other
 // streams, other host threads) race on it; callers must order them.
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "../../include/tbe.h"
@@ -50,12 +52,28 @@ int scratch_address(void** out) {
     return TBE_OK;
 }
 
+int backward_sgd_static(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                        int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                        const float* grad_out, float lr, void* stream);
+
 }  // namespace
 
 extern "C" int tbe_backward_sgd_noalloc(tbe_handle* h, const void* indices, const void* offsets,
                                         int32_t index_dtype, int64_t num_indices, int32_t batch_size,
                                         const float* per_sample_weights, const float* grad_out,
                                         float lr, void* stream) {
+    nvtxRangePushA("tbe_backward_sgd_noalloc");
+    const int rc = backward_sgd_static(h, indices, offsets, index_dtype, num_indices, batch_size,
+                                       per_sample_weights, grad_out, lr, stream);
+    nvtxRangePop();
+    return rc;
+}
+
+namespace {
+
+int backward_sgd_static(tbe_handle* h, const void* indices, const void* offsets, int32_t index_dtype,
+                        int64_t num_indices, int32_t batch_size, const float* per_sample_weights,
+                        const float* grad_out, float lr, void* stream) {
     if (!h || num_indices < 0 || batch_size < 0) return TBE_ERR_INVALID_ARG;
     // Reject a batch whose workspace does not fit before launching anything.
     const size_t need = tbe_backward_workspace_bytes(h, num_indices, batch_size);
@@ -73,3 +91,5 @@ extern "C" int tbe_backward_sgd_noalloc(tbe_handle* h, const void* indices, cons
     return tbe_backward_sgd(h, indices, offsets, index_dtype, num_indices, batch_size,
                             per_sample_weights, grad_out, lr, scratch, kStaticScratchBytes, stream);
 }
+
+}  // namespace

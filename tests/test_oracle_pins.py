@@ -487,3 +487,35 @@ def test_weight_grad_hand_case():
     np.testing.assert_array_equal(got, np.array([-0.5, 4.5, -0.5], np.float32))
     got = oracle.weight_grad([W], ["f32"], ind, off, 2, G, pooling="mean")
     np.testing.assert_allclose(got, np.array([-0.5, 4.5, -0.5], np.float32) / 3, rtol=1e-7)
+
+
+# ------------------------------------------- timing build (CPU baseline)
+
+@pytest.mark.parametrize("optimizer", ["sgd", "adagrad"])
+def test_timing_build_gives_the_plain_builds_results(optimizer):
+    """bench.py times the oracle's OpenMP build on all host cores; each bag's
+    and each run's sums are the same additions in the same order, so its
+    outputs, updated rows and state are bit-identical to the pinned build."""
+    tabs, dts, ind, off, w, _ = random_problem(51, dtypes=("f32", "f16", "bf16"), weights=True, max_len=40,
+                                               oob=True)
+    B = 7
+    G = np.random.default_rng(3).standard_normal((B, 24)).astype(np.float32)
+    results = []
+    try:
+        for build in ("plain", "timing"):
+            if build == "timing":
+                assert oracle.use_timing_build(4) >= 1
+            out, skipped = oracle.forward(np_tables(tabs), dts, ind, off, B, weights=w, pooling="mean")
+            after = np_tables(tabs)
+            state = np.zeros(sum(t.shape[0] for t in tabs), np.float32)
+            oracle.backward(after, dts, ind, off, B, G, optimizer, 0.05, eps=1e-8, weights=w, pooling="mean",
+                            state=state)
+            results.append((out, skipped, after, state))
+    finally:
+        oracle.use_plain_build()
+    (o0, s0, a0, st0), (o1, s1, a1, st1) = results
+    assert s0 == s1 and s0 > 0
+    np.testing.assert_array_equal(o0.view(np.uint32), o1.view(np.uint32))
+    for x, y in zip(a0, a1):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+    np.testing.assert_array_equal(st0.view(np.uint32), st1.view(np.uint32))

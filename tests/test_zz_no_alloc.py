@@ -7,12 +7,14 @@ forbid device allocation once set-up is over.  They cannot supply the
 workspace tbe_backward_sgd asks for.  The no-alloc entry point runs the same
 kernels on a 32 MiB static device array inside the library instead.
 
-The test calls it through the C ABI and checks its updated tables against
+The tests call it through the C ABI and check its updated tables against
 those of tbe_backward_sgd (with a workspace of its own) on identical copies of
-the inputs, for two calls in a row, so the second call also shows that the
-static array's leftover contents from the first call do no harm.  It lives in
-a file of its own that pytest collects last, and it works in a fresh process
-as well as after the other tests.
+the inputs, for two calls in a row; a second test first runs it on a
+different batch (more lookups, weights, another handle with histogram
+tables), so the static array holds that call's leftovers, then checks the
+next call bit for bit against tbe_backward_sgd and against the CPU oracle.
+They live in a file of their own that pytest collects last, and they work in
+a fresh process as well as after the other tests.
 """
 
 import ctypes
@@ -22,7 +24,8 @@ import torch
 
 import recommender_sparse_embeddings_gb300 as tbe
 import workloads
-from helpers import FP32_TOL, LOWP_TOL, DT_NAME, assert_close, decoded
+from helpers import (FP32_TOL, LOWP_TOL, DT_NAME, assert_close, assert_tables_match, decoded, oracle_backward,
+                     table_bits, touched_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -85,3 +88,56 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     torch.cuda.synchronize()
     assert not table.any()  # nothing ran
     h.close()
+
+
+def test_noalloc_leftovers_of_another_batch_do_no_harm():
+    lib = tbe.load_library()
+    # 1. fill the static array with another call's state: a handle with a
+    #    histogram table (dense backward), a weighted batch of more lookups
+    g = torch.Generator().manual_seed(71)
+    other = [(torch.randn((512, 64), generator=g) * 0.01).half().to(DEV),
+             (torch.randn((40000, 32), generator=g) * 0.01).to(DEV),
+             (torch.randn((3000, 128), generator=g) * 0.01).bfloat16().to(DEV)]
+    B1 = 700
+    lens = torch.randint(0, 90, (3 * B1,), generator=g)
+    off1 = torch.cat([torch.zeros(1, dtype=torch.int64), lens.cumsum(0)])
+    N1 = int(off1[-1])
+    rows = torch.tensor([512, 40000, 3000]).repeat_interleave(lens.view(3, B1).sum(1))
+    ind1 = (torch.rand(N1, generator=g) * rows).to(torch.int64)
+    w1 = torch.rand(N1, generator=g)
+    grad1 = torch.randn((B1, 224), generator=g)
+    h1 = tbe.tbe_create(other, "mean")
+    assert tbe.tbe_backward_workspace_bytes(h1, N1, B1) <= STATIC_SCRATCH_BYTES
+    rc = _noalloc_call(lib, h1, ind1.to(DEV), off1.to(DEV), B1, grad1.to(DEV), 0.05, w1.to(DEV))
+    assert rc == tbe.TBE_OK, tbe.tbe_strerror(rc)
+    assert tbe.tbe_get_error(h1) == tbe.TBE_OK
+    h1.close()
+
+    # 2. the checked call: fewer lookups, no weights, sum pooling, a handle
+    #    with another table layout (sorted backward only, deterministic)
+    cfg = workloads.get_config(2).scaled(B=256, rows_div=1000, rows_min=64)
+    specs = workloads.realize_tables(cfg)
+    base = workloads.make_tables(cfg, "cpu", specs)
+    batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
+    grad = workloads.make_grad(cfg, "cpu", specs)
+    assert batch.N < N1 and batch.weights is None
+    tabs_a = [t.to(DEV) for t in base]
+    tabs_b = [t.to(DEV) for t in base]
+    h_a = tbe.tbe_create(tabs_a, cfg.pooling)
+    h_b = tbe.tbe_create(tabs_b, cfg.pooling)
+    ws = tbe.make_workspace(h_a, batch.N, cfg.B)
+    ind, off, gd = batch.indices.to(DEV), batch.offsets.to(DEV), grad.to(DEV)
+    tbe.tbe_backward_sgd(h_a, ind, off, cfg.B, gd, cfg.lr, ws)
+    rc = _noalloc_call(lib, h_b, ind, off, cfg.B, gd, cfg.lr)
+    assert rc == tbe.TBE_OK, tbe.tbe_strerror(rc)
+    assert tbe.tbe_get_error(h_a) == tbe.TBE_OK
+    assert tbe.tbe_get_error(h_b) == tbe.TBE_OK
+    for t, (a, b) in enumerate(zip(tabs_a, tabs_b)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"table {t} differs from tbe_backward_sgd"
+    # and directly against the oracle
+    ref, _ = oracle_backward(base, batch.indices, batch.offsets, cfg.B, grad, "sgd", cfg.lr)
+    before = [table_bits(t) for t in base]
+    assert_tables_match(tabs_b, ref, before, touched_rows(base, batch.indices, batch.offsets, cfg.B),
+                        what="noalloc vs oracle")
+    h_a.close()
+    h_b.close()
