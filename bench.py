@@ -344,7 +344,8 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
     grad = workloads.make_grad(cfg, dev, specs)
     T, B, N = len(specs), cfg.B, batch.N
     flags = (tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0) | (
-        tbe.TBE_FLAG_SORTED_BACKWARD if args.sorted_backward else 0)
+        tbe.TBE_FLAG_SORTED_BACKWARD if args.sorted_backward else 0) | (
+        tbe.TBE_FLAG_FORCE_HISTOGRAM if args.histogram else 0)
     h = tbe.tbe_create(tables, cfg.pooling, flags)
     ws = tbe.make_workspace(h, N, B, dev)
     out = torch.empty((B, h.total_dim), dtype=torch.float32, device=dev)
@@ -446,14 +447,15 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
             raise RuntimeError(f"device error in the weight gradient: {tbe.tbe_strerror(rc)}")
 
     # U (distinct keys) for the byte count: read once after the run; the
-    # histogram tables' lookups are not sorted, so their distinct rows are
-    # counted here
+    # dense-backward tables' lookups are not sorted, so their distinct rows
+    # are counted here
     lay = tbe.tbe_backward_workspace_layout(h, N, B)
     U = int(ws[lay.num_unique:lay.num_unique + 4].view(torch.int32).item())
     offs = off.to(torch.int64).cpu()
     paths = tbe.tbe_table_paths(h)
-    for t, p in enumerate(paths):
-        if p == "histogram" and not args.sorted_backward:
+    bpaths = tbe.tbe_backward_paths(h)
+    for t, p in enumerate(bpaths):
+        if p == "dense":
             lo, hi = int(offs[t * B]), int(offs[(t + 1) * B])
             U += int(torch.unique(ind[lo:hi]).numel())
     # compulsory bytes (each distinct row, the gradient and the batch once):
@@ -497,10 +499,10 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
     # downsweep, run-length count/scan/write, chunk count/scan/write); apply
     # (one per backward class of the sorted-path tables, dense sums + update)
     hist_dtypes = {s.dtype for s, p in zip(specs, paths) if p == "histogram"}
-    dense = bool(hist_dtypes) and not args.sorted_backward  # histogram tables' dense backward
+    dense = "dense" in bpaths  # small tables' dense backward
     fwd_launches = (1 if any(p != "histogram" for p in paths) else 0) + 1 + len(hist_dtypes)
     prep_launches = 2 + (1 if dense else 0) + 2 * passes + (passes if dense else passes - 1) + 6
-    sorted_specs = [s for s, p in zip(specs, paths) if not (dense and p == "histogram")]
+    sorted_specs = [s for s, p in zip(specs, bpaths) if p == "sorted"]
     apply_launches = backward_classes(sorted_specs) + (2 if dense else 0)
     launches_per_step = fwd_launches + prep_launches + apply_launches
 
@@ -512,6 +514,7 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
         "timed_region_s": t_end - t_start,
         "dtype": "f32" if all(sp.dtype == "f32" for sp in specs) else "mixed(f32 accumulate)",
         "paths": sorted(set(paths)),
+        "backward_paths": sorted(set(bpaths)),
         "config": {"workload": cfg.description + (f" (first {T} of the tables)" if args.tables else ""),
                    "config_id": cfg.cfg_id, "T": T, "B": B, "N_lookups": N, "unique_rows": U,
                    "index_dtype": args.index_dtype, "optimizer": cfg.optimizer,
@@ -666,7 +669,7 @@ def run_ours(args):
             "data": "synthetic: seeded generators with the workload's laws (stand-in for the "
                     "pages' production shard configurations)",
         }
-        for k in ("paths", "config", "fwd", "wgrad", "step_gbs", "segments_ms", "breakdown_ms_sequential",
+        for k in ("paths", "backward_paths", "config", "fwd", "wgrad", "step_gbs", "segments_ms", "breakdown_ms_sequential",
                   "algorithmic_bytes", "roofline", "ms_per_step_mean", "timed_region_s"):
             line[k] = head[k]
         line["cpu_baseline"] = cpu
@@ -741,9 +744,11 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-histogram", action="store_true",
-                   help="keep small tables on the gather path (no tensor-core histogram path)")
+                   help="no tensor-core path for small tables (gather forward, sorted backward)")
+    p.add_argument("--histogram", action="store_true",
+                   help="small tables' forward on the tensor-core histogram path")
     p.add_argument("--sorted-backward", action="store_true",
-                   help="histogram tables take the sorted backward instead of the dense (tensor-core) one")
+                   help="small tables take the sorted backward instead of the dense (tensor-core) one")
     p.add_argument("--tables", type=int, default=0,
                    help="use only the first K tables of the workload (profiling cases)")
     args = p.parse_args(argv)

@@ -83,15 +83,24 @@ typedef enum { TBE_I32 = 0, TBE_I64 = 1 } tbe_index_dtype;
 typedef enum { TBE_POOL_SUM = 0, TBE_POOL_MEAN = 1 } tbe_pooling;
 typedef enum { TBE_OPT_SGD = 1, TBE_OPT_ROWWISE_ADAGRAD = 2 } tbe_optimizer_kind;
 
-/* tbe_create flags */
-#define TBE_FLAG_NO_HISTOGRAM 0x1u    /* never use the small-table tensor-core path */
-#define TBE_FLAG_FORCE_HISTOGRAM 0x2u /* use it for every eligible table */
-#define TBE_FLAG_SORTED_BACKWARD 0x4u /* histogram tables too take the sorted backward */
-/* Backward of a histogram table (default): its lookups are not sorted; the
- * table's whole gradient H^T . G is one tensor-core product (bf16 operands
- * split three ways for fp32 accuracy, fp32 accumulation; reproducible), then
- * every touched row gets one optimizer step.  TBE_FLAG_SORTED_BACKWARD sends
- * these tables through the sort and segment reduction like the others. */
+/* tbe_create flags.  A "small table" has 16-bit rows (fp16 or bf16), a dim
+ * that is a multiple of 16 in [16, 256], 16-byte aligned data and at most 512
+ * rows (1024 with TBE_FLAG_FORCE_HISTOGRAM).
+ *  - Backward of a small table (default): its lookups are not sorted; the
+ *    table's whole gradient H^T . G is one tensor-core product (bf16 operands
+ *    split three ways for fp32 accuracy, fp32 accumulation), then every
+ *    touched row gets one optimizer step.  TBE_FLAG_SORTED_BACKWARD sends
+ *    these tables through the sort and segment reduction like the others.
+ *  - Forward of a small table: the gather, like every other table, unless
+ *    TBE_FLAG_FORCE_HISTOGRAM, which pools it on the tensor cores as a
+ *    per-bag histogram times the table (kimbodo "What Happened"), for the
+ *    small tables of each dtype that fit one CTA's shared memory together.
+ *    The default follows measurement: on 64 fp16 tables of 512 x 64 rows
+ *    with 1..64 lookups per bag the gather was the faster of the two.
+ *  - TBE_FLAG_NO_HISTOGRAM: neither tensor-core path. */
+#define TBE_FLAG_NO_HISTOGRAM 0x1u    /* no tensor-core path (forward or backward) */
+#define TBE_FLAG_FORCE_HISTOGRAM 0x2u /* histogram tensor-core forward for small tables */
+#define TBE_FLAG_SORTED_BACKWARD 0x4u /* small tables too take the sorted backward */
 
 /* One embedding table.  data: device, row-major rows x dim of dtype,
  * caller-owned, read by forward and updated in place by backward.  The
@@ -322,6 +331,11 @@ int tbe_last_cuda_error(void);
  * 2 histogram tensor-core path (kimbodo "What Happened": eligible small
  * tables take the histogram path). */
 int tbe_table_paths(const tbe_handle* h, int32_t* out_path);
+
+/* Per-table backward schedule chosen at create time, for tests and tuning:
+ * out_path[t] = 0 sorted (transpose, sort, segment reduction), 1 dense
+ * tensor-core product H^T . G (small tables; see the flags above). */
+int tbe_table_backward_paths(const tbe_handle* h, int32_t* out_path);
 
 #ifdef __cplusplus
 }

@@ -103,6 +103,7 @@ def load_library():
         "tbe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "tbe_last_cuda_error": ([], ctypes.c_int),
         "tbe_table_paths": ([P, ctypes.POINTER(i32)], ctypes.c_int),
+        "tbe_table_backward_paths": ([P, ctypes.POINTER(i32)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -210,6 +211,13 @@ def tbe_table_paths(h: Handle) -> List[str]:
     buf = (ctypes.c_int32 * len(h.tables))()
     _check(load_library().tbe_table_paths(h.ptr, buf), "tbe_table_paths")
     return [PATH_NAMES[int(x)] for x in buf]
+
+
+def tbe_backward_paths(h: Handle) -> List[str]:
+    """Per table, "dense" (tensor-core H^T . G) or "sorted"."""
+    buf = (ctypes.c_int32 * len(h.tables))()
+    _check(load_library().tbe_table_backward_paths(h.ptr, buf), "tbe_table_backward_paths")
+    return ["dense" if int(x) else "sorted" for x in buf]
 
 
 def tbe_forward(h: Handle, indices: torch.Tensor, offsets: torch.Tensor, batch_size: int,

@@ -208,11 +208,11 @@ struct HistGroup {
     const int32_t* tables;  // device: the group's tables
     int n;
     int dmax;         // largest dim
-    size_t ab_bytes;  // largest (128 + dim) x rows padded to 64 x 2: one table's A and W^T operands
+    int kmax;         // largest row count padded to 64
+    size_t wt_bytes;  // largest dim x padded rows x 2 (one table's W^T)
     size_t smem;      // dynamic shared memory of the launch
 };
-size_t hist_ab_bytes(int64_t rows, int dim);
-size_t hist_smem_bytes(size_t ab_bytes);
+size_t hist_smem_bytes(int kmax, size_t wt_bytes);
 cudaError_t hist_configure(int optin_smem);
 cudaError_t launch_hist(const FwdArgs& a, const HistGroup& f16, const HistGroup& bf16, cudaStream_t s);
 

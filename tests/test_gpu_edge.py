@@ -228,8 +228,9 @@ def test_malformed_offsets_on_a_histogram_table_are_reported():
     and the dense backward report BAD_OFFSETS (every read stays inside the
     batch: offsets are clamped to [0, N])."""
     tables = make_tables([(64, 16, torch.float16)])
-    h = tbe.tbe_create(tables, "sum")
+    h = tbe.tbe_create(tables, "sum", tbe.TBE_FLAG_FORCE_HISTOGRAM)
     assert tbe.tbe_table_paths(h) == ["histogram"]
+    assert tbe.tbe_backward_paths(h) == ["dense"]
     ind = torch.tensor([1, 2, 3, 4, 5, 6], dtype=torch.int64, device=DEV)
     off = torch.tensor([0, 4, 2, 6], dtype=torch.int64, device=DEV)
     tbe.tbe_forward(h, ind, off, 3)

@@ -49,11 +49,15 @@ def integer_problem(seed, B, long_bag=False):
 
 
 @pytest.mark.parametrize("long_bag", [False, True])
-def test_forward_bit_exact(long_bag):
+@pytest.mark.parametrize("flags", [0, tbe.TBE_FLAG_FORCE_HISTOGRAM])
+def test_forward_bit_exact(long_bag, flags):
+    """Default flags: every table on the gather; with the histogram flag the
+    two small tables on the tensor cores."""
     B = 300
     tables, ind, off, w, _ = integer_problem(1, B, long_bag)
-    h = tbe.tbe_create(tables, "sum")
-    assert tbe.tbe_table_paths(h) == ["gather", "gather", "gather_elementwise", "histogram", "histogram"]
+    h = tbe.tbe_create(tables, "sum", flags)
+    small = "histogram" if flags else "gather"
+    assert tbe.tbe_table_paths(h) == ["gather", "gather", "gather_elementwise", small, small]
     out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, w.to(DEV))
     assert tbe.tbe_get_error(h) == tbe.TBE_OK
     ref, skipped = oracle.forward([table_bits(t) for t in tables], [DT_NAME[t.dtype] for t in tables],
@@ -65,7 +69,7 @@ def test_forward_bit_exact(long_bag):
 
 @pytest.mark.parametrize("flags", [0, tbe.TBE_FLAG_SORTED_BACKWARD])
 def test_sgd_backward_bit_exact(flags):
-    """Default flags: the histogram tables take the dense backward; with
+    """Default flags: the small tables take the dense backward; with
     TBE_FLAG_SORTED_BACKWARD every table takes the sort."""
     B = 300
     tables, ind, off, w, grad = integer_problem(2, B)

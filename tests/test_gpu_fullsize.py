@@ -1,5 +1,5 @@
 """GPU parity at the workloads' full sizes, in the configuration bench.py
-times (default handle flags, int64 indices: histogram tables take the dense
+times (default handle flags, int64 indices: small tables take the dense
 backward and stay out of the sort).
 
 Full tables (4 to 20 GB) are too large for the oracle, so the checks are:
@@ -61,7 +61,7 @@ def test_full_size(cid):
     # ---- sort / run-length: whole arrays, bit-exact (histogram tables take
     # the dense backward: only the other tables' keys are sorted)
     keys, bag_of = oracle.make_keys(rows, ind, off, B)
-    dense = np.array([p == "histogram" for p in paths])
+    dense = np.array([p == "dense" for p in tbe.tbe_backward_paths(h)])
     keep = np.flatnonzero(~dense[bag_of // B])
     Ns = len(keep)
     perm = np.argsort(keys[keep], kind="stable")

@@ -50,7 +50,7 @@ def check_hist(out, tables, ind, off, B, w=None, pooling="sum", what="", cols=No
     return ref
 
 
-def run_hist(tables, ind, off, B, w=None, pooling="sum", flags=0, expect=tbe.TBE_OK):
+def run_hist(tables, ind, off, B, w=None, pooling="sum", flags=tbe.TBE_FLAG_FORCE_HISTOGRAM, expect=tbe.TBE_OK):
     h = tbe.tbe_create(tables, pooling, flags)
     paths = tbe.tbe_table_paths(h)
     out = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, None if w is None else w.to(DEV))
@@ -64,14 +64,29 @@ def test_path_selection():
     mk = lambda r, d, dt: (torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV)
     tabs = [mk(512, 64, torch.float16), mk(512, 64, torch.bfloat16), mk(512, 64, torch.float32),
             mk(600, 32, torch.float16), mk(100, 24, torch.float16), mk(300, 128, torch.bfloat16)]
+    # default: every forward on the gather; the small tables' backward dense
     h = tbe.tbe_create(tabs, "sum")
-    assert tbe.tbe_table_paths(h) == ["histogram", "histogram", "gather", "gather", "gather", "histogram"]
+    assert tbe.tbe_table_paths(h) == ["gather"] * 6
+    assert tbe.tbe_backward_paths(h) == ["dense", "dense", "sorted", "sorted", "sorted", "dense"]
     h.close()
+    h = tbe.tbe_create(tabs, "sum", tbe.TBE_FLAG_SORTED_BACKWARD)
+    assert tbe.tbe_backward_paths(h) == ["sorted"] * 6
+    h.close()
+    # the histogram forward on request; tables of up to 1024 rows are then
+    # small.  The tables of one dtype share one launch, so together they must
+    # fit one CTA's shared memory (A for the most rows, the largest W^T): the
+    # 600-row fp16 table does not fit beside the 512 x 64 one (gather
+    # forward, dense backward), alone it does
     h = tbe.tbe_create(tabs, "sum", tbe.TBE_FLAG_FORCE_HISTOGRAM)
-    assert tbe.tbe_table_paths(h)[3] == "histogram"
+    assert tbe.tbe_table_paths(h) == ["histogram", "histogram", "gather", "gather", "gather", "histogram"]
+    assert tbe.tbe_backward_paths(h) == ["dense", "dense", "sorted", "dense", "sorted", "dense"]
+    h.close()
+    h = tbe.tbe_create([tabs[3], tabs[2]], "sum", tbe.TBE_FLAG_FORCE_HISTOGRAM)
+    assert tbe.tbe_table_paths(h) == ["histogram", "gather"]
     h.close()
     h = tbe.tbe_create(tabs, "sum", tbe.TBE_FLAG_NO_HISTOGRAM)
     assert "histogram" not in tbe.tbe_table_paths(h)
+    assert tbe.tbe_backward_paths(h) == ["sorted"] * 6
     h.close()
 
 
@@ -279,7 +294,7 @@ def test_histogram_is_deterministic():
     ind, off = batch_for(512, B, 64, seed=34)
     ind = torch.tensor(np.random.default_rng(35).integers(0, 8, ind.numel()), dtype=torch.int64)  # many repeats
     w = torch.rand(ind.numel(), generator=g)
-    h = tbe.tbe_create(tables, "sum")
+    h = tbe.tbe_create(tables, "sum", tbe.TBE_FLAG_FORCE_HISTOGRAM)
     a = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, w.to(DEV)).cpu()
     b = tbe.tbe_forward(h, ind.to(DEV), off.to(DEV), B, w.to(DEV)).cpu()
     assert tbe.tbe_get_error(h) == tbe.TBE_OK
@@ -311,7 +326,7 @@ def test_histogram_workload_small_tables():
     specs = workloads.realize_tables(cfg)
     tables = [t.to(DEV) for t in workloads.make_tables(cfg, "cpu", specs)]
     batch = workloads.make_batch(cfg, "cpu", torch.int64, specs)
-    h = tbe.tbe_create(tables, cfg.pooling)
+    h = tbe.tbe_create(tables, cfg.pooling, tbe.TBE_FLAG_FORCE_HISTOGRAM)
     paths = tbe.tbe_table_paths(h)
     assert paths[:64] == ["histogram"] * 64 and paths[64] == "gather"
     out = tbe.tbe_forward(h, batch.indices.to(DEV), batch.offsets.to(DEV), cfg.B, batch.weights.to(DEV))

@@ -121,11 +121,12 @@ def check_prepare(cfg, tables, batch, flags):
 
     U = int(view(lay.num_unique, 1)[0])
     keys, bag = oracle.make_keys([t.shape[0] for t in tables], batch.indices.numpy(), batch.offsets.numpy(), cfg.B)
-    # the histogram tables' lookups take the dense backward unless
+    # the small tables' lookups take the dense backward unless
     # TBE_FLAG_SORTED_BACKWARD: only the other tables' keys are sorted (their
     # positions in ascending order)
-    dense = np.array([p == "histogram" and not (flags & tbe.TBE_FLAG_SORTED_BACKWARD)
-                      for p in tbe.tbe_table_paths(h)])
+    dense = np.array([p == "dense" for p in tbe.tbe_backward_paths(h)])
+    if flags & tbe.TBE_FLAG_SORTED_BACKWARD:
+        assert not dense.any()
     keep = np.flatnonzero(~dense[bag // cfg.B])
     ref = oracle.sort_rle(keys[keep])
     Ns = len(keep)
