@@ -20,12 +20,13 @@
 //    stream starts so the read overlaps the gradient gather; after the stream
 //    each key gets its optimizer step and its row is stored.  Sums are plain
 //    fp32 (at most 255 terms).
-//  Long runs, "accumulate": a warp sums one 256-lookup chunk with compensated
-//    (Kahan) fp32 addition, five gradient rows (dim 256: two) in flight per
-//    row group, and writes the partial; the warp that completes the last
-//    chunk of a run (atomic count after a fence) adds the partials in a fixed
-//    order with Kahan addition, updates the row, and resets the count so the
-//    prepared workspace can be applied again.
+//  Long runs, "accumulate": a warp sums one 256-lookup chunk, five gradient
+//    rows (dim 256: two) in flight per row group, each step's rows in fp32
+//    (packed two-wide FMAs) and the step sums with compensated (Kahan)
+//    addition, and writes the partial; the warp that completes the last chunk of
+//    a run (atomic count after a fence) adds the partials in a fixed order
+//    with compensated (Kahan) addition, updates the row, and resets the count
+//    so the prepared workspace can be applied again.
 //
 // Lanes own columns: a row is read by a group of LPR lanes (8 for dim 32, 16
 // for dim 64, 32 otherwise), lane l holding columns blk*LPR*4 + (l%LPR)*4 +
@@ -58,6 +59,19 @@ struct Kahan {
     __device__ __forceinline__ float value() const { return s - c; }
 };
 
+
+// acc += s * (x, y) on both halves of a float pair, one packed fp32 FMA
+// (each half rounds exactly like fmaf).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x, float y) {
+    asm("{\n\t.reg .b64 p, q, r;\n\t"
+        "mov.b64 p, {%2, %2};\n\t"
+        "mov.b64 q, {%3, %4};\n\t"
+        "mov.b64 r, {%0, %1};\n\t"
+        "fma.rn.f32x2 r, p, q, r;\n\t"
+        "mov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "f"(x), "f"(y));
+}
 
 // Row shapes of the vector classes.  A row is read by a group of LPR lanes,
 // each lane holding VW = 4 consecutive columns (16-byte gradient loads) of
@@ -166,11 +180,13 @@ __device__ __forceinline__ float optimizer_step(const ApplyArgs& a, int dim, con
 #pragma unroll
         for (int o = LPR / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
         const float m = m_old + __fdiv_rn(sq, (float)dim);
-        const float denom = sqrtf(m) + a.eps;
+        // lr / (sqrt(m) + eps) once per row (rounded once more than a
+        // division per column)
+        const float step = __fdiv_rn(a.lr, sqrtf(m) + a.eps);
 #pragma unroll
         for (int q = 0; q < NB; ++q)
 #pragma unroll
-            for (int v = 0; v < VW; ++v) S::set(row, q, v, S::get(row, q, v) - a.lr * __fdiv_rn(g[q][v], denom));
+            for (int v = 0; v < VW; ++v) S::set(row, q, v, fmaf(-step, g[q][v], S::get(row, q, v)));
         return m;
     }
 #pragma unroll
@@ -335,9 +351,10 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
                 for (int s = 0; s < R; ++s) {
                     const float w = sl[u] == s ? ss[u] : 0.f;
 #pragma unroll
-                    for (int q = 0; q < NB; ++q)
-#pragma unroll
-                        for (int v = 0; v < VW; ++v) acc[s][q][v] = fmaf(w, g[u][q][v], acc[s][q][v]);
+                    for (int q = 0; q < NB; ++q) {
+                        ffma2(acc[s][q][0], acc[s][q][1], w, g[u][q][0], g[u][q][1]);
+                        ffma2(acc[s][q][2], acc[s][q][3], w, g[u][q][2], g[u][q][3]);
+                    }
                 }
         }
         // one optimizer step per key of the piece; group 0 stores the rows
@@ -465,8 +482,11 @@ __device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace&
 // -------------------------------------------------------------- long runs
 
 // Partial sum of one chunk, lookups [s0, s1) of one key: row group g adds
-// lookups g, g + NG, ... with compensated addition, GROUP gradient rows in
-// flight; the groups' sums are added and group 0 writes the partial row.
+// lookups g, g + NG, ..., GROUP gradient rows in flight per step; a step's
+// GROUP products are summed in fp32 and the step sums are added with
+// compensated (Kahan) addition (a long run's lookups often share gradient
+// rows, so its partial sums grow linearly and plain fp32 sums would drift);
+// the groups' sums are added and group 0 writes the partial row.
 template <int DT, int CODE>
 __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                                const TableDesc& td, int t, uint32_t s0, uint32_t s1,
@@ -527,13 +547,25 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
                     }
                 }
             }
+            // the step's GROUP lookups in plain fp32 (a skipped lookup's
+            // row is zero: adding it changes nothing), the step's sum into
+            // the chunk's with compensated addition
+            float blk[NB][VW];
+#pragma unroll
+            for (int q = 0; q < NB; ++q)
+#pragma unroll
+                for (int v = 0; v < VW; ++v) blk[q][v] = 0.f;
 #pragma unroll
             for (int u = 0; u < GROUP; ++u)
-                if (bb[u] >= 0)
 #pragma unroll
-                    for (int q = 0; q < NB; ++q)
+                for (int q = 0; q < NB; ++q) {
+                    ffma2(blk[q][0], blk[q][1], ss[u], g[u][q][0], g[u][q][1]);
+                    ffma2(blk[q][2], blk[q][3], ss[u], g[u][q][2], g[u][q][3]);
+                }
 #pragma unroll
-                        for (int v = 0; v < VW; ++v) acc[q][v].add_scaled(ss[u], g[u][q][v]);
+            for (int q = 0; q < NB; ++q)
+#pragma unroll
+                for (int v = 0; v < VW; ++v) acc[q][v].add(blk[q][v]);
         }
         cb = nb;
         cs = ns;
