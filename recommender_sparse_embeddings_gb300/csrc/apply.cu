@@ -60,19 +60,6 @@ struct Kahan {
 };
 
 
-// acc += s * (x, y) on both halves of a float pair, one packed fp32 FMA
-// (each half rounds exactly like fmaf).
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x, float y) {
-    asm("{\n\t.reg .b64 p, q, r;\n\t"
-        "mov.b64 p, {%2, %2};\n\t"
-        "mov.b64 q, {%3, %4};\n\t"
-        "mov.b64 r, {%0, %1};\n\t"
-        "fma.rn.f32x2 r, p, q, r;\n\t"
-        "mov.b64 {%0, %1}, r;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(s), "f"(x), "f"(y));
-}
-
 // Row shapes of the vector classes.  A row is read by a group of LPR lanes,
 // each lane holding VW = 4 consecutive columns (16-byte gradient loads) of
 // each of NB column blocks of LPR*4 columns; a warp holds NG = 32/LPR groups,

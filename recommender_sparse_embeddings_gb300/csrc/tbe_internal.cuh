@@ -101,6 +101,19 @@ __device__ __forceinline__ void store_elem(void* base, int64_t k, float v) {
     }
 }
 
+// acc += s * (x, y) on both halves of a float pair, one packed fp32 FMA
+// (each half rounds exactly like fmaf).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x, float y) {
+    asm("{\n\t.reg .b64 p, q, r;\n\t"
+        "mov.b64 p, {%2, %2};\n\t"
+        "mov.b64 q, {%3, %4};\n\t"
+        "mov.b64 r, {%0, %1};\n\t"
+        "fma.rn.f32x2 r, p, q, r;\n\t"
+        "mov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "f"(x), "f"(y));
+}
+
 // Unpack one 16-byte vector of DT into E = 16/sizeof(DT) floats.
 template <int DT>
 __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
