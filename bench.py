@@ -47,11 +47,23 @@ DOMINANT_KERNELS = {
     "apply": "apply_class_kernel per backward class (+ dense_mma_kernel, dense_update_kernel)",
 }
 
+# the sources of each call's kernels (a traffic profile is valid while they
+# are unchanged)
+_CSRC = "recommender_sparse_embeddings_gb300/csrc/"
 KERNEL_FILES = {
-    "forward": "recommender_sparse_embeddings_gb300/csrc/forward.cu",
-    "prepare": "recommender_sparse_embeddings_gb300/csrc/prepare.cu",
-    "apply": "recommender_sparse_embeddings_gb300/csrc/apply.cu",
+    "forward": [_CSRC + "forward.cu", _CSRC + "hist.cu", _CSRC + "tbe_internal.cuh"],
+    "prepare": [_CSRC + "prepare.cu", _CSRC + "tbe_internal.cuh"],
+    "apply": [_CSRC + "apply.cu", _CSRC + "dense.cu", _CSRC + "tbe_internal.cuh"],
 }
+
+
+def kernel_sources_sha256(segment: str) -> str:
+    """sha256 over the call's kernel sources, in the listed order."""
+    h = hashlib.sha256()
+    for f in KERNEL_FILES[segment]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 # ------------------------------------------------------------ distributed
@@ -213,21 +225,20 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- profile
 
-def profile_traffic(segment: str, cfg_id: int, T: int):
-    """DRAM bytes per launch of a call's main kernel on this workload, from the
-    committed ncu summary, or None if there is none (for this workload and
-    table count) or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{segment}_w{cfg_id}.md")
+def profile_traffic(segment: str, cfg, T: int):
+    """DRAM bytes of one call (all its kernels) on this workload, from the
+    committed ncu summary profiles/launches_traffic_<workload>.md, or None if
+    there is none (for this workload and table count) or a kernel source
+    changed since."""
+    path = os.path.join(ROOT, "profiles", f"launches_traffic_{cfg.name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    t = re.search(r"tables:\s*([0-9]+)", text)
-    if not m or not h or not t or int(t.group(1)) != T:
+    t = re.search(r"^tables:\s*([0-9]+)", text, re.M)
+    m = re.search(r"^traffic\[" + re.escape(segment) + r"\]:\s*([0-9.eE+]+)\s+sha256=([0-9a-f]+)", text, re.M)
+    if not m or not t or int(t.group(1)) != T:
         return None
-    src = os.path.join(ROOT, KERNEL_FILES[segment])
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
+    if kernel_sources_sha256(segment) != m.group(2):
         return None
     return float(m.group(1))
 
@@ -492,7 +503,7 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
     achieved = nbytes[dominant] / (call_ms[dominant] / 1e3) / 1e9
     timing_src = ("timed region, CUDA events on the caller's stream, median of the steps" if dominant == "apply"
                   else "per-call run, CUDA events on the caller's stream, median of the steps")
-    traffic = profile_traffic(dominant, cfg.cfg_id, T)
+    traffic = profile_traffic(dominant, cfg, T)
     # our kernels per step: forward (gather pool if any gather table, long
     # bags, one histogram launch per dtype with histogram tables); prepare
     # (bag marks, [compaction], keys, per radix pass [upsweep] + scan +
