@@ -640,6 +640,7 @@ int tbe_backward_prepare(tbe_handle* h, const void* indices, const void* offsets
     a.key_bits = h->key_bits;
     a.digit_bits = h->digit_bits;
     a.compact = h->n_dense > 0;
+    a.chunk = long_chunk_lookups(num_indices, h->num_sms);
     return cuda_status(launch_prepare(a, w, s));
 }
 
@@ -693,6 +694,7 @@ int tbe_backward_apply(tbe_handle* h, int64_t num_indices, int32_t batch_size, c
     a.grad_vec = ((uintptr_t)grad_out % 16) == 0;
     a.total_d = h->total_d;
     a.part_stride = part_stride(h);
+    a.chunk = long_chunk_lookups(num_indices, h->num_sms);
     a.total_rows = (uint32_t)h->total_rows;
     a.has_scale = 0;
     a.opt = opt->kind;

@@ -7,10 +7,10 @@
 // One kernel per backward class (table dtype x row shape) present in the
 // handle, so each kernel's registers are sized for one shape only; the class
 // kernels run side by side on the handle's apply streams.  A class kernel
-// walks a work list table by table: the 256-lookup chunks of the table's
-// long runs (numbered in key order by the preparation step), then batches of
-// kBatchRows consecutive distinct keys.  Warps take work items from a
-// per-class atomic counter.
+// walks a work list table by table: the chunks of the table's long runs
+// (numbered in key order by the preparation step; 256 to 1024 lookups, by
+// batch size), then batches of kBatchRows consecutive distinct keys.  Warps
+// take work items from a per-class atomic counter.
 //
 //  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
 //    batch into pieces of at most R keys and walks each piece's sorted lookups
@@ -20,19 +20,24 @@
 //    stream starts so the read overlaps the gradient gather; after the stream
 //    each key gets its optimizer step and its row is stored.  Sums are plain
 //    fp32 (at most 255 terms).
-//  Long runs, "accumulate": a warp sums one 256-lookup chunk, five gradient
-//    rows (dim 256: two) in flight per row group, each step's rows in fp32
-//    (packed two-wide FMAs) and the step sums with compensated (Kahan)
-//    addition, and writes the partial; the warp that completes the last chunk of
-//    a run (atomic count after a fence) adds the partials in a fixed order
-//    with compensated (Kahan) addition, updates the row, and resets the count
-//    so the prepared workspace can be applied again.
-//
-// Lanes own columns: a row is read by a group of LPR lanes (8 for dim 32, 16
-// for dim 64, 32 otherwise), lane l holding columns blk*LPR*4 + (l%LPR)*4 +
-// [0, 4) of each column block, so every gradient load is 16 bytes wide; the
-// 32/LPR groups of a warp take different lookups of the same keys and add
-// their sums at the end.
+//    Lanes own columns: a row is read by a group of LPR lanes (8 for dim 32,
+//    16 for dim 64, 32 otherwise), lane l holding columns blk*LPR*4 +
+//    (l%LPR)*4 + [0, 4) of each column block, so every gradient load is 16
+//    bytes wide; the 32/LPR groups of a warp take different lookups of the
+//    same keys and add their sums at the end.
+//  Long runs, "accumulate": a warp sums one chunk of the run.  Every lane
+//    takes the same lookup and holds VW = dim/32 consecutive columns, so one
+//    load instruction reads a whole gradient row; G rows are loaded per step
+//    (8 for dim <= 128, 2 for dim 256), and the chunk's positions, bags and
+//    scales stream in 32 at a time, the bags and scales one window ahead and
+//    the positions two, so the gather never waits on its own metadata.  Each
+//    step's G products are summed in fp32 (packed two-wide FMAs) and the
+//    step sums added with compensated (Kahan) addition (consecutive lookups
+//    of a long run often share a bag, so longer plain sums would round
+//    coarsely); the partial row goes to the workspace.  The warp that
+//    completes the last chunk of a run (atomic count after a fence) adds the
+//    partials in chunk order with compensated addition, updates the row,
+//    and resets the count so the prepared workspace can be applied again.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -466,159 +471,358 @@ __device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace&
     }
 }
 
-// -------------------------------------------------------------- long runs
+// ------------------------------------------------- long runs: row shapes
 
-// Partial sum of one chunk, lookups [s0, s1) of one key: row group g adds
-// lookups g, g + NG, ..., GROUP gradient rows in flight per step; a step's
-// GROUP products are summed in fp32 and the step sums are added with
-// compensated (Kahan) addition (a long run's lookups often share gradient
-// rows, so its partial sums grow linearly and plain fp32 sums would drift);
-// the groups' sums are added and group 0 writes the partial row.
-template <int DT, int CODE>
-__device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
-                                               const TableDesc& td, int t, uint32_t s0, uint32_t s1,
-                                               float* part_row, int lane) {
-    using Sh = ShapeOf<CODE>;
-    constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
-    using S = Slice<DT, VW, NB, LPR>;
-    constexpr int GROUP = NB == 1 ? 5 : 2;  // gradient rows in flight per row group
-    constexpr int STEP = NG * GROUP;
-    const int grp = lane / LPR;
-    const int64_t tB = (int64_t)t * a.B;
-    Kahan acc[NB][VW];
+// A row is held by the whole warp, lane l holding columns [l*VW, l*VW + VW).
+// G gradient rows are loaded per step (up to 4 KB a warp); PF partial rows
+// are in flight when a long run's partials are added.
+template <int CODE>
+struct VecShape {
+    static constexpr int D = CODE == SHAPE_D32 ? 32 : (CODE == SHAPE_D64 ? 64 : (CODE == SHAPE_D128 ? 128 : 256));
+    static constexpr int VW = D / 32;
+    static constexpr int G = VW == 8 ? 2 : (32 / VW > 8 ? 8 : 32 / VW);  // long runs
+    static constexpr int PF = 32 / VW;
+};
+
+// VW gradient floats at p (4*VW bytes, aligned to min(16, 4*VW)).
+template <int VW>
+__device__ __forceinline__ void ld_gv(const float* p, float (&f)[VW]) {
+    if constexpr (VW == 1) {
+        f[0] = __ldg(p);
+    } else if constexpr (VW == 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+        f[0] = v.x; f[1] = v.y;
+    } else {
 #pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    auto meta = [&](uint32_t c0, int& b, float& s) {
-        const uint32_t i = c0 + lane;
-        b = -1;
-        s = 1.f;
-        if (i < s1) {
-            const uint32_t pos = __ldg(pos_sorted + i);
-            if (pos < (uint32_t)a.N) {
-                const int64_t bag = (int64_t)__ldg(ws.bag + pos);
-                if (bag >= tB && bag < tB + a.B) b = (int)(bag - tB);
-                if (a.has_scale) s = __ldg(ws.scale + pos);
-            }
+        for (int h = 0; h < VW / 4; ++h) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + h);
+            f[4 * h] = v.x; f[4 * h + 1] = v.y; f[4 * h + 2] = v.z; f[4 * h + 3] = v.w;
         }
-    };
-    int cb;
-    float cs;
-    meta(s0, cb, cs);
-    for (uint32_t c0 = s0; c0 < s1; c0 += 32) {
-        int nb;
-        float ns;
-        meta(c0 + 32, nb, ns);
-        const int n = (int)tmin<uint32_t>(32u, s1 - c0);
-#pragma unroll
-        for (int k0 = 0; k0 < 32; k0 += STEP) {
-            if (k0 >= n) break;
-            int bb[GROUP];
-            float ss[GROUP];
-            float g[GROUP][NB][VW];
-#pragma unroll
-            for (int u = 0; u < GROUP; ++u) {
-                const int e = k0 + u * NG + grp;  // this group's lookup within the 32
-                bb[u] = __shfl_sync(0xffffffffu, cb, e);
-                ss[u] = __shfl_sync(0xffffffffu, cs, e);
-                if (e >= n) bb[u] = -1;
-                const float* grow = a.grad + (int64_t)(bb[u] < 0 ? 0 : bb[u]) * a.total_d + td.doff;
-#pragma unroll
-                for (int q = 0; q < NB; ++q) {
-                    if (bb[u] >= 0) {
-                        ld_grad4(grow + S::col(lane, q), g[u][q]);
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < VW; ++v) g[u][q][v] = 0.f;
-                    }
-                }
-            }
-            // the step's GROUP lookups in plain fp32 (a skipped lookup's
-            // row is zero: adding it changes nothing), the step's sum into
-            // the chunk's with compensated addition
-            float blk[NB][VW];
-#pragma unroll
-            for (int q = 0; q < NB; ++q)
-#pragma unroll
-                for (int v = 0; v < VW; ++v) blk[q][v] = 0.f;
-#pragma unroll
-            for (int u = 0; u < GROUP; ++u)
-#pragma unroll
-                for (int q = 0; q < NB; ++q) {
-                    ffma2(blk[q][0], blk[q][1], ss[u], g[u][q][0], g[u][q][1]);
-                    ffma2(blk[q][2], blk[q][3], ss[u], g[u][q][2], g[u][q][3]);
-                }
-#pragma unroll
-            for (int q = 0; q < NB; ++q)
-#pragma unroll
-                for (int v = 0; v < VW; ++v) acc[q][v].add(blk[q][v]);
-        }
-        cb = nb;
-        cs = ns;
     }
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) {
-            float x = acc[q][v].value();
-            if constexpr (NG > 1) x = group_sum<LPR>(x);
-            if (grp == 0) part_row[S::col(lane, q) + v] = x;
-        }
 }
 
-// The run's gradient: its nc partial rows added in chunk order (row group g
-// takes chunks g, g + NG, ..., PF rows in flight; compensated addition; the
-// groups' sums added last), then the row's optimizer step.
+// The same through L2 only (partial rows written by other warps of this
+// kernel).
+template <int VW>
+__device__ __forceinline__ void ld_gv_cg(const float* p, float (&f)[VW]) {
+    if constexpr (VW == 1) {
+        f[0] = __ldcg(p);
+    } else if constexpr (VW == 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+        f[0] = v.x; f[1] = v.y;
+    } else {
+#pragma unroll
+        for (int h = 0; h < VW / 4; ++h) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p) + h);
+            f[4 * h] = v.x; f[4 * h + 1] = v.y; f[4 * h + 2] = v.z; f[4 * h + 3] = v.w;
+        }
+    }
+}
+
+template <int VW>
+__device__ __forceinline__ void st_fv(float* p, const float (&f)[VW]) {
+    if constexpr (VW == 1) {
+        p[0] = f[0];
+    } else if constexpr (VW == 2) {
+        *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < VW / 4; ++h)
+            reinterpret_cast<float4*>(p)[h] = make_float4(f[4 * h], f[4 * h + 1], f[4 * h + 2], f[4 * h + 3]);
+    }
+}
+
+// acc += s * x over VW columns (packed two-wide FMAs).
+template <int VW>
+__device__ __forceinline__ void fma_v(float (&acc)[VW], float s, const float (&x)[VW]) {
+    if constexpr (VW == 1) {
+        acc[0] = fmaf(s, x[0], acc[0]);
+    } else {
+#pragma unroll
+        for (int v = 0; v < VW; v += 2) ffma2(acc[v], acc[v + 1], s, x[v], x[v + 1]);
+    }
+}
+
+// A lane's VW consecutive elements of a table row, kept as raw 32-bit words.
+template <int DT, int VW>
+struct RowV {
+    static constexpr int W = DT == DT_F32 ? VW : (VW + 1) / 2;
+
+    // p: the lane's first element
+    __device__ __forceinline__ static void load(uint32_t (&w)[W], const void* p) {
+        if constexpr (DT == DT_F32) {
+            if constexpr (VW == 1) {
+                w[0] = *reinterpret_cast<const uint32_t*>(p);
+            } else if constexpr (VW == 2) {
+                const uint2 v = *reinterpret_cast<const uint2*>(p);
+                w[0] = v.x; w[1] = v.y;
+            } else {
+#pragma unroll
+                for (int h = 0; h < VW / 4; ++h) {
+                    const uint4 v = reinterpret_cast<const uint4*>(p)[h];
+                    w[4 * h] = v.x; w[4 * h + 1] = v.y; w[4 * h + 2] = v.z; w[4 * h + 3] = v.w;
+                }
+            }
+        } else {
+            if constexpr (VW == 1) {
+                w[0] = *reinterpret_cast<const unsigned short*>(p);
+            } else if constexpr (VW == 2) {
+                w[0] = *reinterpret_cast<const uint32_t*>(p);
+            } else if constexpr (VW == 4) {
+                const uint2 v = *reinterpret_cast<const uint2*>(p);
+                w[0] = v.x; w[1] = v.y;
+            } else {
+                const uint4 v = *reinterpret_cast<const uint4*>(p);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            }
+        }
+    }
+
+    __device__ __forceinline__ static void store(const uint32_t (&w)[W], void* p) {
+        if constexpr (DT == DT_F32) {
+            if constexpr (VW == 1) {
+                *reinterpret_cast<uint32_t*>(p) = w[0];
+            } else if constexpr (VW == 2) {
+                *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+            } else {
+#pragma unroll
+                for (int h = 0; h < VW / 4; ++h)
+                    reinterpret_cast<uint4*>(p)[h] = make_uint4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
+            }
+        } else {
+            if constexpr (VW == 1) {
+                *reinterpret_cast<unsigned short*>(p) = (unsigned short)(w[0] & 0xffffu);
+            } else if constexpr (VW == 2) {
+                *reinterpret_cast<uint32_t*>(p) = w[0];
+            } else if constexpr (VW == 4) {
+                *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+            } else {
+                *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+
+    __device__ __forceinline__ static float get(const uint32_t (&w)[W], int v) {
+        if constexpr (DT == DT_F32) {
+            return __uint_as_float(w[v]);
+        } else {
+            const uint32_t h = (w[v / 2] >> (16 * (v & 1))) & 0xffffu;
+            return DT == DT_F16 ? h_bits_to_float(h) : bf16_bits_to_float(h);
+        }
+    }
+
+    __device__ __forceinline__ static void set(uint32_t (&w)[W], int v, float x) {
+        if constexpr (DT == DT_F32) {
+            w[v] = __float_as_uint(x);
+        } else {
+            const uint32_t h = DT == DT_F16 ? (uint32_t)__half_as_ushort(__float2half_rn(x))
+                                            : (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+            uint32_t& word = w[v / 2];
+            word = (v & 1) ? ((word & 0x0000ffffu) | (h << 16)) : ((word & 0xffff0000u) | h);
+        }
+    }
+};
+
+// Optimizer step of one row held by the whole warp, given its gradient g
+// (this lane's columns);
+// `row` holds the old values and receives the new ones.  m_old: the row's
+// Adagrad state (ignored by SGD); returns the new state.
+template <int DT, int VW>
+__device__ __forceinline__ float optimizer_step_w(const ApplyArgs& a, int dim, const float (&g)[VW],
+                                                uint32_t (&row)[RowV<DT, VW>::W], float m_old) {
+    using R = RowV<DT, VW>;
+    if (a.opt == 2) {
+        float sq = 0.f;
+#pragma unroll
+        for (int v = 0; v < VW; ++v) sq = fmaf(g[v], g[v], sq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        const float m = m_old + __fdiv_rn(sq, (float)dim);
+        // lr / (sqrt(m) + eps) once per row (rounded once more than a
+        // division per column)
+        const float step = __fdiv_rn(a.lr, sqrtf(m) + a.eps);
+#pragma unroll
+        for (int v = 0; v < VW; ++v) R::set(row, v, fmaf(-step, g[v], R::get(row, v)));
+        return m;
+    }
+#pragma unroll
+    for (int v = 0; v < VW; ++v) R::set(row, v, fmaf(-a.lr, g[v], R::get(row, v)));
+    return m_old;
+}
+
+// ------------------------------------------------- streaming the lookups
+
+// Raw metadata of the sorted slot a lane looks ahead at: its flat bag
+// (0xffffffff past the stream or for an invalid position) and its scale.
+template <bool HS>
+__device__ __forceinline__ void meta_issue(const ApplyArgs& a, const Workspace& ws, uint32_t pos, uint32_t& bag,
+                                           float& s) {
+    bag = 0xffffffffu;
+    s = 0.f;
+    if (pos < (uint32_t)a.N) {
+        bag = __ldg(ws.bag + pos);
+        if constexpr (HS) s = __ldg(ws.scale + pos);
+    }
+}
+
+__device__ __forceinline__ uint32_t pos_issue(const uint32_t* pos_sorted, uint32_t i, uint32_t end) {
+    return i < end ? __ldg(pos_sorted + i) : 0xffffffffu;
+}
+
+// The slots [E0, E1) of one table t as a stream of 32-slot windows.  Lane k
+// holds, for the current window w, cb = bag row of slot w + k within the
+// table (-1 if none) and cs = its scale; the next window's raw bag and scale
+// and the positions of the one after are in flight meanwhile.
+template <bool HS>
+struct Stream {
+    uint32_t p;     // positions of window w + 64
+    uint32_t nbag;  // raw bags of window w + 32
+    float ns;       // raw scales of window w + 32
+    int cb;
+    float cs;
+
+    __device__ __forceinline__ void start(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                          uint32_t E0, uint32_t E1, int lane) {
+        const uint32_t p0 = pos_issue(pos_sorted, E0 + lane, E1);
+        meta_issue<HS>(a, ws, p0, nbag, ns);
+        p = pos_issue(pos_sorted, E0 + 32 + lane, E1);
+    }
+    // Makes window w current and issues the loads of the two after it.
+    __device__ __forceinline__ void advance(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                            uint32_t w, uint32_t E1, uint32_t tB, int lane) {
+        const uint32_t rel = nbag - tB;
+        cb = rel < (uint32_t)a.B ? (int)rel : -1;
+        cs = cb < 0 ? 0.f : (HS ? ns : 1.f);
+        meta_issue<HS>(a, ws, p, nbag, ns);
+        p = pos_issue(pos_sorted, w + 64 + lane, E1);
+    }
+};
+
+// Gradient rows of the lookups k0 .. k0+G-1 of the current window (those at
+// or past n, or without a bag, read as zero rows).
+template <int VW, int G, bool FULL>
+__device__ __forceinline__ void load_step(const ApplyArgs& a, const float* gb, int cb, int k0, int n,
+                                          float (&g)[G][VW]) {
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+        const int k = k0 + u;
+        const int b = __shfl_sync(0xffffffffu, cb, k & 31);
+        if (FULL) {
+            ld_gv<VW>(gb + (int64_t)b * a.total_d, g[u]);
+        } else if (k < n && b >= 0) {
+            ld_gv<VW>(gb + (int64_t)b * a.total_d, g[u]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < VW; ++v) g[u][v] = 0.f;
+        }
+    }
+}
+
+// The scale of lookup k of the current window (0 for one without a bag).
+__device__ __forceinline__ float step_scale(float cs, int k) { return __shfl_sync(0xffffffffu, cs, k & 31); }
+
+// ------------------------------------------------------------- long runs
+
+// Partial sum of one chunk, sorted slots [s0, s1) of one key of table t:
+// each step's G products summed in fp32, the step sums added with
+// compensated addition (consecutive lookups of a long run often share a
+// bag, so sums over many of them would grow and round coarsely); written to
+// part_row.
+template <int CODE, bool HS>
+__device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+                                               const TableDesc& td, int t, uint32_t s0, uint32_t s1, float* part_row,
+                                               int lane) {
+    using V = VecShape<CODE>;
+    constexpr int VW = V::VW, G = V::G;
+    const uint32_t tB = (uint32_t)t * (uint32_t)a.B;
+    const float* gb = a.grad + td.doff + lane * VW;
+    float sum[VW], cmp[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) sum[v] = cmp[v] = 0.f;
+    // one step's sum into the compensated totals
+    auto add_step = [&](const float (&blk)[VW]) {
+        if constexpr (VW == 1) {
+            Kahan k{sum[0], cmp[0]};
+            k.add(blk[0]);
+            sum[0] = k.s;
+            cmp[0] = k.c;
+        } else {
+#pragma unroll
+            for (int v = 0; v < VW; v += 2) kahan2(sum[v], sum[v + 1], cmp[v], cmp[v + 1], blk[v], blk[v + 1]);
+        }
+    };
+    Stream<HS> st;
+    st.start(a, ws, pos_sorted, s0, s1, lane);
+    for (uint32_t w = s0; w < s1; w += 32) {
+        st.advance(a, ws, pos_sorted, w, s1, tB, lane);
+        const int n = (int)tmin<uint32_t>(32u, s1 - w);
+        if (n == 32 && __all_sync(0xffffffffu, st.cb >= 0)) {
+#pragma unroll 1
+            for (int k0 = 0; k0 < 32; k0 += G) {
+                float g[G][VW], blk[VW];
+                load_step<VW, G, true>(a, gb, st.cb, k0, 32, g);
+#pragma unroll
+                for (int v = 0; v < VW; ++v) blk[v] = 0.f;
+#pragma unroll
+                for (int u = 0; u < G; ++u) fma_v<VW>(blk, HS ? step_scale(st.cs, k0 + u) : 1.f, g[u]);
+                add_step(blk);
+            }
+        } else {
+#pragma unroll 1
+            for (int k0 = 0; k0 < n; k0 += G) {
+                float g[G][VW], blk[VW];
+                load_step<VW, G, false>(a, gb, st.cb, k0, n, g);
+#pragma unroll
+                for (int v = 0; v < VW; ++v) blk[v] = 0.f;
+#pragma unroll
+                for (int u = 0; u < G; ++u) fma_v<VW>(blk, HS ? step_scale(st.cs, k0 + u) : 1.f, g[u]);
+                add_step(blk);
+            }
+        }
+    }
+    float x[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) x[v] = sum[v] - cmp[v];
+    st_fv<VW>(part_row + lane * VW, x);
+}
+
+// The run's gradient: its nc partial rows added in chunk order (PF rows in
+// flight, compensated addition), then the row's optimizer step.
 template <int DT, int CODE>
-__device__ __forceinline__ void long_combine(const ApplyArgs& a, const TableDesc& td, uint32_t key,
-                                             const float* part0, uint32_t nc, int lane) {
-    using Sh = ShapeOf<CODE>;
-    constexpr int VW = Sh::VW, NB = Sh::NB, LPR = Sh::LPR, NG = Sh::NG;
-    using S = Slice<DT, VW, NB, LPR>;
-    const int grp = lane / LPR;
-    Kahan acc[NB][VW];
+__device__ __forceinline__ void long_combine_vec(const ApplyArgs& a, const TableDesc& td, uint32_t key,
+                                                 const float* part0, uint32_t nc, int lane) {
+    using V = VecShape<CODE>;
+    constexpr int VW = V::VW, PF = V::PF;
+    using R = RowV<DT, VW>;
+    Kahan acc[VW];
 #pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) acc[q][v] = Kahan{0.f, 0.f};
-    constexpr int PF = 8 / NB;  // partial rows in flight per row group
-    for (uint32_t j0 = 0; j0 < nc; j0 += PF * NG) {
-        float4 x[PF][NB];
+    for (int v = 0; v < VW; ++v) acc[v] = Kahan{0.f, 0.f};
+    for (uint32_t j0 = 0; j0 < nc; j0 += PF) {
+        float x[PF][VW];
 #pragma unroll
         for (int k = 0; k < PF; ++k) {
-            const uint32_t j = j0 + (uint32_t)(k * NG + grp);
-            const float* p = part0 + (int64_t)(j < nc ? j : 0) * a.part_stride;
-#pragma unroll
-            for (int q = 0; q < NB; ++q) x[k][q] = __ldcg(reinterpret_cast<const float4*>(p + S::col(lane, q)));
+            const uint32_t j = j0 + (uint32_t)k;
+            ld_gv_cg<VW>(part0 + (int64_t)(j < nc ? j : 0) * a.part_stride + lane * VW, x[k]);
         }
 #pragma unroll
         for (int k = 0; k < PF; ++k)
-            if (j0 + (uint32_t)(k * NG + grp) < nc)
+            if (j0 + (uint32_t)k < nc)
 #pragma unroll
-                for (int q = 0; q < NB; ++q) {
-                    acc[q][0].add(x[k][q].x);
-                    acc[q][1].add(x[k][q].y);
-                    acc[q][2].add(x[k][q].z);
-                    acc[q][3].add(x[k][q].w);
-                }
+                for (int v = 0; v < VW; ++v) acc[v].add(x[k][v]);
     }
-    float g[NB][VW];
+    float g[VW];
 #pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) {
-            g[q][v] = acc[q][v].value();
-            if constexpr (NG > 1) g[q][v] = group_sum<LPR>(g[q][v]);
-        }
-    uint32_t row[S::WORDS];
-    const int64_t r = (int64_t)key - td.rowbase;
-    S::load(row, td.data, r, td.dim, lane);
+    for (int v = 0; v < VW; ++v) g[v] = acc[v].value();
+    char* rp = static_cast<char*>(td.data) + ((int64_t)key - td.rowbase) * td.row_bytes +
+               (int64_t)lane * VW * elem_bytes(DT);
+    uint32_t row[R::W];
+    R::load(row, rp);
     const float m_old = a.opt == 2 ? a.state[key] : 0.f;
-    const float m = optimizer_step<DT, VW, NB, LPR>(a, td.dim, g, row, m_old);
-    if (grp == 0) S::store(row, td.data, r, td.dim, lane);
+    const float m = optimizer_step_w<DT, VW>(a, V::D, g, row, m_old);
+    R::store(row, rp);
     if (a.opt == 2 && lane == 0) a.state[key] = m;
 }
+
 
 template <int DT, int CODE>
 __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
@@ -653,7 +857,10 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
             }
         }
     } else {
-        long_chunk_vec<DT, CODE>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
+        if (a.has_scale)
+            long_chunk_vec<CODE, true>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
+        else
+            long_chunk_vec<CODE, false>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
     }
     // 2) the warp that finishes a run's last chunk combines all of them
     __threadfence();
@@ -667,7 +874,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
     if constexpr (CODE == SHAPE_GENERIC)
         generic_row<DT>(a, ws, pos_sorted, td, t, key, 0, 0, part0, nc, lane);
     else
-        long_combine<DT, CODE>(a, td, key, part0, nc, lane);
+        long_combine_vec<DT, CODE>(a, td, key, part0, nc, lane);
     // every chunk of this run has been counted: reset for the next apply call
     if (lane == 0) ws.chunk_done[base] = 0;
 }
@@ -755,14 +962,15 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
             const uint32_t r0 = __ldg(ws.runstart + u);
             const uint32_t r1 = tmin<uint32_t>(__ldg(ws.runstart + u + 1), N);
             if (r1 <= r0) continue;
-            const uint32_t nc = (r1 - r0 + kLongRun - 1) / kLongRun;
+            const uint32_t chunk = (uint32_t)a.chunk;
+            const uint32_t nc = (r1 - r0 + chunk - 1) / chunk;
             const uint32_t jc = g - g0;
             const uint32_t key = __ldg(ws.uniq + u);
             if (jc >= nc || g0 + nc > nchunks || key < (uint64_t)td.rowbase ||
                 (uint64_t)key >= (uint64_t)td.rowbase + (uint64_t)td.rows)
                 continue;
-            const uint32_t s0 = r0 + jc * kLongRun;
-            const uint32_t s1 = tmin<uint32_t>(s0 + (uint32_t)kLongRun, r1);
+            const uint32_t s0 = r0 + jc * chunk;
+            const uint32_t s1 = tmin<uint32_t>(s0 + chunk, r1);
             long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, g, g0, nc, lane);
         } else {
             const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);

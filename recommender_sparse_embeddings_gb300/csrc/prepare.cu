@@ -18,9 +18,10 @@
 //     (rle_count_kernel), a scan over the tiles, then rle_kernel writes the
 //     distinct keys with their first sorted slot (runstart[U] = N) and the
 //     first distinct key of each table.
-//  4. chunk_count/chunk_write: number the 256-lookup chunks of every run of
-//     at least kLongRun lookups in key order (a scan over the distinct keys),
-//     so each table's chunks form one consecutive range for the apply step.
+//  4. chunk_count/chunk_write: number the chunks (256 to 1024 lookups, by
+//     batch size) of every run of at least kLongRun lookups in key order (a
+//     scan over the distinct keys), so each table's chunks form one
+//     consecutive range for the apply step.
 #include "tbe_internal.cuh"
 
 namespace tbe {
@@ -757,10 +758,9 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
     const uint32_t excl = block_exclusive_scan_256(__popc(heads), s_scan, &tile_total);
     const uint32_t U = tmin<uint32_t>(ws.counters[CTR_U], N);
     uint32_t u = ws.tcount[tile] + excl;
-    // table of a key, kept with its key range [t_lo, t_hi): sorted neighbours
-    // mostly share a table, so the search runs about once per table change
-    // the table of the previous key: sorted neighbours mostly share a table,
-    // so the search runs about once per table change
+    // the table of the previous key, kept with the end of its key range:
+    // sorted neighbours mostly share a table, so the search runs about once
+    // per table change
     int tprev = -1;
     uint32_t t_hi = 0u;  // first key past tprev's range
     if (p0 > 0 && p0 <= N) {
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(kSortThreads) rle_kernel(PrepArgs a, Workspace
 // Chunks of the long runs, numbered in key order after the run-length
 // encoding (count, scan, write over tiles of kSortTile distinct keys): every
 // run of at least kLongRun lookups gets its first chunk g0, the number of
-// chunks of all earlier runs; the run's ceil(len / kLongRun) chunks g0 ..
+// chunks of all earlier runs; the run's ceil(len / chunk) chunks g0 ..
 // get (u, g0) and the run's finished-chunk count (kept at g0) is cleared.
 // cstart[t] is the first chunk of table t (the chunk base at its first
 // distinct key) and cstart[T] the total, so the chunks of each table are one
@@ -827,7 +827,7 @@ __device__ __forceinline__ void run_chunks(const PrepArgs& a, const Workspace& w
         nc[q] = 0;
         const uint32_t r0 = tmin<uint32_t>(rs[q], N), r1 = tmin<uint32_t>(rs[q + 1], N);
         if (u0 + q < U && r1 > r0 && r1 - r0 >= (uint32_t)kLongRun && ws.uniq[u0 + q] < a.total_rows)
-            nc[q] = (r1 - r0 + kLongRun - 1) / kLongRun;
+            nc[q] = (r1 - r0 + (uint32_t)a.chunk - 1) / (uint32_t)a.chunk;
     }
 }
 

@@ -24,6 +24,15 @@ constexpr int kLongBag = 2048;
 constexpr int kLongBagCap = 1 << 16;
 // Runs of at least this many lookups take the chunked accumulate path.
 constexpr int kLongRun = 256;
+// Lookups per chunk of a long run for a batch of N lookups: 256, doubled up
+// to 1024 while the batch still makes at least eight chunks per apply warp
+// (3 CTAs of 8 warps per SM), so big batches take fewer, longer work items.
+inline int long_chunk_lookups(int64_t N, int num_sms) {
+    const int64_t warps = (int64_t)num_sms * 3 * 8;
+    int c = kLongRun;
+    while (c < 4 * kLongRun && N / (2 * c) >= 8 * warps) c *= 2;
+    return c;
+}
 // Keys per tile of the key, sort and run-length kernels (256 threads x 16).
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
@@ -112,6 +121,25 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x, fl
         "mov.b64 {%0, %1}, r;\n\t}"
         : "+f"(a0), "+f"(a1)
         : "f"(s), "f"(x), "f"(y));
+}
+
+// Compensated (Kahan) addition of (x0, x1) into the sums (s0, s1) with
+// compensations (c0, c1), both halves at once with packed fp32 adds (each
+// half rounds exactly like the scalar steps y = x - c, t = s + y,
+// c = (t - s) - y, s = t).
+__device__ __forceinline__ void kahan2(float& s0, float& s1, float& c0, float& c1, float x0, float x1) {
+    asm("{\n\t.reg .b64 S, C, X, Y, T, D;\n\t"
+        "mov.b64 S, {%0, %1};\n\t"
+        "mov.b64 C, {%2, %3};\n\t"
+        "mov.b64 X, {%4, %5};\n\t"
+        "sub.rn.f32x2 Y, X, C;\n\t"
+        "add.rn.f32x2 T, S, Y;\n\t"
+        "sub.rn.f32x2 D, T, S;\n\t"
+        "sub.rn.f32x2 C, D, Y;\n\t"
+        "mov.b64 {%0, %1}, T;\n\t"
+        "mov.b64 {%2, %3}, C;\n\t}"
+        : "+f"(s0), "+f"(s1), "+f"(c0), "+f"(c1)
+        : "f"(x0), "f"(x1));
 }
 
 // Unpack one 16-byte vector of DT into E = 16/sizeof(DT) floats.
@@ -285,6 +313,7 @@ struct PrepArgs {
     int key_bits;
     int digit_bits;  // radix digit width (8 or 9)
     int compact;     // dense tables present (their lookups are not sorted)
+    int chunk;       // lookups per chunk of a long run (long_chunk_lookups)
 };
 
 // Backward row-shape codes: dim 32, 64, 128, 256 with aligned rows and
@@ -305,6 +334,7 @@ struct ApplyArgs {
     int grad_vec;  // grad is 16-byte aligned (vector loads allowed)
     int total_d;
     int part_stride;  // floats per partial-sum row (multiple of 4)
+    int chunk;        // lookups per chunk of a long run (as the preparation used)
     uint32_t total_rows;
     int has_scale;  // filled in on the device from CTR_HAS_SCALE
     int opt;
