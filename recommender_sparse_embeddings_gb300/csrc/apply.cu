@@ -9,8 +9,8 @@
 // kernels run side by side on the handle's apply streams.  A class kernel
 // walks a work list table by table: the chunks of the table's long runs
 // (numbered in key order by the preparation step; 256 to 1024 lookups, by
-// batch size), then batches of kBatchRows consecutive distinct keys.  Warps
-// take work items from a per-class atomic counter.
+// batch size), then batches of up to kBatchRows consecutive distinct keys.
+// Warps take work items from a per-class atomic counter.
 //
 //  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
 //    batch into pieces of at most R keys and walks each piece's sorted lookups
@@ -42,7 +42,13 @@
 
 namespace tbe {
 
-constexpr int kBatchRows = 16;  // distinct keys per short-run work item
+// Distinct keys per short-run work item: 31 (every lane then holds a key's
+// first slot, lane n the batch's end), or 16 when the batch would then give
+// the apply warps fewer than sixteen items each (measured: the longer
+// batches pay off on the hot-row workload, 23 items a warp, and lose on the
+// mixed workload, 11).
+constexpr int kBatchRows = 31;
+constexpr int kBatchRowsSmall = 16;
 // Resident CTAs of 256 threads per SM the class kernels are built for (80
 // registers a thread); the grid is one wave of them.
 constexpr int kApplyCtasPerSm = 3;
@@ -198,6 +204,19 @@ struct Meta {
     float s;
 };
 
+// Gradient rows in flight per row group (GROUP; NG*GROUP lookups per warp
+// step, 2 KB of gradient per warp) and keys per piece (R), whose table-row
+// slices and gradient sums stay in registers: R * (row words + columns) +
+// GROUP * columns live words per lane, at most about 40.
+template <int DT, int NB>
+struct ShortTune {
+    static constexpr int WORDS = Slice<DT, 4, NB, 32>::WORDS;
+    static constexpr int COLS = 4 * NB;
+    static constexpr int GROUP = 4 / NB;
+    static constexpr int R0 = (40 - GROUP * COLS) / (WORDS + COLS);
+    static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
+};
+
 __device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
                                           uint32_t w, uint32_t Eend, int64_t tB, int lane) {
     const uint32_t i = w + lane;
@@ -213,22 +232,11 @@ __device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& w
     return m;
 }
 
-// Gradient rows in flight per row group (GROUP; NG*GROUP lookups per warp
-// step, 2 KB of gradient per warp) and keys per piece (R), whose table-row
-// slices and gradient sums stay in registers: R * (row words + columns) +
-// GROUP * columns live words per lane, at most about 40.
-template <int DT, int NB>
-struct ShortTune {
-    static constexpr int WORDS = Slice<DT, 4, NB, 32>::WORDS;
-    static constexpr int COLS = 4 * NB;
-    static constexpr int GROUP = 4 / NB;
-    static constexpr int R0 = (40 - GROUP * COLS) / (WORDS + COLS);
-    static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
-};
-
 // A sliding window over the batch's sorted lookups: metadata of lookups
 // [w0, w0 + 64) in two 32-lookup halves; the next half is fetched as soon as
-// the stream passes the middle, so it is in flight 32 lookups ahead.
+// the stream passes the middle, so it is in flight 32 lookups ahead.  (A
+// deeper pipeline, positions two halves ahead, measured slower: the extra
+// registers cost more than the waits it removes.)
 struct MetaWindow {
     uint32_t w0;
     Meta m0, m1;
@@ -900,6 +908,7 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
     const uint32_t nchunks =
         tmin<uint32_t>(*(volatile uint32_t*)&ws.counters[CTR_NCHUNK], (uint32_t)ws.max_chunks);
     const uint32_t N = (uint32_t)a.N;
+    const uint32_t kb = U / kBatchRows >= 16u * gridDim.x * (blockDim.x >> 5) ? kBatchRows : kBatchRowsSmall;
 
     // work items (chunks + batches) of the class's tables, exclusive-scanned
     uint32_t carry = 0;
@@ -912,7 +921,7 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
             const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
             const uint32_t cs = tmin<uint32_t>(__ldg(ws.cstart + t), nchunks);
             const uint32_t ce = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.cstart + t + 1), cs), nchunks);
-            ni = (ce - cs) + (ue - us + kBatchRows - 1) / kBatchRows;
+            ni = (ce - cs) + (ue - us + kb - 1) / kb;
         }
         uint32_t x = ni;
 #pragma unroll
@@ -975,9 +984,9 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
         } else {
             const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
             const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
-            const uint32_t u0 = us + (j - (ce - cs)) * kBatchRows;
+            const uint32_t u0 = us + (j - (ce - cs)) * kb;
             if (u0 >= ue) continue;
-            short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kBatchRows, ue - u0), lane);
+            short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kb, ue - u0), lane);
         }
     }
     // every warp has taken its last item: the last one to leave resets the
