@@ -97,6 +97,19 @@ def reduce_sum(value: float, device) -> float:
     return float(t.item())
 
 
+def wants_length_order(specs, mode: str) -> bool:
+    """TBE_FLAG_LENGTH_ORDER as a caller who knows the batch's length law
+    would set it: on for uniform lengths over a wide range (where it was
+    measured faster), off for fixed or Poisson lengths (where it was not)."""
+    if mode != "auto":
+        return mode == "on"
+    for sp in specs:
+        law = sp.length
+        if law[0] == "uniform" and law[2] >= 4 * max(law[1], 1):
+            return True
+    return False
+
+
 def barrier():
     if torch.distributed.is_available() and torch.distributed.is_initialized():
         torch.distributed.barrier()
@@ -354,9 +367,11 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
     batch = workloads.make_batch(cfg, dev, idx_dtype, specs)
     grad = workloads.make_grad(cfg, dev, specs)
     T, B, N = len(specs), cfg.B, batch.N
+    length_order = wants_length_order(specs, args.length_order)
     flags = (tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0) | (
         tbe.TBE_FLAG_SORTED_BACKWARD if args.sorted_backward else 0) | (
-        tbe.TBE_FLAG_FORCE_HISTOGRAM if args.histogram else 0)
+        tbe.TBE_FLAG_FORCE_HISTOGRAM if args.histogram else 0) | (
+        tbe.TBE_FLAG_LENGTH_ORDER if length_order else 0)
     h = tbe.tbe_create(tables, cfg.pooling, flags)
     ws = tbe.make_workspace(h, N, B, dev)
     out = torch.empty((B, h.total_dim), dtype=torch.float32, device=dev)
@@ -531,6 +546,7 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
                    "index_dtype": args.index_dtype, "optimizer": cfg.optimizer,
                    "parallelism": f"replicas x{world}",
                    "launch": "CUDA graph replay" if args.graph else "stream launches",
+                   "bag_order": "by length (TBE_FLAG_LENGTH_ORDER)" if length_order else "index order",
                    "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
         "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
                 "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
@@ -758,6 +774,9 @@ def main(argv=None):
                    help="no tensor-core path for small tables (gather forward, sorted backward)")
     p.add_argument("--histogram", action="store_true",
                    help="small tables' forward on the tensor-core histogram path")
+    p.add_argument("--length-order", choices=["auto", "on", "off"], default="auto",
+                   help="forward bags pooled in order of length (TBE_FLAG_LENGTH_ORDER); auto: for "
+                        "workloads whose bag lengths are drawn uniformly over a range spanning 4x or more")
     p.add_argument("--sorted-backward", action="store_true",
                    help="small tables take the sorted backward instead of the dense (tensor-core) one")
     p.add_argument("--tables", type=int, default=0,

@@ -38,6 +38,7 @@ TBE_OPT_SGD, TBE_OPT_ROWWISE_ADAGRAD = 1, 2
 TBE_FLAG_NO_HISTOGRAM = 0x1
 TBE_FLAG_FORCE_HISTOGRAM = 0x2
 TBE_FLAG_SORTED_BACKWARD = 0x4
+TBE_FLAG_LENGTH_ORDER = 0x8
 
 PATH_NAMES = {0: "gather", 1: "gather_elementwise", 2: "histogram"}
 

@@ -48,6 +48,10 @@ struct tbe_handle {
     int passes = 1;
     int last_B = -1;
     int parity = 0;
+    // the forward's length-keyed bag order: counts [T][kLenBuckets], flags
+    // [T], CTA counters [T], order [T][B]; grown when a batch needs more
+    void* dorder = nullptr;
+    int64_t order_cap = 0;  // bags (T x B) the order array holds
     int vec_out = 0;
     cudaStream_t side = nullptr;  // preparation stream of tbe_forward_prepare
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -282,7 +286,30 @@ int cuda_fail(cudaError_t e) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? TBE_OK : cuda_fail(e); }
 
+// Device bytes of the length-keyed order for n = T x B bags.
+size_t order_bytes(const tbe_handle* h, int64_t n) {
+    return sizeof(uint32_t) * ((size_t)h->T * (kLenBuckets + 2) + (size_t)n);
+}
+
 int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
+    const int64_t n = (int64_t)h->T * B;
+    if ((h->flags & TBE_FLAG_LENGTH_ORDER) && n > h->order_cap) {
+        // grow the order array (cudaFree waits for the device: no kernel
+        // still reads the old one)
+        if (h->dorder) cudaFree(h->dorder);
+        h->dorder = nullptr;
+        h->order_cap = 0;
+        const cudaError_t e = cudaMalloc(&h->dorder, order_bytes(h, n));
+        if (e != cudaSuccess) {
+            h->dorder = nullptr;
+            return e == cudaErrorMemoryAllocation ? TBE_ERR_NO_MEMORY : cuda_fail(e);
+        }
+        // the counts and the per-table CTA counters start at zero (the
+        // kernels leave them so)
+        const cudaError_t z = cudaMemset(h->dorder, 0, order_bytes(h, 0));
+        if (z != cudaSuccess) return cuda_fail(z);
+        h->order_cap = n;
+    }
     if (B == h->last_B) return TBE_OK;
     cudaError_t e = launch_forward_schedule(h->dtabs, h->T, B, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -302,7 +329,7 @@ int tbe_create(const tbe_table* tables, int32_t num_tables, int32_t pooling, uin
     if (!tables || num_tables <= 0) return TBE_ERR_INVALID_ARG;
     if (num_tables > kMaxTables) return TBE_ERR_UNSUPPORTED;
     if (pooling != TBE_POOL_SUM && pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
-    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM | TBE_FLAG_SORTED_BACKWARD))
+    if (flags & ~(TBE_FLAG_NO_HISTOGRAM | TBE_FLAG_FORCE_HISTOGRAM | TBE_FLAG_SORTED_BACKWARD | TBE_FLAG_LENGTH_ORDER))
         return TBE_ERR_INVALID_ARG;
     tbe_handle* h = new (std::nothrow) tbe_handle();
     if (!h) return TBE_ERR_NO_MEMORY;
@@ -514,6 +541,7 @@ void tbe_destroy(tbe_handle* h) {
         if (h->apply_streams[i]) cudaStreamDestroy(h->apply_streams[i]);
     }
     if (h->dev) cudaFree(h->dev);
+    if (h->dorder) cudaFree(h->dorder);
     delete h;
 }
 
@@ -553,6 +581,12 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
     a.total_warps = (int)warps;
     a.parity = h->parity;
     a.num_sms = h->num_sms;
+    if (h->dorder) {  // TBE_FLAG_LENGTH_ORDER
+        a.lcount = static_cast<uint32_t*>(h->dorder);
+        a.lflag = a.lcount + (size_t)h->T * kLenBuckets;
+        a.ldone = a.lflag + h->T;
+        a.order = a.ldone + h->T;
+    }
     rc = cuda_status(launch_forward(a, s));
     if (rc == TBE_OK && h->hist_f16.n + h->hist_bf16.n > 0)
         rc = cuda_status(launch_hist(a, h->hist_f16, h->hist_bf16, s));

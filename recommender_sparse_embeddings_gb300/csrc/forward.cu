@@ -246,6 +246,7 @@ __device__ __forceinline__ void bag_range(const FwdArgs& a, int64_t bag, int64_t
 
 template <typename IDX>
 __global__ void __launch_bounds__(256, 4) fwd_pool_kernel(FwdArgs a) {
+    chain_wait();  // returns at once unless launched chained (after the bag order)
     const int gw = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (gw >= a.total_warps) return;
     const int lane = threadIdx.x & 31;
@@ -265,8 +266,14 @@ __global__ void __launch_bounds__(256, 4) fwd_pool_kernel(FwdArgs a) {
     const int slot = lane / G, sub = lane % G;
     const int w = gw - td.warp_begin;
     const int cb = w % ncb;
-    const int b = (w / ncb) * (32 / G) + slot;
+    int b = (w / ncb) * (32 / G) + slot;
     if (b >= a.B) return;  // the whole slot leaves together
+    // length-keyed order: slot b takes the table's b-th bag by length
+    if (a.order && a.lflag[t]) {
+        const uint32_t ob = __ldg(a.order + (int64_t)t * a.B + b);
+        if (ob >= (uint32_t)a.B) return;  // (a permutation of the table's bags: never taken)
+        b = (int)ob;
+    }
     const unsigned mask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (slot * G));
     const int64_t bag = (int64_t)t * a.B + b;
     int64_t start, end;
@@ -423,6 +430,133 @@ __global__ void __launch_bounds__(256) fwd_long_kernel(FwdArgs a) {
     if (blockIdx.x == 0 && threadIdx.x == 0) a.blk->long_count[a.parity ^ 1] = 0;
 }
 
+// ------------------------------------------------------ length-keyed order
+//
+// A warp pools 32/G bags side by side and a CTA holds its SM slot until its
+// longest bag is done, so bags of very different lengths in one CTA leave
+// most of its lanes idle.  When a table's bags differ in length, its bags
+// are taken in order of length instead (a counting sort per table: lengths
+// bucketed, kLenBuckets buckets), so each CTA's bags are about equally long.
+// Each bag's result does not depend on which slot pools it.
+
+// Both kernels run one CTA per chunk of kOrderChunk bags of one table
+// (grid T x chunks); lcount and ldone are zero between calls (the last CTA
+// of each table clears them).
+constexpr int kOrderChunk = 4096;
+
+// Length bucket of bag b of table t.
+template <typename IDX>
+__device__ __forceinline__ uint32_t bag_len_bucket(const FwdArgs& a, int t, int b) {
+    const IDX* off = reinterpret_cast<const IDX*>(a.offsets);
+    const int64_t g = (int64_t)t * a.B + b;
+    const int64_t len = ld_index(off, g + 1) - ld_index(off, g);
+    return len < 0 ? 0u : (len >= kLenBuckets - 1 ? (uint32_t)(kLenBuckets - 1) : (uint32_t)len);
+}
+
+// Counts the chunk's bags per length bucket (shared memory, one atomic per
+// group of equal buckets in a warp) into lcount[t]; the table's last CTA
+// turns the counts into the buckets' first ranks and sets lflag[t] when the
+// table's bags have more than one length.
+template <typename IDX>
+__global__ void __launch_bounds__(256) bag_len_count_kernel(FwdArgs a, int chunks) {
+    __shared__ uint32_t s_cnt[kLenBuckets];
+    __shared__ uint32_t s_last;
+    const int t = (int)(blockIdx.x / (unsigned)chunks), j = (int)(blockIdx.x % (unsigned)chunks);
+    const int lane = threadIdx.x & 31;
+    if (a.tabs[t].path == PATH_HIST) {
+        if (j == 0 && threadIdx.x == 0) a.lflag[t] = 0u;
+        return;
+    }
+    for (int k = threadIdx.x; k < kLenBuckets; k += blockDim.x) s_cnt[k] = 0u;
+    __syncthreads();
+    const int b0 = j * kOrderChunk, b1 = tmin<int>(a.B, b0 + kOrderChunk);
+    for (int base = b0; base < b1; base += blockDim.x) {  // whole warps together
+        const int b = base + threadIdx.x;
+        const uint32_t l = b < b1 ? bag_len_bucket<IDX>(a, t, b) : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, l);
+        if (l != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[l], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    uint32_t* c = a.lcount + (int64_t)t * kLenBuckets;
+    for (int k = threadIdx.x; k < kLenBuckets; k += blockDim.x)
+        if (s_cnt[k]) atomicAdd(c + k, s_cnt[k]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.ldone + t, 1u) == (uint32_t)chunks - 1u;
+    __syncthreads();
+    if (!s_last) return;
+    // last CTA of the table: exclusive scan of the counts (warp 0)
+    __threadfence();
+    if (threadIdx.x < 32) {
+        constexpr int P = kLenBuckets / 32;
+        uint32_t v[P], sum = 0, nz = 0;
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            v[i] = __ldcg(c + lane * P + i);
+            sum += v[i];
+            nz += v[i] != 0u;
+        }
+        uint32_t x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) nz += __shfl_xor_sync(0xffffffffu, nz, o);
+        uint32_t run = x - sum;
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            c[lane * P + i] = run;
+            run += v[i];
+        }
+        if (lane == 0) {
+            a.lflag[t] = nz > 1u ? 1u : 0u;
+            a.ldone[t] = 0u;
+        }
+    }
+}
+
+// Every bag of a table with lflag set gets its rank: its bucket's next free
+// one (a warp's bags of one bucket take consecutive ranks in lane order).
+// The table's last CTA clears lcount[t] (and the first CTA does when the
+// table keeps index order).
+template <typename IDX>
+__global__ void __launch_bounds__(256) bag_len_order_kernel(FwdArgs a, int chunks) {
+    chain_wait();
+    __shared__ uint32_t s_last;
+    const int t = (int)(blockIdx.x / (unsigned)chunks), j = (int)(blockIdx.x % (unsigned)chunks);
+    const int lane = threadIdx.x & 31;
+    if (a.tabs[t].path == PATH_HIST) return;
+    uint32_t* c = a.lcount + (int64_t)t * kLenBuckets;
+    if (!a.lflag[t]) {
+        if (j == 0)
+            for (int k = threadIdx.x; k < kLenBuckets; k += blockDim.x) c[k] = 0u;
+        return;
+    }
+    const int b0 = j * kOrderChunk, b1 = tmin<int>(a.B, b0 + kOrderChunk);
+    for (int base = b0; base < b1; base += blockDim.x) {  // whole warps together
+        const int b = base + threadIdx.x;
+        const uint32_t l = b < b1 ? bag_len_bucket<IDX>(a, t, b) : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, l);
+        const int leader = __ffs(peers) - 1;
+        uint32_t r0 = 0;
+        if (l != 0xffffffffu && lane == leader) r0 = atomicAdd(c + l, (uint32_t)__popc(peers));
+        r0 = __shfl_sync(0xffffffffu, r0, leader);
+        if (l != 0xffffffffu) {
+            const uint32_t r = r0 + (uint32_t)__popc(peers & ((1u << lane) - 1u));
+            if (r < (uint32_t)a.B) a.order[(int64_t)t * a.B + r] = (uint32_t)b;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.ldone + t, 1u) == (uint32_t)chunks - 1u;
+    __syncthreads();
+    if (!s_last) return;
+    for (int k = threadIdx.x; k < kLenBuckets; k += blockDim.x) c[k] = 0u;
+    if (threadIdx.x == 0) a.ldone[t] = 0u;
+}
+
 // Warp map for batch size B: warp_begin[t] = sum over earlier non-histogram
 // tables of ceil(B / (32 / G_u)) * blocks_u.  One small CTA, launched when B
 // changes.
@@ -446,13 +580,33 @@ cudaError_t launch_forward_schedule(TableDesc* tabs, int T, int B, cudaStream_t 
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
     if (a.total_warps > 0) {
+        const bool ordered = a.order != nullptr;
+        if (ordered) {
+            // the length-keyed order: count (+ scan), then rank
+            const int chunks = (a.B + kOrderChunk - 1) / kOrderChunk;
+            const unsigned ogrid = (unsigned)((int64_t)a.T * chunks);
+            if (a.idx64)
+                bag_len_count_kernel<int64_t><<<ogrid, 256, 0, s>>>(a, chunks);
+            else
+                bag_len_count_kernel<int32_t><<<ogrid, 256, 0, s>>>(a, chunks);
+            const cudaError_t e = a.idx64
+                                      ? launch_chained(bag_len_order_kernel<int64_t>, dim3(ogrid), dim3(256), s, a, chunks)
+                                      : launch_chained(bag_len_order_kernel<int32_t>, dim3(ogrid), dim3(256), s, a, chunks);
+            if (e != cudaSuccess) return e;
+        }
         const int64_t threads = (int64_t)a.total_warps * 32;
         const unsigned grid = (unsigned)((threads + 255) / 256);
-        if (a.idx64)
-            fwd_pool_kernel<int64_t><<<grid, 256, 0, s>>>(a);
-        else
-            fwd_pool_kernel<int32_t><<<grid, 256, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e;
+        if (ordered) {
+            e = a.idx64 ? launch_chained(fwd_pool_kernel<int64_t>, dim3(grid), dim3(256), s, a)
+                        : launch_chained(fwd_pool_kernel<int32_t>, dim3(grid), dim3(256), s, a);
+        } else {
+            if (a.idx64)
+                fwd_pool_kernel<int64_t><<<grid, 256, 0, s>>>(a);
+            else
+                fwd_pool_kernel<int32_t><<<grid, 256, 0, s>>>(a);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
     }
     const unsigned lgrid = (unsigned)(a.num_sms > 0 ? a.num_sms : 1);

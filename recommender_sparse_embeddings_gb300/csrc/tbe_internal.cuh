@@ -221,7 +221,18 @@ struct FwdArgs {
     int total_warps;
     int parity;    // which long-bag counter this call uses
     int num_sms;
+    // length-keyed bag order (null: bags in index order): per table, the
+    // count of its bags of each length bucket (then the buckets' starts),
+    // whether its bags differ in length, and its bags ordered by length
+    uint32_t* lcount;  // [T][kLenBuckets]
+    uint32_t* lflag;   // [T]
+    uint32_t* ldone;   // [T]: CTAs of the table done (zero between calls)
+    uint32_t* order;   // [T][B]
 };
+
+// Bag-length buckets of the length-keyed order: lengths 0 .. kLenBuckets-2,
+// and longer ones together.
+constexpr int kLenBuckets = 256;
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 
