@@ -291,7 +291,8 @@ size_t order_bytes(const tbe_handle* h, int64_t n) {
     return sizeof(uint32_t) * ((size_t)h->T * (kLenBuckets + 2) + (size_t)n);
 }
 
-int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
+// With TBE_FLAG_LENGTH_ORDER: the order arrays, grown for T x B bags.
+int ensure_order(tbe_handle* h, int32_t B) {
     const int64_t n = (int64_t)h->T * B;
     if ((h->flags & TBE_FLAG_LENGTH_ORDER) && n > h->order_cap) {
         // grow the order array (cudaFree waits for the device: no kernel
@@ -310,6 +311,13 @@ int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
         if (z != cudaSuccess) return cuda_fail(z);
         h->order_cap = n;
     }
+    return TBE_OK;
+}
+
+// Order arrays and the forward's warp map for batch size B.
+int ensure_schedule(tbe_handle* h, int32_t B, cudaStream_t s) {
+    const int rc = ensure_order(h, B);
+    if (rc) return rc;
     if (B == h->last_B) return TBE_OK;
     cudaError_t e = launch_forward_schedule(h->dtabs, h->T, B, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -617,7 +625,27 @@ int tbe_per_sample_weight_grad(tbe_handle* h, const void* indices, const void* o
     a.grad_vec = h->total_d % 4 == 0 && ((uintptr_t)grad_out % 16) == 0;
     a.mean = h->pooling == TBE_POOL_MEAN;
     a.out = grad_weights;
-    return cuda_status(launch_wgrad(a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->flags & TBE_FLAG_LENGTH_ORDER) {
+        // the forward's length-keyed bag order, computed for this batch
+        rc = ensure_order(h, batch_size);
+        if (rc) return rc;
+        FwdArgs o{};
+        o.tabs = h->dtabs;
+        o.T = h->T;
+        o.B = batch_size;
+        o.offsets = offsets;
+        o.idx64 = a.idx64;
+        o.lcount = static_cast<uint32_t*>(h->dorder);
+        o.lflag = o.lcount + (size_t)h->T * kLenBuckets;
+        o.ldone = o.lflag + h->T;
+        o.order = o.ldone + h->T;
+        rc = cuda_status(launch_bag_order(o, s));
+        if (rc) return rc;
+        a.lflag = o.lflag;
+        a.order = o.order;
+    }
+    return cuda_status(launch_wgrad(a, s));
 }
 
 size_t tbe_backward_workspace_bytes(const tbe_handle* h, int64_t num_indices, int32_t batch_size) {

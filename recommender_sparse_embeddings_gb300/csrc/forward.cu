@@ -578,20 +578,24 @@ cudaError_t launch_forward_schedule(TableDesc* tabs, int T, int B, cudaStream_t 
     return cudaGetLastError();
 }
 
+// The length-keyed order (count with scan, then rank): two kernels on s; a
+// kernel that reads the order should follow them chained.
+cudaError_t launch_bag_order(const FwdArgs& a, cudaStream_t s) {
+    const int chunks = (a.B + kOrderChunk - 1) / kOrderChunk;
+    const unsigned ogrid = (unsigned)((int64_t)a.T * chunks);
+    if (a.idx64)
+        bag_len_count_kernel<int64_t><<<ogrid, 256, 0, s>>>(a, chunks);
+    else
+        bag_len_count_kernel<int32_t><<<ogrid, 256, 0, s>>>(a, chunks);
+    return a.idx64 ? launch_chained(bag_len_order_kernel<int64_t>, dim3(ogrid), dim3(256), s, a, chunks)
+                   : launch_chained(bag_len_order_kernel<int32_t>, dim3(ogrid), dim3(256), s, a, chunks);
+}
+
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
     if (a.total_warps > 0) {
         const bool ordered = a.order != nullptr;
         if (ordered) {
-            // the length-keyed order: count (+ scan), then rank
-            const int chunks = (a.B + kOrderChunk - 1) / kOrderChunk;
-            const unsigned ogrid = (unsigned)((int64_t)a.T * chunks);
-            if (a.idx64)
-                bag_len_count_kernel<int64_t><<<ogrid, 256, 0, s>>>(a, chunks);
-            else
-                bag_len_count_kernel<int32_t><<<ogrid, 256, 0, s>>>(a, chunks);
-            const cudaError_t e = a.idx64
-                                      ? launch_chained(bag_len_order_kernel<int64_t>, dim3(ogrid), dim3(256), s, a, chunks)
-                                      : launch_chained(bag_len_order_kernel<int32_t>, dim3(ogrid), dim3(256), s, a, chunks);
+            const cudaError_t e = launch_bag_order(a, s);
             if (e != cudaSuccess) return e;
         }
         const int64_t threads = (int64_t)a.total_warps * 32;

@@ -235,6 +235,9 @@ struct FwdArgs {
 constexpr int kLenBuckets = 256;
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+// The length-keyed bag order alone (reads T, B, offsets, idx64, tabs and
+// the order arrays of a).
+cudaError_t launch_bag_order(const FwdArgs& a, cudaStream_t s);
 
 // Gradient of the per-sample weights (wgrad.cu).
 struct WgradArgs {
@@ -251,8 +254,13 @@ struct WgradArgs {
     int grad_vec;       // grad rows and table column offsets allow 16-byte loads
     int mean;
     float* out;         // [N]
+    // length-keyed bag order (null: index order), as the forward's
+    const uint32_t* lflag;  // [T]
+    const uint32_t* order;  // [T][B]
 };
 
+// With a.order set, the bag order was just launched on s and the kernel
+// follows it chained.
 cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s);
 
 // Small-table tensor-core path (hist.cu).  One launch per table dtype.

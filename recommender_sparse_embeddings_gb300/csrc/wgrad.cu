@@ -191,11 +191,19 @@ __device__ __forceinline__ void wgrad_bag(const TableDesc& td, const WgradArgs& 
 
 template <typename IDX>
 __global__ void __launch_bounds__(256, 4) wgrad_kernel(WgradArgs a) {
-    const int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // one warp per bag
+    chain_wait();  // returns at once unless launched chained (after the bag order)
+    int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // one warp per bag
     if (bag >= (int64_t)a.T * a.B) return;
     const int lane = threadIdx.x & 31;
     const int t = (int)(bag / a.B);
-    const int b = (int)(bag - (int64_t)t * a.B);
+    int b = (int)(bag - (int64_t)t * a.B);
+    // length-keyed order: warp b takes the table's b-th bag by length
+    if (a.order && a.lflag[t]) {
+        const uint32_t ob = __ldg(a.order + bag);
+        if (ob >= (uint32_t)a.B) return;  // (a permutation of the table's bags: never taken)
+        b = (int)ob;
+        bag = (int64_t)t * a.B + b;
+    }
     const TableDesc td = a.tabs[t];
     int64_t start, end;
     wg_bag_range<IDX>(a, bag, start, end, lane == 0);
@@ -214,6 +222,9 @@ cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s) {
     const int64_t warps = (int64_t)a.T * a.B;
     if (warps == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+    if (a.order)
+        return a.idx64 ? launch_chained(wgrad_kernel<int64_t>, dim3(blocks), dim3(256), s, a)
+                       : launch_chained(wgrad_kernel<int32_t>, dim3(blocks), dim3(256), s, a);
     if (a.idx64)
         wgrad_kernel<int64_t><<<blocks, 256, 0, s>>>(a);
     else

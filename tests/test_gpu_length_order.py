@@ -78,3 +78,30 @@ def test_length_order_repeated_calls_are_stable():
     assert tbe.tbe_get_error(h) == tbe.TBE_OK
     assert torch.equal(first.view(torch.int32), again.view(torch.int32))
     h.close()
+
+
+@pytest.mark.parametrize("pooling", ["sum", "mean"])
+def test_length_order_weight_gradient(pooling):
+    """The per-sample weight gradient with the length-keyed order: the same
+    bits as index order, and the oracle's values."""
+    import oracle
+    from helpers import DT_NAME, FP32_TOL, table_bits
+    from test_gpu_wgrad import allowance, values
+    tables = make_tables(11)
+    h_ord = tbe.tbe_create(tables, pooling, tbe.TBE_FLAG_NO_HISTOGRAM | tbe.TBE_FLAG_LENGTH_ORDER)
+    h_idx = tbe.tbe_create(tables, pooling, tbe.TBE_FLAG_NO_HISTOGRAM)
+    B = 1200
+    ind, off, _ = make_batch(B, 12)
+    total_d = sum(d for _, d, _ in SPECS)
+    grad = torch.randn((B, total_d), generator=torch.Generator().manual_seed(13))
+    got = tbe.tbe_per_sample_weight_grad(h_ord, ind.to(DEV), off.to(DEV), B, grad.to(DEV))
+    base = tbe.tbe_per_sample_weight_grad(h_idx, ind.to(DEV), off.to(DEV), B, grad.to(DEV))
+    assert tbe.tbe_get_error(h_ord) == tbe.TBE_OK
+    assert torch.equal(got.view(torch.int32), base.view(torch.int32))
+    ref = oracle.weight_grad([table_bits(t) for t in tables], [DT_NAME[t.dtype] for t in tables],
+                             ind.numpy(), off.numpy(), B, grad.numpy(), pooling=pooling)
+    tol = dict(FP32_TOL)
+    tol["atol"] = tol["atol"] + allowance(values(tables), ind.numpy(), off.numpy(), B, grad.numpy(), pooling)
+    assert_close(got.cpu().numpy(), ref, what="weight gradient, length order", **tol)
+    h_ord.close()
+    h_idx.close()
