@@ -589,19 +589,24 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
         bufs = [dict(ind=torch.empty_like(ind), off=torch.empty_like(off),
                      w=None if w is None else torch.empty_like(w), grad=torch.empty_like(grad),
                      out=torch.empty_like(out)) for _ in range(2)]
-        copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        # copies in on two streams (the batch on one, the upstream gradient on
+        # the other, so two copy engines work at once), out on a third
+        copy_in, copy_in2, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]     # buffer i holds its step's inputs
         ev_used = [torch.cuda.Event() for _ in range(2)]   # buffer i's step has read its inputs
         ev_out = [torch.cuda.Event() for _ in range(2)]    # buffer i's output is on the host
 
         def copy_inputs(i):
             copy_in.wait_event(ev_used[i])
+            copy_in2.wait_event(ev_used[i])
             with torch.cuda.stream(copy_in):
                 bufs[i]["ind"].copy_(h_ind, non_blocking=True)
                 bufs[i]["off"].copy_(h_off, non_blocking=True)
                 if h_w is not None:
                     bufs[i]["w"].copy_(h_w, non_blocking=True)
+            with torch.cuda.stream(copy_in2):
                 bufs[i]["grad"].copy_(h_grad, non_blocking=True)
+            copy_in.wait_stream(copy_in2)
             ev_in[i].record(copy_in)
 
         def e2e_step(k, last):
@@ -640,8 +645,8 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
             (0 if w is None else w.numel() * 4) + grad.numel() * 4
         rec["e2e"] = {"value": units * args.steps / (e2e_ms / 1e3), "unit": "lookups/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": out.numel() * 4, "ms_per_step": e2e_ms / args.steps,
-                      "pipelining": "two buffer sets: step k+1's inputs copy in during step k, step k's "
-                                    "output copies out beside its apply",
+                      "pipelining": "two buffer sets: step k+1's inputs copy in during step k (batch and "
+                                    "gradient on two copy streams), step k's output copies out beside its apply",
                       "l2": "not flushed between steps (one timed interval over all steps); the tables "
                             "exceed L2"}
         rc = tbe.tbe_get_error(h)
