@@ -368,9 +368,12 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
     grad = workloads.make_grad(cfg, dev, specs)
     T, B, N = len(specs), cfg.B, batch.N
     length_order = wants_length_order(specs, args.length_order)
+    # the small tables' forward: the histogram path where the workload
+    # prescribes it (auto), else the library's default (the gather)
+    histogram = cfg.histogram_forward if args.histogram == "auto" else args.histogram == "on"
     flags = (tbe.TBE_FLAG_NO_HISTOGRAM if args.no_histogram else 0) | (
         tbe.TBE_FLAG_SORTED_BACKWARD if args.sorted_backward else 0) | (
-        tbe.TBE_FLAG_FORCE_HISTOGRAM if args.histogram else 0) | (
+        tbe.TBE_FLAG_FORCE_HISTOGRAM if histogram else 0) | (
         tbe.TBE_FLAG_LENGTH_ORDER if length_order else 0)
     h = tbe.tbe_create(tables, cfg.pooling, flags)
     ws = tbe.make_workspace(h, N, B, dev)
@@ -547,6 +550,7 @@ def measure(tbe, cfg_id, args, dev, clk, headline):
                    "parallelism": f"replicas x{world}",
                    "launch": "CUDA graph replay" if args.graph else "stream launches",
                    "bag_order": "by length (TBE_FLAG_LENGTH_ORDER)" if length_order else "index order",
+                   "small_table_forward": "tensor-core histogram" if histogram else "gather",
                    "l2": "flushed (256 MiB write) before every step, outside the timed interval"},
         "fwd": {"lookups_per_s": N / (brk["forward"] / 1e3),
                 "gbs": nbytes["forward"] / (brk["forward"] / 1e3) / 1e9,
@@ -777,8 +781,9 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-histogram", action="store_true",
                    help="no tensor-core path for small tables (gather forward, sorted backward)")
-    p.add_argument("--histogram", action="store_true",
-                   help="small tables' forward on the tensor-core histogram path")
+    p.add_argument("--histogram", choices=["auto", "on", "off"], default="auto",
+                   help="small tables' forward on the tensor-core histogram path (TBE_FLAG_FORCE_HISTOGRAM); "
+                        "auto: where the workload prescribes it")
     p.add_argument("--length-order", choices=["auto", "on", "off"], default="auto",
                    help="forward bags pooled in order of length (TBE_FLAG_LENGTH_ORDER); auto: for "
                         "workloads whose bag lengths are drawn uniformly over a range spanning 4x or more")

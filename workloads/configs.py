@@ -56,6 +56,9 @@ class WorkloadConfig:
     rows_div: int = 1
     rows_min: int = 1
     description: str = ""
+    # the workload prescribes the tensor-core histogram forward for its small
+    # tables
+    histogram_forward: bool = False
 
     def scaled(self, B: int, rows_div: int = 1, rows_min: int = 64) -> "WorkloadConfig":
         """Same laws, fewer bags and (optionally) fewer rows per table."""
@@ -130,7 +133,9 @@ CONFIGS = {
                      + [TableSpec(20_000_000, 128, "f32", ("uniform", 1, 64), ("uniform",))]),
         description="T=64 fp16 tables of 512 rows, dim 64, plus one fp32 table of 20M "
                     "rows, dim 128, B=32768, pooling factor uniform in [1,64], uniform "
-                    "indices, weights U(0,1), sum pooling, SGD",
+                    "indices, weights U(0,1), sum pooling, SGD; the small tables take the "
+                    "histogram x table tensor-core forward",
+        histogram_forward=True,
     ),
 }
 
