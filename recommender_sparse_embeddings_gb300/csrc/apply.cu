@@ -891,8 +891,8 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 
 // All work of one backward class (table dtype DT, row shape CODE), table by
 // table in key order: each class table's long-run chunks (one consecutive
-// range cstart[t] .. cstart[t+1]), then its short-run batches of kBatchRows
-// distinct keys.  Neighbouring work items thus read gradient columns of the
+// range cstart[t] .. cstart[t+1]), then its short-run batches of kb (16 or
+// kBatchRows) distinct keys.  Neighbouring work items thus read gradient columns of the
 // same table, which keeps them in L2.  Warps take items one at a time from an
 // atomic counter, so no warp idles while work is left; the last warp to
 // finish resets the counter, so apply can run again on the same prepared
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
         const uint32_t cs = tmin<uint32_t>(__ldg(ws.cstart + t), nchunks);
         const uint32_t ce = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.cstart + t + 1), cs), nchunks);
         if (j < ce - cs) {
-            // one 256-lookup chunk of a long run of this table
+            // one chunk of a long run of this table
             const uint32_t g = cs + j;
             const uint2 e = __ldg(ws.chunk_info + g);
             const uint32_t u = e.x, g0 = e.y;
