@@ -239,9 +239,9 @@ int tbe_forward_prepare(tbe_handle* h, const void* indices, const void* offsets,
  * s_i * grad_out[bag_i, Doff_t : Doff_t+dim_t] in fp32 (runs of fewer than 256
  * lookups stream through one warp; longer runs are split into chunks of 256
  * to 1024 lookups, by batch size, whose partial sums are added in a fixed
- * order), then applies the
- * optimizer once to that row.  grad_out: device fp32 [batch_size, sum of
- * dims].  num_indices and batch_size must equal the prepare call's.  When
+ * order), then applies the optimizer once to that row.  grad_out: device
+ * fp32 [batch_size, sum of dims].  num_indices and batch_size must equal the
+ * prepare call's.  When
  * the handle's tables fall into more than one backward class (dtype x row
  * shape), the class kernels run on side streams owned by the handle that
  * start after the work already queued on `stream`, and `stream` waits for
