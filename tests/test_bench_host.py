@@ -93,3 +93,20 @@ def test_reference_arm_prints_contract_line(capsys):
     assert line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_length_order_rule_follows_the_length_law():
+    """The bench turns the length-keyed order on only for lengths drawn
+    uniformly over a wide range (workload 5), and --length-order on|off
+    overrides it."""
+    for cid, want in [(1, False), (2, False), (3, False), (4, False), (5, True)]:
+        specs = workloads.realize_tables(workloads.get_config(cid))
+        assert bench.wants_length_order(specs, "auto") is want, cid
+        assert bench.wants_length_order(specs, "on") is True
+        assert bench.wants_length_order(specs, "off") is False
+
+
+def test_histogram_forward_only_where_a_workload_prescribes_it():
+    assert [workloads.get_config(c).histogram_forward for c in (1, 2, 3, 4, 5)] == [False] * 4 + [True]
+    # shrunk parity variants keep the prescription
+    assert workloads.get_config(5).scaled(B=160, rows_div=1000, rows_min=512).histogram_forward
