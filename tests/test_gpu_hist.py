@@ -475,3 +475,28 @@ def test_dense_and_sorted_backward_agree_on_the_histogram_workload():
         assert tbe.tbe_get_error(h) == tbe.TBE_OK
         assert_tables_match(tables, ref_tabs, before, touched, what=f"workload 5 flags={flags}")
         h.close()
+
+
+@pytest.mark.parametrize("pooling,weighted", [("sum", True), ("mean", False)])
+def test_histogram_forward_with_length_order(pooling, weighted):
+    """TBE_FLAG_LENGTH_ORDER and the histogram forward on one handle (the
+    order applies to the gathered tables; the histogram tiles keep index
+    order).  Lengths 0..90 (empty bags included), several tables of both
+    16-bit dtypes, B not a multiple of the 64-bag tile: the result matches
+    the oracle within the histogram allowance, with and without the flag."""
+    g = torch.Generator().manual_seed(21)
+    specs = [(512, 64, torch.float16), (300, 32, torch.float16), (512, 64, torch.bfloat16)]
+    tables = [(torch.randn((r, d), generator=g) * 0.01).to(dt).to(DEV) for r, d, dt in specs]
+    B = 1000
+    rng = np.random.default_rng(22)
+    lengths = rng.integers(0, 91, len(specs) * B)
+    ind = torch.tensor(np.concatenate([rng.integers(0, specs[t][0], lengths[t * B + b])
+                                       for t in range(len(specs)) for b in range(B)]), dtype=torch.int64)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int64)
+    w = torch.rand(ind.numel(), generator=g) if weighted else None
+    flags = tbe.TBE_FLAG_FORCE_HISTOGRAM
+    out_o, paths = run_hist(tables, ind, off, B, w, pooling, flags | tbe.TBE_FLAG_LENGTH_ORDER)
+    assert paths == ["histogram"] * 3
+    out_i, _ = run_hist(tables, ind, off, B, w, pooling, flags)
+    check_hist(out_o, tables, ind, off, B, w, pooling, what="histogram, length order")
+    check_hist(out_i, tables, ind, off, B, w, pooling, what="histogram, index order")
