@@ -144,16 +144,18 @@ typedef struct tbe_handle tbe_handle;
 
 /* Byte offsets, inside a backward workspace, of the arrays the preparation
  * step (transpose, sort, run-length encoding) leaves there.  All arrays are
- * uint32.  sorted_keys/sorted_pos: Ns entries (key = rowbase_t + row, or
- * sum-of-rows for a skipped lookup; pos = the lookup's position in indices),
- * stably sorted by key, where Ns = N, or, when the handle has dense-backward
+ * uint32.  sorted_keys/sorted_vals: Ns entries (key = rowbase_t + row, or
+ * sum-of-rows for a skipped lookup; val = the lookup's position in indices
+ * when the batch has per-sample weights or mean pooling, else its flat bag
+ * t*B + b), stably sorted by key (equal keys keep ascending positions, hence
+ * ascending bags), where Ns = N, or, when the handle has dense-backward
  * tables (histogram tables, unless TBE_FLAG_SORTED_BACKWARD), the number of
  * lookups of the other tables: a dense table's lookups are not sorted.
  * uniq: the distinct keys ascending; runstart: the first sorted slot of each
  * (runstart[U] = Ns); num_unique: one entry, U. */
 typedef struct {
     uint64_t sorted_keys;
-    uint64_t sorted_pos;
+    uint64_t sorted_vals;
     uint64_t uniq;
     uint64_t runstart;
     uint64_t num_unique;

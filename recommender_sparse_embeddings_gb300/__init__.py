@@ -63,7 +63,7 @@ class _Optimizer(ctypes.Structure):
 
 
 class WorkspaceLayout(ctypes.Structure):
-    _fields_ = [("sorted_keys", ctypes.c_uint64), ("sorted_pos", ctypes.c_uint64),
+    _fields_ = [("sorted_keys", ctypes.c_uint64), ("sorted_vals", ctypes.c_uint64),
                 ("uniq", ctypes.c_uint64), ("runstart", ctypes.c_uint64),
                 ("num_unique", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
 

@@ -661,7 +661,7 @@ int tbe_backward_workspace_layout(const tbe_handle* h, int64_t num_indices, int3
     const Layout L = make_layout(h, num_indices, batch_size, kLayoutWithScale);
     const bool odd = h->passes % 2 == 1;
     out->sorted_keys = odd ? L.keys1 : L.keys0;
-    out->sorted_pos = odd ? L.vals1 : L.vals0;
+    out->sorted_vals = odd ? L.vals1 : L.vals0;
     out->uniq = L.uniq;
     out->runstart = L.runstart;
     out->num_unique = L.counters + sizeof(uint32_t) * CTR_U;

@@ -12,9 +12,15 @@
 // batch size), then batches of up to kBatchRows consecutive distinct keys.
 // Warps take work items from a per-class atomic counter.
 //
+// A sorted slot's value is the lookup's position when the batch has
+// per-lookup scales (weights or mean pooling): its bag and scale are then
+// read by position.  Without scales the sort carries the flat bag itself,
+// which spares a random 4-byte read per lookup (from an N-entry array that
+// on large batches does not stay in L2).
+//
 //  Short runs (fewer than kLongRun lookups), "streaming": a warp splits its
 //    batch into pieces of at most R keys and walks each piece's sorted lookups
-//    as one stream: positions, bags and scales are fetched 32 lookups at a
+//    as one stream: sorted values, bags and scales are fetched 32 lookups at a
 //    time one chunk ahead, gradient rows several at a time, and each lookup is
 //    added to its key's sum.  The piece's table rows are read before the
 //    stream starts so the read overlaps the gradient gather; after the stream
@@ -28,9 +34,9 @@
 //  Long runs, "accumulate": a warp sums one chunk of the run.  Every lane
 //    takes the same lookup and holds VW = dim/32 consecutive columns, so one
 //    load instruction reads a whole gradient row; G rows are loaded per step
-//    (8 for dim <= 128, 2 for dim 256), and the chunk's positions, bags and
-//    scales stream in 32 at a time, the bags and scales one window ahead and
-//    the positions two, so the gather never waits on its own metadata.  Each
+//    (8 for dim <= 128, 2 for dim 256), and the chunk's sorted values, bags
+//    and scales stream in 32 at a time, the bags and scales one window ahead
+//    and the values two, so the gather never waits on its own metadata.  Each
 //    step's G products are summed in fp32 (packed two-wide FMAs) and the
 //    step sums added with compensated (Kahan) addition (consecutive lookups
 //    of a long run often share a bag, so longer plain sums would round
@@ -217,16 +223,16 @@ struct ShortTune {
     static constexpr int R = R0 > 8 ? 8 : (R0 < 1 ? 1 : R0);
 };
 
-__device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ Meta load_meta(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                           uint32_t w, uint32_t Eend, int64_t tB, int lane) {
     const uint32_t i = w + lane;
     Meta m{-1, 1.f};
     if (i < Eend) {
-        const uint32_t pos = __ldg(pos_sorted + i);
-        if (pos < (uint32_t)a.N) {
-            const int64_t bag = (int64_t)__ldg(ws.bag + pos);
-            if (bag >= tB && bag < tB + a.B) m.b = (int)(bag - tB);
-            if (a.has_scale) m.s = __ldg(ws.scale + pos);
+        const uint32_t v = __ldg(sorted_val + i);  // position with scales, else the flat bag
+        if (!a.has_scale || v < (uint32_t)a.N) {
+            const uint32_t rel = (a.has_scale ? __ldg(ws.bag + v) : v) - (uint32_t)tB;
+            if (rel < (uint32_t)a.B) m.b = (int)rel;
+            if (a.has_scale) m.s = __ldg(ws.scale + v);
         }
     }
     return m;
@@ -250,7 +256,7 @@ struct MetaWindow {
 // and each is added to its key's sum; the groups' sums are added up and each
 // key gets its optimizer step.
 template <int DT, int CODE>
-__device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                                 const TableDesc& td, int t, uint32_t rs, uint32_t key, float mstate,
                                                 uint32_t rows, int lane) {
     using Sh = ShapeOf<CODE>;
@@ -296,8 +302,8 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
         // window at the piece's first lookup
         if (win.w0 == 0xffffffffu || E0 < win.w0 || E0 >= win.w0 + 64) {
             win.w0 = E0;
-            win.m0 = load_meta(a, ws, pos_sorted, E0, Eend, tB, lane);
-            win.m1 = load_meta(a, ws, pos_sorted, E0 + 32, Eend, tB, lane);
+            win.m0 = load_meta(a, ws, sorted_val, E0, Eend, tB, lane);
+            win.m1 = load_meta(a, ws, sorted_val, E0 + 32, Eend, tB, lane);
         }
         float acc[R][NB][VW];
 #pragma unroll
@@ -311,7 +317,7 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
             while (i >= win.w0 + 32) {  // slide: keep [w0, w0 + 64) ahead of i
                 win.m0 = win.m1;
                 win.w0 += 32;
-                win.m1 = load_meta(a, ws, pos_sorted, win.w0 + 32, Eend, tB, lane);
+                win.m1 = load_meta(a, ws, sorted_val, win.w0 + 32, Eend, tB, lane);
             }
             int sl[GROUP];
             float ss[GROUP];
@@ -383,7 +389,7 @@ __device__ __forceinline__ void short_batch_vec(const ApplyArgs& a, const Worksp
 // column moves, so it makes two passes.  With partial_src, the gradient is
 // the ordered sum of nchunks partial rows instead of the lookups [s0, s1).
 template <int DT>
-__device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                             const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
                                             const float* partial_src, uint32_t nchunks, int lane) {
     const int D = td.dim;
@@ -412,11 +418,11 @@ __device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace&
                     }
             } else {
                 for (uint32_t i = s0; i < s1; ++i) {
-                    const uint32_t pos = __ldg(pos_sorted + i);
-                    if (pos >= (uint32_t)a.N) continue;
-                    const int64_t bag = __ldg(ws.bag + pos);
+                    const uint32_t v = __ldg(sorted_val + i);  // position with scales, else the flat bag
+                    if (a.has_scale && v >= (uint32_t)a.N) continue;
+                    const int64_t bag = a.has_scale ? (int64_t)__ldg(ws.bag + v) : (int64_t)v;
                     if (bag < tB || bag >= tB + a.B) continue;
-                    const float s = a.has_scale ? __ldg(ws.scale + pos) : 1.f;
+                    const float s = a.has_scale ? __ldg(ws.scale + v) : 1.f;
                     const float* grow = a.grad + (bag - tB) * a.total_d + td.doff;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -448,7 +454,7 @@ __device__ __forceinline__ void generic_row(const ApplyArgs& a, const Workspace&
 
 // One batch: distinct keys [u0, u0 + n) of table t (n <= kBatchRows).
 template <int DT, int CODE>
-__device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                             const TableDesc& td, int t, uint32_t u0, uint32_t n, int lane) {
     const uint32_t N = (uint32_t)a.N;
     // lane l <= n: first sorted slot of batch row l (lane n: end of the last
@@ -472,10 +478,10 @@ __device__ __forceinline__ void short_batch(const ApplyArgs& a, const Workspace&
             const uint32_t kr = __shfl_sync(0xffffffffu, key, r);
             const uint32_t s0 = __shfl_sync(0xffffffffu, rs, r);
             const uint32_t s1 = __shfl_sync(0xffffffffu, rs, r + 1);
-            generic_row<DT>(a, ws, pos_sorted, td, t, kr, s0, s1, nullptr, 0, lane);
+            generic_row<DT>(a, ws, sorted_val, td, t, kr, s0, s1, nullptr, 0, lane);
         }
     } else if (rows) {
-        short_batch_vec<DT, CODE>(a, ws, pos_sorted, td, t, rs, key, mstate, rows, lane);
+        short_batch_vec<DT, CODE>(a, ws, sorted_val, td, t, rs, key, mstate, rows, lane);
     }
 }
 
@@ -660,49 +666,55 @@ __device__ __forceinline__ float optimizer_step_w(const ApplyArgs& a, int dim, c
 
 // ------------------------------------------------- streaming the lookups
 
-// Raw metadata of the sorted slot a lane looks ahead at: its flat bag
-// (0xffffffff past the stream or for an invalid position) and its scale.
+// Raw metadata of the sorted slot a lane looks ahead at, from its sorted
+// value v: its flat bag (0xffffffff past the stream or for an invalid
+// position) and its scale.  With scales (HS) v is a position and both are
+// looked up; without, v is the bag itself.
 template <bool HS>
-__device__ __forceinline__ void meta_issue(const ApplyArgs& a, const Workspace& ws, uint32_t pos, uint32_t& bag,
+__device__ __forceinline__ void meta_issue(const ApplyArgs& a, const Workspace& ws, uint32_t v, uint32_t& bag,
                                            float& s) {
     bag = 0xffffffffu;
     s = 0.f;
-    if (pos < (uint32_t)a.N) {
-        bag = __ldg(ws.bag + pos);
-        if constexpr (HS) s = __ldg(ws.scale + pos);
+    if constexpr (HS) {
+        if (v < (uint32_t)a.N) {
+            bag = __ldg(ws.bag + v);
+            s = __ldg(ws.scale + v);
+        }
+    } else {
+        bag = v;
     }
 }
 
-__device__ __forceinline__ uint32_t pos_issue(const uint32_t* pos_sorted, uint32_t i, uint32_t end) {
-    return i < end ? __ldg(pos_sorted + i) : 0xffffffffu;
+__device__ __forceinline__ uint32_t val_issue(const uint32_t* sorted_val, uint32_t i, uint32_t end) {
+    return i < end ? __ldg(sorted_val + i) : 0xffffffffu;
 }
 
 // The slots [E0, E1) of one table t as a stream of 32-slot windows.  Lane k
 // holds, for the current window w, cb = bag row of slot w + k within the
 // table (-1 if none) and cs = its scale; the next window's raw bag and scale
-// and the positions of the one after are in flight meanwhile.
+// and the sorted values of the one after are in flight meanwhile.
 template <bool HS>
 struct Stream {
-    uint32_t p;     // positions of window w + 64
+    uint32_t p;     // sorted values of window w + 64
     uint32_t nbag;  // raw bags of window w + 32
     float ns;       // raw scales of window w + 32
     int cb;
     float cs;
 
-    __device__ __forceinline__ void start(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+    __device__ __forceinline__ void start(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                           uint32_t E0, uint32_t E1, int lane) {
-        const uint32_t p0 = pos_issue(pos_sorted, E0 + lane, E1);
+        const uint32_t p0 = val_issue(sorted_val, E0 + lane, E1);
         meta_issue<HS>(a, ws, p0, nbag, ns);
-        p = pos_issue(pos_sorted, E0 + 32 + lane, E1);
+        p = val_issue(sorted_val, E0 + 32 + lane, E1);
     }
     // Makes window w current and issues the loads of the two after it.
-    __device__ __forceinline__ void advance(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+    __device__ __forceinline__ void advance(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                             uint32_t w, uint32_t E1, uint32_t tB, int lane) {
         const uint32_t rel = nbag - tB;
         cb = rel < (uint32_t)a.B ? (int)rel : -1;
         cs = cb < 0 ? 0.f : (HS ? ns : 1.f);
         meta_issue<HS>(a, ws, p, nbag, ns);
-        p = pos_issue(pos_sorted, w + 64 + lane, E1);
+        p = val_issue(sorted_val, w + 64 + lane, E1);
     }
 };
 
@@ -737,7 +749,7 @@ __device__ __forceinline__ float step_scale(float cs, int k) { return __shfl_syn
 // bag, so sums over many of them would grow and round coarsely); written to
 // part_row.
 template <int CODE, bool HS>
-__device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                                const TableDesc& td, int t, uint32_t s0, uint32_t s1, float* part_row,
                                                int lane) {
     using V = VecShape<CODE>;
@@ -760,9 +772,9 @@ __device__ __forceinline__ void long_chunk_vec(const ApplyArgs& a, const Workspa
         }
     };
     Stream<HS> st;
-    st.start(a, ws, pos_sorted, s0, s1, lane);
+    st.start(a, ws, sorted_val, s0, s1, lane);
     for (uint32_t w = s0; w < s1; w += 32) {
-        st.advance(a, ws, pos_sorted, w, s1, tB, lane);
+        st.advance(a, ws, sorted_val, w, s1, tB, lane);
         const int n = (int)tmin<uint32_t>(32u, s1 - w);
         if (n == 32 && __all_sync(0xffffffffu, st.cb >= 0)) {
 #pragma unroll 1
@@ -833,7 +845,7 @@ __device__ __forceinline__ void long_combine_vec(const ApplyArgs& a, const Table
 
 
 template <int DT, int CODE>
-__device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* pos_sorted,
+__device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& ws, const uint32_t* sorted_val,
                                           const TableDesc& td, int t, uint32_t key, uint32_t s0, uint32_t s1,
                                           uint32_t chunk, uint32_t base, uint32_t nc, int lane) {
     float* part_row = ws.partial + (int64_t)chunk * a.part_stride;
@@ -846,11 +858,11 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = Kahan{0.f, 0.f};
             for (uint32_t i = s0; i < s1; ++i) {
-                const uint32_t pos = __ldg(pos_sorted + i);
-                if (pos >= (uint32_t)a.N) continue;
-                const int64_t bag = __ldg(ws.bag + pos);
+                const uint32_t v = __ldg(sorted_val + i);  // position with scales, else the flat bag
+                if (a.has_scale && v >= (uint32_t)a.N) continue;
+                const int64_t bag = a.has_scale ? (int64_t)__ldg(ws.bag + v) : (int64_t)v;
                 if (bag < tB || bag >= tB + a.B) continue;
-                const float s = a.has_scale ? __ldg(ws.scale + pos) : 1.f;
+                const float s = a.has_scale ? __ldg(ws.scale + v) : 1.f;
                 const float* grow = a.grad + (bag - tB) * a.total_d + td.doff;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -866,9 +878,9 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
         }
     } else {
         if (a.has_scale)
-            long_chunk_vec<CODE, true>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
+            long_chunk_vec<CODE, true>(a, ws, sorted_val, td, t, s0, s1, part_row, lane);
         else
-            long_chunk_vec<CODE, false>(a, ws, pos_sorted, td, t, s0, s1, part_row, lane);
+            long_chunk_vec<CODE, false>(a, ws, sorted_val, td, t, s0, s1, part_row, lane);
     }
     // 2) the warp that finishes a run's last chunk combines all of them
     __threadfence();
@@ -880,7 +892,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
     __threadfence();
     const float* part0 = ws.partial + (int64_t)base * a.part_stride;
     if constexpr (CODE == SHAPE_GENERIC)
-        generic_row<DT>(a, ws, pos_sorted, td, t, key, 0, 0, part0, nc, lane);
+        generic_row<DT>(a, ws, sorted_val, td, t, key, 0, 0, part0, nc, lane);
     else
         long_combine_vec<DT, CODE>(a, td, key, part0, nc, lane);
     // every chunk of this run has been counted: reset for the next apply call
@@ -898,7 +910,7 @@ __device__ __forceinline__ void long_item(const ApplyArgs& a, const Workspace& w
 // finish resets the counter, so apply can run again on the same prepared
 // workspace.
 template <int DT, int CODE>
-__global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* pos_sorted) {
+__global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(ApplyArgs a, Workspace ws, const uint32_t* sorted_val) {
     chain_wait();  // returns at once unless launched chained
     __shared__ uint32_t s_ibase[kMaxTables + 1];  // first work item of each class table
     __shared__ uint32_t s_warp[8];
@@ -980,13 +992,13 @@ __global__ void __launch_bounds__(256, kApplyCtasPerSm) apply_class_kernel(Apply
                 continue;
             const uint32_t s0 = r0 + jc * chunk;
             const uint32_t s1 = tmin<uint32_t>(s0 + chunk, r1);
-            long_item<DT, CODE>(a, ws, pos_sorted, td, t, key, s0, s1, g, g0, nc, lane);
+            long_item<DT, CODE>(a, ws, sorted_val, td, t, key, s0, s1, g, g0, nc, lane);
         } else {
             const uint32_t us = tmin<uint32_t>(__ldg(ws.ustart + t), U);
             const uint32_t ue = tmin<uint32_t>(tmax<uint32_t>(__ldg(ws.ustart + t + 1), us), U);
             const uint32_t u0 = us + (j - (ce - cs)) * kb;
             if (u0 >= ue) continue;
-            short_batch<DT, CODE>(a, ws, pos_sorted, td, t, u0, tmin<uint32_t>(kb, ue - u0), lane);
+            short_batch<DT, CODE>(a, ws, sorted_val, td, t, u0, tmin<uint32_t>(kb, ue - u0), lane);
         }
     }
     // every warp has taken its last item: the last one to leave resets the
@@ -1027,7 +1039,7 @@ cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32
                          cudaStream_t s, const cudaStream_t* streams, cudaEvent_t ev_fork,
                          const cudaEvent_t* ev_join) {
     if (a_in.N == 0) return cudaSuccess;
-    const uint32_t* pos_sorted = ws.vals[ws.sorted_buf];
+    const uint32_t* sorted_val = ws.vals[ws.sorted_buf];
     const unsigned grid = (unsigned)(a_in.num_sms * kApplyCtasPerSm);
     int present = dense ? 1 : 0;  // the dense tables' work counts as one more launch group
     for (int cls = 0; cls < kNumClasses; ++cls) present += class_count[cls] > 0;
@@ -1059,11 +1071,11 @@ cudaError_t launch_apply(const ApplyArgs& a_in, const Workspace& ws, const int32
         ++k;
         cudaError_t e;
         if (dt == DT_F32)
-            e = launch_dtype<DT_F32>(a, ws, pos_sorted, code, grid, cs, chained);
+            e = launch_dtype<DT_F32>(a, ws, sorted_val, code, grid, cs, chained);
         else if (dt == DT_F16)
-            e = launch_dtype<DT_F16>(a, ws, pos_sorted, code, grid, cs, chained);
+            e = launch_dtype<DT_F16>(a, ws, sorted_val, code, grid, cs, chained);
         else
-            e = launch_dtype<DT_BF16>(a, ws, pos_sorted, code, grid, cs, chained);
+            e = launch_dtype<DT_BF16>(a, ws, sorted_val, code, grid, cs, chained);
         if (e != cudaSuccess) return e;
     }
     if (fork) {

@@ -365,13 +365,17 @@ __global__ void __launch_bounds__(256, 3) keys_kernel(PrepArgs a, Workspace ws) 
                     // key (and no bag: the dense backward walks bag offsets)
                     ws.hrow[p] = in_range ? (uint16_t)xv[k] : (uint16_t)0xffffu;
                 } else {
-                    ws.bag[p] = bag;
                     const uint32_t key = in_range ? rowbase + (uint32_t)xv[k] : a.total_rows;
                     keyk = key;
                     // malformed offsets could send a slot out of range: clamp
                     const uint32_t c = ws.compact ? tmin<uint32_t>(p + shift, ns - 1u) : p;
                     ws.keys[0][c] = key;
-                    if (ws.compact) ws.vals[0][c] = p;
+                    if (!ws.scale) {
+                        ws.vals[0][c] = bag;  // no scale to look up: the sort carries the bag itself
+                    } else {
+                        ws.bag[p] = bag;
+                        if (ws.compact) ws.vals[0][c] = p;
+                    }
                 }
                 if (ws.scale) {
                     float sc = a.weights ? s_w[li] : 1.f;
@@ -942,8 +946,10 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
     int cur = 0;
     for (int p = 0; p < ws.passes; ++p) {
         // the first pass numbers the positions itself unless the keys kernel
-        // wrote them (compacted keys) and counted its tiles' digits otherwise
-        const bool gen = p == 0 && !a.compact;
+        // wrote the values (compacted keys, or bags when there is no scale);
+        // the keys kernel counted the first pass's digits unless compacted
+        const bool counted = p == 0 && !a.compact;
+        const bool gen = counted && ws.scale != nullptr;
         const uint32_t* kin = ws.keys[cur];
         const uint32_t* vin = gen ? nullptr : ws.vals[cur];
         uint32_t* kout = ws.keys[cur ^ 1];
@@ -952,11 +958,11 @@ cudaError_t launch_prepare(const PrepArgs& a, Workspace& ws, cudaStream_t s) {
         const int shift = p * ws.digit_bits;
         const uint32_t nt = (uint32_t)tiles, n = (uint32_t)a.N;
         if (ws.digit_bits == 9) {
-            if (!gen) launch_chained(upsweep_kernel<9>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
+            if (!counted) launch_chained(upsweep_kernel<9>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<9>(ws.tcount, hp, nt, n, nsp, s);
             launch_downsweep<9>(gen, match, tiles, s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         } else {
-            if (!gen) launch_chained(upsweep_kernel<8>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
+            if (!counted) launch_chained(upsweep_kernel<8>, dim3(ugrid), dim3(kSortThreads), s, kin, n, nsp, shift, ws.tcount, nt, hp);
             launch_scan<8>(ws.tcount, hp, nt, n, nsp, s);
             launch_downsweep<8>(gen, match, tiles, s, kin, vin, kout, vout, ws.tcount, nt, n, nsp, shift);
         }

@@ -282,8 +282,8 @@ struct Workspace {
     uint32_t* tcount;     // [1 << digit_bits][tiles]: digit counts of each tile, then digit starts
     uint32_t* tile_bag;   // [tiles]: first bag of each key tile (zeroed per call)
     uint32_t* keys[2];    // [N] ping-pong
-    uint32_t* vals[2];    // [N] ping-pong
-    uint32_t* bag;        // [N] flat bag of each position
+    uint32_t* vals[2];    // [N] ping-pong: with scale, each lookup's position; without, its flat bag
+    uint32_t* bag;        // [N] flat bag of each position (written only with scale)
     float* scale;         // [N] s_i of each position (weights and/or mean)
     uint32_t* uniq;       // [N]
     uint32_t* runstart;   // [N+1]

@@ -72,7 +72,8 @@ def test_full_size(cid):
         return ws[offset:offset + 4 * n].view(torch.int32).cpu().numpy().view(np.uint32).astype(np.int64)
 
     np.testing.assert_array_equal(u32(lay.sorted_keys, Ns), skeys)
-    np.testing.assert_array_equal(u32(lay.sorted_pos, Ns), keep[perm])
+    scaled = w is not None or cfg.pooling == "mean"  # values: positions, else flat bags
+    np.testing.assert_array_equal(u32(lay.sorted_vals, Ns), keep[perm] if scaled else bag_of[keep[perm]])
     U = int(u32(lay.num_unique, 1)[0])
     head = np.flatnonzero(np.r_[True, skeys[1:] != skeys[:-1]])
     assert U == len(head)

@@ -131,7 +131,11 @@ def check_prepare(cfg, tables, batch, flags):
     ref = oracle.sort_rle(keys[keep])
     Ns = len(keep)
     np.testing.assert_array_equal(view(lay.sorted_keys, Ns), ref["sorted_keys"])
-    np.testing.assert_array_equal(view(lay.sorted_pos, Ns), keep[ref["sorted_pos"]])
+    # the sorted values: positions when the batch has scales (weights or mean
+    # pooling), else the lookups' flat bags
+    spos = keep[ref["sorted_pos"]]
+    scaled = batch.weights is not None or cfg.pooling == "mean"
+    np.testing.assert_array_equal(view(lay.sorted_vals, Ns), spos if scaled else bag[spos])
     assert U == len(ref["uniq"])
     np.testing.assert_array_equal(view(lay.uniq, U), ref["uniq"])
     rs = view(lay.runstart, U + 1)
