@@ -424,6 +424,14 @@ def test_dense_backward_out_of_range_is_skipped(index_dtype):
     _dense_case(specs, 130, "sum", False, "sgd", seed=9, oob_table=0, index_dtype=index_dtype)
 
 
+def test_dense_backward_forced_1024_rows():
+    """TBE_FLAG_FORCE_HISTOGRAM admits tables of up to 1024 rows to the dense
+    backward: at dim 128 a table spans four row groups of CTAs (two 128-row
+    M tiles each), next to a 1000 x 64 table and a sorted-path table."""
+    specs = [(1024, 128, torch.bfloat16), (1000, 64, torch.float16), (4000, 32, torch.float32)]
+    _dense_case(specs, 200, "sum", True, "sgd", flags=tbe.TBE_FLAG_FORCE_HISTOGRAM, seed=31)
+
+
 def test_dense_backward_applies_twice():
     """prepare once, apply twice: the shared-memory sums start from zero each
     time (the accumulators are cleared per apply).  Each apply is checked as
