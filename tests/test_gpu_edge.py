@@ -77,6 +77,28 @@ def test_run_length_threshold(optimizer, dtype, dim):
     run_backward_and_compare(tables, ind, off, B, grad, optimizer, what=f"threshold {dtype} {dim}")
 
 
+@pytest.mark.parametrize("optimizer", ["sgd", "adagrad"])
+def test_sparse_batch_bag_ids_beyond_the_lookup_count(optimizer):
+    """Without per-lookup scales the sort carries each lookup's flat bag,
+    and a flat bag id can exceed the number of lookups: here 2 x 6000 bags
+    hold 700 lookups, all in bags past id 700 (the second table's bags are
+    5999 and up), one row hit 400 times (a long run) and others once."""
+    rng = np.random.default_rng(17)
+    B = 6000
+    tabs = [[[] for _ in range(B)] for _ in range(2)]
+    for k in range(400):  # table 0: row 5 in bags 1000..1399, a long run
+        tabs[0][1000 + k].append(5)
+    for b in rng.choice(np.arange(2000, B), size=150, replace=False):
+        tabs[0][int(b)].append(int(rng.integers(0, 900)))
+    for b in rng.choice(np.arange(0, B), size=150, replace=False):
+        tabs[1][int(b)].append(int(rng.integers(0, 700)))
+    ind, off, B = csr(tabs)
+    assert ind.numel() == 700 and 2 * B > 8 * ind.numel()
+    tables = make_tables([(900, 128, torch.float32), (700, 64, torch.bfloat16)], seed=18)
+    grad = torch.randn((B, 192), generator=torch.Generator().manual_seed(19))
+    run_backward_and_compare(tables, ind, off, B, grad, optimizer, what=f"sparse batch {optimizer}")
+
+
 def test_prepared_workspace_applies_twice():
     """prepare once, apply twice (the long-run completion counts reset)."""
     rng = np.random.default_rng(3)
