@@ -4,11 +4,13 @@
 //
 //  1. bag_marks_kernel + keys_kernel: one (table,row) key per lookup, key =
 //     rowbase_t + idx (or the sentinel sum-of-rows for an index out of
-//     range), the flat bag of each position, the lookup's scale s_i when
-//     weights or mean pooling apply, and the first radix pass's digit counts.
+//     range), and its sort value: with per-lookup scales (weights or mean
+//     pooling) the position, and the bag and scale s_i by position; without,
+//     the flat bag itself (the apply then needs nothing else).  Also the
+//     first radix pass's digit counts.
 //     Positions are tiled evenly (the first bag of each tile is marked by a
 //     pass over the bags), so bag lengths do not unbalance the work.
-//  2. a stable LSD radix sort of (key, position), 8- or 9-bit digits,
+//  2. a stable LSD radix sort of (key, value), 8- or 9-bit digits,
 //     reduce-then-scan per pass: per-tile digit counts and the pass's digit
 //     histogram (the keys kernel gives the first pass's, the upsweep the
 //     others), a scan per digit over the tiles, and a scatter that
@@ -530,8 +532,8 @@ __device__ __forceinline__ uint32_t lanes_with_digit(uint32_t d) {
 // Stable scatter of one tile by digit (one CTA per tile): ranks the keys in
 // input order (lanes_with_digit + per-warp counters), places them by digit in
 // shared memory and writes each digit's run to its global start from the
-// scan.  The first pass generates the values (positions) instead of
-// reading them.
+// scan.  FIRST: the values are the positions, generated instead of read
+// (the first pass of a batch with per-lookup scales and no compaction).
 template <bool FIRST, int RB, bool MATCH>
 __global__ void __launch_bounds__(kSortThreads, MATCH ? 4 : 3) downsweep_kernel(const uint32_t* __restrict__ keys_in,
                                                                     const uint32_t* __restrict__ vals_in,
