@@ -199,8 +199,9 @@ int tbe_forward(tbe_handle* h, const void* indices, const void* offsets, int32_t
 /* ---------------------------------------------------------------- backward */
 
 /* Bytes of device workspace the backward calls need for this batch shape:
- * the arrays of the backward's preparation steps (one key, position, bag and
- * scale per lookup; the sort's ping-pong buffers and digit counts; distinct
+ * the arrays of the backward's preparation steps (one key and one sort value
+ * per lookup, and room for each lookup's bag and scale, which batches with
+ * per-lookup scales use; the sort's ping-pong buffers and digit counts; distinct
  * keys and run starts; partial sums of the runs of at least 256 lookups), as
  * kimbodo "Kimbodo Engineering Perspective" (transpose, sort, run-length
  * encoding) and "What Happened" (separate accumulation for long runs) define
