@@ -63,6 +63,37 @@ def test_prepare_sort_and_rle_bit_exact(cid, flags):
     check_prepare(cfg, tables, batch, flags)
 
 
+@pytest.mark.parametrize("pooling,weighted", [("sum", False), ("sum", True), ("mean", False)])
+def test_prepare_compacted_keys_values(pooling, weighted):
+    """A small fp16 table takes the dense backward, so only the other two
+    tables' keys are sorted (compacted); without per-lookup scales the sort
+    carries their flat bags, with weights or mean pooling their positions.
+    Bags of 0..50 lookups, a few hot rows for runs past 256."""
+    rng = np.random.default_rng(23)
+    specs = [(5000, 32, torch.float32), (512, 64, torch.float16), (70000, 64, torch.bfloat16)]
+    tables = [torch.zeros((r, d), dtype=dt, device=DEV) for r, d, dt in specs]
+    B = 3000
+    lens = rng.integers(0, 51, len(specs) * B)
+    idx = []
+    for t, (r, _, _) in enumerate(specs):
+        n = int(lens[t * B:(t + 1) * B].sum())
+        ii = rng.integers(0, r, n)
+        m = rng.random(n) < 0.1
+        ii[m] = rng.integers(0, 4)
+        idx.append(ii)
+    ind = np.concatenate(idx).astype(np.int64)
+    batch = types.SimpleNamespace(
+        indices=torch.from_numpy(ind),
+        offsets=torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)),
+        weights=torch.from_numpy(rng.random(len(ind)).astype(np.float32)) if weighted else None)
+    batch.N = len(ind)
+    cfg = types.SimpleNamespace(B=B, pooling=pooling)
+    h = tbe.tbe_create(tables, pooling)
+    assert tbe.tbe_backward_paths(h) == ["sorted", "dense", "sorted"]
+    h.close()
+    check_prepare(cfg, tables, batch, 0)
+
+
 def test_prepare_sort_bit_exact_many_waves():
     """A batch of many more 4096-key tiles than one wave of sort CTAs (three
     per SM): the downsweep then ranks by warp match instead of ballots.
