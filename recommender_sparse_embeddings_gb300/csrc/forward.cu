@@ -101,7 +101,8 @@ __device__ __forceinline__ void gather_accumulate(const uint4* __restrict__ tab,
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w[u], f[e], acc[e]);
+                        for (int e = 0; e < E; e += 2)  // packed: each half rounds like fmaf
+                            ffma2(acc[e], acc[e + 1], w[u], f[e], f[e + 1]);
                     }
                 }
             }
